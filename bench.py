@@ -1,0 +1,395 @@
+#!/usr/bin/env python3
+"""Stochastic Attention forward throughput on one GB300 (or N replicas).
+
+Workload: the long-prefill GQA shape -- batch 1, n = 32768 tokens, 32 query
+heads / 8 kv heads, head_dim 128, bf16, causal SA with w = 128, one seeded
+sigma.  One step = one sa_forward call (the whole hot path: sigma gather,
+windowed attention, sigma^-1 scatter) through the libsa C ABI.
+
+Prints ONE JSON line (rank 0).  ``value`` is device-timed tokens/s with
+inputs resident in HBM (L2 flushed between steps); ``e2e`` times the same
+call with the host->device copies of Q/K/V/sigma from pinned memory and the
+device->host copy of the output inside the timed region.  ``roofline``
+compares the kernel's algorithmic bytes per launch (Q, K, V and Y once,
+sigma once) over its CUDA-event duration with the measured HBM copy peak.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference
+implementation of this method) on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(workload="long_prefill_gqa", batch=1, seq_len=32768, num_q_heads=32,
+                num_kv_heads=8, head_dim=128, window=128, causal=True, path="sa", seed=0)
+METRIC = "SA fwd tokens/s and % roofline (bf16, n=32K, w=128, GQA 32q/8kv, d=128)"
+PROFILE = os.path.join(ROOT, "profiles", "sa_tc_kernel_long_prefill_gqa_w128.md")
+TC_SOURCE = os.path.join(ROOT, "stochastic_sliding_window_gb300", "csrc", "sa_tc.cu")
+
+_G: dict = {}  # arrays shared with forked oracle workers
+
+
+def causal_sa_pairs(n: int, window: int) -> int:
+    """Attended (query, key) pairs of causal SA in one sequence: each token
+    itself plus, of every unordered pair at permuted distance 1..h, exactly
+    one edge."""
+    h = min(window // 2, n - 1)
+    return n + sum(n - d for d in range(1, h + 1))
+
+
+def algorithmic(wl) -> tuple[int, float]:
+    b, n, hq, hkv, d = wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"], wl["head_dim"]
+    bytes_alg = 2 * b * n * d * (hq + 2 * hkv + hq) + 4 * b * n
+    flops = 4.0 * d * hq * b * causal_sa_pairs(n, wl["window"])
+    return bytes_alg, flops
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+def profiled_traffic() -> int | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (its sha256 is recorded in the summary)."""
+    try:
+        text = open(PROFILE).read()
+        src = hashlib.sha256(open(TC_SOURCE, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != src:
+        return None
+    return int(m_tr.group(1))
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def _oracle_chunk(rows):
+    import oracle
+    oracle.sa_rows(_G["q"], _G["k"], _G["v"], _G["perm"], _G["window"], _G["causal"], rows=rows)
+    return len(rows)
+
+
+def publish_oracle_inputs(case, perm, wl):
+    """Make the inputs visible to oracle workers forked after this call."""
+    _G.update(q=case.q, k=case.k, v=case.v, perm=perm, window=wl["window"], causal=wl["causal"])
+
+
+def oracle_throughput(case, perm, wl, seconds: float, pool=None, cores: int = 1) -> dict:
+    """Time the oracle on a seeded sample of query tokens (all heads of each).
+    Workers in ``pool`` must have been forked after publish_oracle_inputs."""
+    import numpy as np
+    import oracle
+    n = wl["seq_len"]
+    rng = np.random.default_rng(1)
+    calib = [(0, int(i)) for i in rng.integers(0, n, 16)]
+    t0 = time.perf_counter()
+    oracle.sa_rows(case.q, case.k, case.v, perm, wl["window"], wl["causal"], rows=calib)
+    per_row = max((time.perf_counter() - t0) / len(calib), 1e-6)
+    count = int(max(cores * 4, min(n * wl["batch"], seconds * cores / per_row)))
+    rows = [(0, int(i)) for i in rng.integers(0, n, count)]
+    chunk = max(1, count // (cores * 4))
+    chunks = [rows[i:i + chunk] for i in range(0, count, chunk)]
+    t0 = time.perf_counter()
+    if pool is None:
+        done = sum(_oracle_chunk(c) for c in chunks)
+    else:
+        done = sum(pool.map(_oracle_chunk, chunks))
+    wall = time.perf_counter() - t0
+    return dict(value=done / wall, unit="tokens/s", cores=cores, kind="oracle",
+                sample=f"{done} seeded query tokens (all {wl['num_q_heads']} heads each) of the "
+                       f"n={n} workload, fp64 NumPy oracle, {cores} worker processes",
+                seconds=wall)
+
+
+def make_pool(cores: int):
+    import multiprocessing as mp
+    # Forked before any CUDA call in this process; workers see the inputs
+    # copy-on-write.
+    return mp.get_context("fork").Pool(cores)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+# ------------------------------------------------------------------ main legs
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    from sa_synth import make_case
+    import oracle
+    wl = WORKLOAD
+    case = make_case(wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"],
+                     wl["head_dim"], wl["seed"])
+    perm = np.stack([oracle.make_perm(wl["seed"], 0, b, wl["seq_len"]) for b in range(wl["batch"])])
+    cores = len(os.sched_getaffinity(0))
+    publish_oracle_inputs(case, perm, wl)
+    pool = make_pool(cores)
+    per_step = max(0.5, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_throughput(case, perm, wl, per_step / 4, pool, cores)
+    runs = [oracle_throughput(case, perm, wl, per_step, pool, cores) for _ in range(args.steps)]
+    pool.close()
+    tokens = sum(r["value"] * r["seconds"] for r in runs)
+    secs = sum(r["seconds"] for r in runs)
+    value = tokens / secs
+    line = dict(impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=world,
+                steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * secs / args.steps,
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic",
+                config={k: wl[k] for k in ("workload", "batch", "seq_len", "num_q_heads",
+                                           "num_kv_heads", "head_dim", "window", "causal")},
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=cores, kind="oracle",
+                                  sample=runs[0]["sample"].split(",")[0] + " per step (seeded "
+                                  "sample), fp64 NumPy oracle"),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+                gpu_launches=0)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    rank, world, local = dist_env()
+    wl = WORKLOAD
+    from sa_synth import bf16_bits, make_case
+    case = make_case(wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"],
+                     wl["head_dim"], wl["seed"])
+
+    import stochastic_sliding_window_gb300 as sa
+    sa.load()
+    perm_np = sa.make_perms(wl["seed"], 0, wl["batch"], wl["seq_len"])
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = len(os.sched_getaffinity(0))
+        publish_oracle_inputs(case, perm_np.astype(np.int64), wl)
+        pool = make_pool(cores)  # before the first CUDA call
+        cpu = oracle_throughput(case, perm_np.astype(np.int64), wl, args.cpu_seconds, pool, cores)
+        pool.close()
+        pool.join()
+        cpu.pop("seconds", None)
+
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def to_dev(x):
+        return torch.from_numpy(bf16_bits(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = to_dev(case.q), to_dev(case.k), to_dev(case.v)
+    perm = torch.from_numpy(perm_np).to(dev)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        sa.sa_forward(q, k, v, perm, wl["window"], causal=wl["causal"], out=out, err=err,
+                      stream=stream)
+
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    launches_per_step = sa.last_launch_count()
+    kernel = sa.last_kernel()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_seconds:  # settle clocks before timing
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = sa.check_error(err)
+    if status != sa.SA_OK:
+        raise RuntimeError(f"device error word reports status {status}")
+
+    # end to end: pinned host buffers in, result out, copies inside the timing
+    hq = torch.from_numpy(bf16_bits(case.q).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(bf16_bits(case.k).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(bf16_bits(case.v).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hp = torch.from_numpy(perm_np).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hp))
+    d2h = hout.numel() * hout.element_size()
+    q2, k2, v2, p2, o2 = (torch.empty_like(x) for x in (q, k, v, perm, out))
+
+    def e2e_step():
+        q2.copy_(hq, non_blocking=True)
+        k2.copy_(hk, non_blocking=True)
+        v2.copy_(hv, non_blocking=True)
+        p2.copy_(hp, non_blocking=True)
+        sa.sa_forward(q2, k2, v2, p2, wl["window"], causal=wl["causal"], out=o2, err=err,
+                      stream=stream)
+        hout.copy_(o2, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
+
+    if rank != 0:
+        return 0
+    tokens = wl["batch"] * wl["seq_len"]
+    ms_per_step = total_ms / args.steps
+    value = world * tokens / (ms_per_step * 1e-3)
+    bytes_alg, flops_alg = algorithmic(wl)
+    peaks = load_peaks()
+    achieved = bytes_alg / (ms_per_step * 1e-3) / 1e9
+    traffic = profiled_traffic()
+    line = dict(
+        metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="bf16", data="synthetic",
+        config={k: wl[k] for k in ("workload", "batch", "seq_len", "num_q_heads", "num_kv_heads",
+                                   "head_dim", "window", "causal", "path")}
+        | dict(l2="flushed between steps (256 MB write); inputs 671 MB > L2",
+               kernel="tcgen05" if kernel == sa.KERNEL_TCGEN05 else "simt",
+               parallelism="replicas" if world > 1 else "single-gpu"),
+        roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                      frac=achieved / peaks["hbm_gbs"], traffic=traffic,
+                      peak_source=f"{peaks['source']} hbm_gbs (copy, read+write)",
+                      bytes_per_launch=bytes_alg, flops_per_launch=flops_alg,
+                      tensor_frac=flops_alg / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"]),
+        cpu_baseline=cpu,
+        e2e=dict(value=world * tokens / (e2e_ms * 1e-3), unit="tokens/s",
+                 h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+        clocks=clocks,
+        gpu_launches=args.steps * launches_per_step,
+        wall_s_timed=wall,
+    )
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--soak-seconds", type=float, default=1.5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

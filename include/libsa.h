@@ -1,0 +1,180 @@
+/*
+ * libsa -- Stochastic Attention (SA) forward pass on NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes ("Stochastic Attention" technical summaries,
+ * gist.science/ja/paper/2604.00754 and gist.science/ko/paper/2604.00754):
+ *
+ *   SA   ("Core mechanism", steps 1-3): permute the rows of Q, K and V by a
+ *        random permutation sigma, X'[p] = X[sigma[p]]; run sliding-window
+ *        attention over the permuted rows with the window |p - q| <= h,
+ *        h = floor(w / 2), truncated at the sequence ends; scatter the result
+ *        back, Y[sigma[p]] = Y'[p].  The causal variant ("Theoretical
+ *        properties", causal-constraint bullet) additionally keeps only keys
+ *        with sigma[q] <= sigma[p], i.e. keys that precede the query in the
+ *        ORIGINAL order (the query itself included).
+ *   SWA  ("Problem statement"): token i attends to keys [max(0, i-w+1), i].
+ *   Gated dual path ("Gated SA and SWA", the displayed equation):
+ *        Y = sigmoid(a_sa) * Y_sa + sigmoid(a_swa) * Y_swa, with the gate
+ *        logits a_sa, a_swa given per token and query head.
+ *
+ * Softmax weights are exp(scale * <q, k>) normalised over the window;
+ * scale defaults to 1/sqrt(head_dim).  Grouped-query attention: query head
+ * hq uses kv head hq / (num_q_heads / num_kv_heads).
+ *
+ * Layouts (all row-major and contiguous, "BSHD"):
+ *   q    bf16  [batch, seqlen, num_q_heads,  head_dim]
+ *   k, v bf16  [batch, seqlen, num_kv_heads, head_dim]
+ *   out  bf16  [batch, seqlen, num_q_heads,  head_dim]
+ *   perm int32 [batch, seqlen]   sigma of each sequence (shared by all heads)
+ *   gate logits fp32 [batch, seqlen, num_q_heads], indexed by ORIGINAL token.
+ *
+ * Ownership and execution: the caller owns every buffer.  Device pointers
+ * must come from the CUDA device that is current on the calling thread.  The
+ * forward calls enqueue kernels on `stream` and return without waiting; they
+ * allocate no memory.  The library keeps a thread-local detail string for the
+ * last error (sa_last_error_message) and one device-side error word of its
+ * own that is used when a call is given a NULL error word.
+ *
+ * Errors: argument checks run on the host before anything is launched and
+ * return SA_ERR_INVALID_ARG or SA_ERR_UNSUPPORTED.  A failed launch returns
+ * SA_ERR_CUDA.  Faults detected on the device (a perm entry outside [0, n),
+ * a duplicate perm entry, a pipeline wait that ran past its limit) are OR-ed
+ * into a device error word as SA_ERRBIT_* bits; sa_check_error() reads it.
+ * No call traps, aborts or waits without a bound.
+ */
+#ifndef LIBSA_H
+#define LIBSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sa_status {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1, /* NULL pointer, size <= 0, Hq % Hkv != 0, ... */
+  SA_ERR_UNSUPPORTED = 2, /* valid request this build cannot run (head_dim, alignment, kernel) */
+  SA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  SA_ERR_BAD_PERM = 4,    /* device check found perm entries out of range or repeated */
+  SA_ERR_TIMEOUT = 5      /* a device pipeline wait ran past its bound; results are invalid */
+} sa_status_t;
+
+/* Kernel choice (sa_params_t.kernel). */
+enum {
+  SA_KERNEL_AUTO = 0,   /* tcgen05 tensor-core kernel when the shape fits it, else SIMT */
+  SA_KERNEL_SIMT = 1,   /* CUDA-core kernel: any window, the correctness baseline */
+  SA_KERNEL_TCGEN05 = 2 /* tcgen05/TMEM kernel; SA_ERR_UNSUPPORTED if the shape does not fit */
+};
+
+/* Bits of the device error word. */
+#define SA_ERRBIT_RANGE 1   /* a perm entry outside [0, seqlen) */
+#define SA_ERRBIT_DUP 2     /* two positions of perm name the same token */
+#define SA_ERRBIT_TIMEOUT 4 /* a bounded pipeline wait gave up */
+
+typedef struct sa_params {
+  int32_t batch;        /* B >= 1 */
+  int32_t seqlen;       /* n >= 1 */
+  int32_t num_q_heads;  /* Hq >= 1, a multiple of num_kv_heads */
+  int32_t num_kv_heads; /* Hkv >= 1 */
+  int32_t head_dim;     /* d: 64 or 128 */
+  int32_t window;       /* w >= 1.  SA: half-width h = w / 2 (floor).  SWA: w keys. */
+  int32_t window_swa;   /* gated call only: SWA window; <= 0 means "same as window" */
+  int32_t causal;       /* SA: 0 = window only, 1 = also sigma[q] <= sigma[p] */
+  float softmax_scale;  /* <= 0 means 1/sqrt(head_dim) */
+  int32_t kernel;       /* SA_KERNEL_* */
+  int32_t* err;         /* device int32 error word, or NULL for the library's own */
+} sa_params_t;
+
+/*
+ * Stochastic Attention forward ("Core mechanism" steps 1-3; causal rule from
+ * "Theoretical properties").  Reads q, k, v (bf16, BSHD), perm (device int32
+ * [B, n], must be a permutation of [0, n) per sequence; the forward kernels
+ * trust it, validate it first with sa_inverse_perm + sa_check_error if it is
+ * untrusted), writes every row of out (bf16 [B, n, Hq, d]).  out must not
+ * alias q, k or v.  All device pointers 16-byte aligned.
+ */
+sa_status_t sa_forward(const sa_params_t* params, const void* q, const void* k, const void* v,
+                       const int32_t* perm, void* out, cudaStream_t stream);
+
+/*
+ * Sliding-window attention over the original order ("Problem statement"):
+ * token i attends to keys [max(0, i - window + 1), i].  Same layouts and
+ * rules as sa_forward; params->causal is ignored (SWA is always causal).
+ */
+sa_status_t swa_forward(const sa_params_t* params, const void* q, const void* k, const void* v,
+                        void* out, cudaStream_t stream);
+
+/*
+ * Gated SA + SWA dual path ("Gated SA and SWA" equation):
+ *   out = sigmoid(gate_sa_logits) * SA(q,k,v; perm, window, causal)
+ *       + sigmoid(gate_swa_logits) * SWA(q,k,v; window_swa)
+ * Gate logits: device fp32 [B, n, Hq], indexed by original token and query
+ * head, broadcast over head_dim.  The merge happens in place in out (the SWA
+ * term is written first, the SA term is added by the second kernel), so the
+ * workspace is unused: pass NULL / 0 (sa_gated_workspace_size returns 0).
+ */
+sa_status_t sa_swa_gated_forward(const sa_params_t* params, const void* q, const void* k,
+                                 const void* v, const int32_t* perm, const float* gate_sa_logits,
+                                 const float* gate_swa_logits, void* out, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace sa_swa_gated_forward needs for these params (0). */
+size_t sa_gated_workspace_size(const sa_params_t* params);
+
+/*
+ * sigma^{-1} ("Core mechanism" step 3; "Theoretical properties": an O(n)
+ * index operation): inv[b, perm[b, p]] = p for every sequence b.  perm and
+ * inv are device int32 [batch, n] and must not overlap.  Entries of perm
+ * outside [0, n) set SA_ERRBIT_RANGE, repeated entries set SA_ERRBIT_DUP in
+ * *d_err (device int32; NULL selects the library's own word); inv is then
+ * unspecified.  Asynchronous on `stream`; read the verdict with
+ * sa_check_error.
+ */
+sa_status_t sa_inverse_perm(const int32_t* perm, int32_t* inv, int32_t batch, int32_t n,
+                            int32_t* d_err, cudaStream_t stream);
+
+/*
+ * Host: draw sigma ~ Uniform(S_n) for (seed, layer, batch_index) ("Core
+ * mechanism" step 1: one independent permutation per layer) into perm_host
+ * (int32[n], caller-owned).  Generator: the stream state is the output of one
+ * splitmix64 step applied to seed + (layer << 32) + batch_index; then a
+ * Durstenfeld Fisher-Yates shuffle of the identity, i = n-1 .. 1, swapping
+ * positions i and j = (x * (i + 1)) >> 64 for each splitmix64 output x.
+ * layer and batch_index must be >= 0.  Runs on the calling thread; no GPU.
+ */
+sa_status_t sa_make_perm(uint64_t seed, int32_t layer, int32_t batch_index, int32_t n,
+                         int32_t* perm_host);
+
+/*
+ * Synchronise `stream`, read the device error word (NULL: the library's own)
+ * and map it to a status: SA_ERR_TIMEOUT if SA_ERRBIT_TIMEOUT is set, else
+ * SA_ERR_BAD_PERM if a perm bit is set, else SA_OK.  The word is left as is.
+ */
+sa_status_t sa_check_error(const int32_t* d_err, cudaStream_t stream);
+
+/* Enqueue a reset of the device error word (NULL: the library's own) to 0. */
+sa_status_t sa_clear_error(int32_t* d_err, cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* sa_status_string(sa_status_t status);
+
+/* Detail of the last failing call on this thread ("" if none). */
+const char* sa_last_error_message(void);
+
+/* SA_KERNEL_SIMT or SA_KERNEL_TCGEN05: the kernel the last successful forward
+ * call on this thread launched (0 before any). */
+int32_t sa_last_kernel(void);
+
+/* Number of kernel launches the last successful forward call on this thread
+ * made (1 for SA/SWA, 2 for the gated path). */
+int32_t sa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBSA_H */

@@ -1,0 +1,227 @@
+"""ctypes binding of libsa (include/libsa.h).
+
+Argument marshalling only: shapes and dtypes are checked, pointers, sizes and
+the current CUDA stream are handed to the C entry points, and status codes
+become exceptions.  Every step of the attention runs in libsa's kernels; if
+the library is missing and cannot be built, calls raise -- there is no
+fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from ctypes import POINTER, byref, c_char_p, c_float, c_int32, c_size_t, c_uint64, c_void_p
+from pathlib import Path
+
+import numpy as np
+
+LIB_PATH = Path(__file__).resolve().with_name("libsa.so")
+
+SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_BAD_PERM, SA_ERR_TIMEOUT = range(6)
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_TCGEN05 = 0, 1, 2
+ERRBIT_RANGE, ERRBIT_DUP, ERRBIT_TIMEOUT = 1, 2, 4
+
+# Every function the header declares, with (restype, argtypes).
+SIGNATURES = {
+    "sa_forward": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "swa_forward": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "sa_swa_gated_forward": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                       c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "sa_gated_workspace_size": (c_size_t, [c_void_p]),
+    "sa_inverse_perm": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
+    "sa_make_perm": (c_int32, [c_uint64, c_int32, c_int32, c_int32, POINTER(c_int32)]),
+    "sa_check_error": (c_int32, [c_void_p, c_void_p]),
+    "sa_clear_error": (c_int32, [c_void_p, c_void_p]),
+    "sa_status_string": (c_char_p, [c_int32]),
+    "sa_last_error_message": (c_char_p, []),
+    "sa_last_kernel": (c_int32, []),
+    "sa_last_launch_count": (c_int32, []),
+}
+
+
+class SaParams(ctypes.Structure):
+    """Mirror of sa_params_t."""
+    _fields_ = [
+        ("batch", c_int32),
+        ("seqlen", c_int32),
+        ("num_q_heads", c_int32),
+        ("num_kv_heads", c_int32),
+        ("head_dim", c_int32),
+        ("window", c_int32),
+        ("window_swa", c_int32),
+        ("causal", c_int32),
+        ("softmax_scale", c_float),
+        ("kernel", c_int32),
+        ("err", c_void_p),
+    ]
+
+
+class SaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libsa.so (building it first if it is absent or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing:
+        from .build import build
+        build()
+    if not LIB_PATH.exists():
+        raise RuntimeError(f"libsa is not built ({LIB_PATH} missing)")
+    lib = ctypes.CDLL(str(LIB_PATH))
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _raise(st: int):
+    lib = load()
+    msg = lib.sa_last_error_message().decode() or lib.sa_status_string(st).decode()
+    raise SaError(st, msg)
+
+
+def _check(st: int):
+    if st != SA_OK:
+        _raise(st)
+
+
+def _stream(t, stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, name, dtype, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _params(q, k, window, window_swa, causal, softmax_scale, kernel, err) -> SaParams:
+    b, n, hq, d = q.shape
+    if k.shape[0] != b or k.shape[1] != n or k.shape[3] != d:
+        raise ValueError("q and k/v shapes disagree")
+    return SaParams(b, n, hq, k.shape[2], d, int(window), int(window_swa), int(bool(causal)),
+                    float(softmax_scale), int(kernel), c_void_p(err.data_ptr() if err is not None else None))
+
+
+def _qkv(q, k, v):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 4)
+    if k.shape != v.shape:
+        raise ValueError("k and v shapes differ")
+
+
+def sa_forward(q, k, v, perm, window: int, causal: bool = True, softmax_scale: float = 0.0,
+               out=None, kernel: int = KERNEL_AUTO, err=None, stream=None):
+    """Stochastic Attention forward; returns out (bf16 [B, n, Hq, d])."""
+    import torch
+    _qkv(q, k, v)
+    _need(perm, "perm", torch.int32, 2)
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, 4)
+    prm = _params(q, k, window, 0, causal, softmax_scale, kernel, err)
+    _check(load().sa_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(), perm.data_ptr(),
+                             out.data_ptr(), _stream(q, stream)))
+    return out
+
+
+def swa_forward(q, k, v, window: int, softmax_scale: float = 0.0, out=None,
+                kernel: int = KERNEL_AUTO, err=None, stream=None):
+    """Sliding-window attention over the original order."""
+    import torch
+    _qkv(q, k, v)
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, 4)
+    prm = _params(q, k, window, 0, True, softmax_scale, kernel, err)
+    _check(load().swa_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              _stream(q, stream)))
+    return out
+
+
+def sa_swa_gated_forward(q, k, v, perm, gate_sa, gate_swa, window: int, window_swa: int = 0,
+                         causal: bool = True, softmax_scale: float = 0.0, out=None,
+                         kernel: int = KERNEL_AUTO, err=None, stream=None):
+    """sigmoid(gate_sa) * SA + sigmoid(gate_swa) * SWA."""
+    import torch
+    _qkv(q, k, v)
+    _need(perm, "perm", torch.int32, 2)
+    _need(gate_sa, "gate_sa", torch.float32, 3)
+    _need(gate_swa, "gate_swa", torch.float32, 3)
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, 4)
+    prm = _params(q, k, window, window_swa, causal, softmax_scale, kernel, err)
+    lib = load()
+    ws = lib.sa_gated_workspace_size(byref(prm))
+    work = torch.empty(ws, dtype=torch.uint8, device=q.device) if ws else None
+    _check(lib.sa_swa_gated_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                    perm.data_ptr(), gate_sa.data_ptr(), gate_swa.data_ptr(),
+                                    out.data_ptr(), work.data_ptr() if work is not None else None,
+                                    ws, _stream(q, stream)))
+    return out
+
+
+def sa_inverse_perm(perm, inv=None, err=None, stream=None):
+    """sigma^{-1} on the device; check the verdict with check_error(err)."""
+    import torch
+    _need(perm, "perm", torch.int32, 2)
+    inv = torch.empty_like(perm) if inv is None else inv
+    _need(inv, "inv", torch.int32, 2)
+    b, n = perm.shape
+    _check(load().sa_inverse_perm(perm.data_ptr(), inv.data_ptr(), b, n,
+                                  err.data_ptr() if err is not None else None, _stream(perm, stream)))
+    return inv
+
+
+def check_error(err=None, stream=None) -> int:
+    """Synchronise and map the device error word to a status (0 = fine)."""
+    import torch
+    dev = err.device if err is not None else torch.device("cuda", torch.cuda.current_device())
+    s = _stream(torch.empty(0, device=dev), stream)
+    return int(load().sa_check_error(err.data_ptr() if err is not None else None, s))
+
+
+def clear_error(err=None, stream=None):
+    import torch
+    dev = err.device if err is not None else torch.device("cuda", torch.cuda.current_device())
+    _check(load().sa_clear_error(err.data_ptr() if err is not None else None,
+                                 _stream(torch.empty(0, device=dev), stream)))
+
+
+def make_perm(seed: int, layer: int, batch_index: int, n: int) -> np.ndarray:
+    """sigma for (seed, layer, batch_index) from the library's host generator."""
+    buf = (c_int32 * n)()
+    _check(load().sa_make_perm(c_uint64(seed & ((1 << 64) - 1)), int(layer), int(batch_index),
+                               int(n), buf))
+    return np.frombuffer(buf, dtype=np.int32).copy()
+
+
+def make_perms(seed: int, layer: int, batch: int, n: int) -> np.ndarray:
+    """[batch, n] int32: one sigma per sequence."""
+    return np.stack([make_perm(seed, layer, b, n) for b in range(batch)])
+
+
+def last_kernel() -> int:
+    return int(load().sa_last_kernel())
+
+
+def last_launch_count() -> int:
+    return int(load().sa_last_launch_count())

@@ -1,0 +1,244 @@
+// C-ABI entry points of libsa: argument validation, kernel choice, the host
+// sigma generator and error reporting.  Every step of the attention itself
+// runs in the CUDA kernels of sa_simt.cu / sa_tc.cu / sa_perm.cu.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "sa_internal.h"
+
+namespace sa {
+
+static thread_local char g_msg[512] = "";
+static thread_local int32_t g_last_kernel = 0;
+static thread_local int32_t g_last_launches = 0;
+
+__device__ int32_t g_error_word = 0;
+
+sa_status_t fail(sa_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+int32_t* default_error_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+  return static_cast<int32_t*>(p);
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared shape checks of the three forward calls.
+static sa_status_t check_params(const sa_params_t* prm, bool need_window) {
+  if (prm == nullptr) return fail(SA_ERR_INVALID_ARG, "params is NULL");
+  if (prm->batch < 1 || prm->seqlen < 1 || prm->num_q_heads < 1 || prm->num_kv_heads < 1)
+    return fail(SA_ERR_INVALID_ARG, "batch, seqlen and head counts must be >= 1");
+  if (prm->num_q_heads % prm->num_kv_heads != 0)
+    return fail(SA_ERR_INVALID_ARG, "num_q_heads (%d) must be a multiple of num_kv_heads (%d)",
+                prm->num_q_heads, prm->num_kv_heads);
+  if (prm->head_dim != 64 && prm->head_dim != 128)
+    return fail(SA_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", prm->head_dim);
+  if (need_window && prm->window < 1) return fail(SA_ERR_INVALID_ARG, "window must be >= 1");
+  if (prm->kernel < SA_KERNEL_AUTO || prm->kernel > SA_KERNEL_TCGEN05)
+    return fail(SA_ERR_INVALID_ARG, "unknown kernel selector %d", prm->kernel);
+  const double rows = double(prm->batch) * prm->seqlen * prm->num_q_heads;
+  if (rows * prm->head_dim >= 9.0e18 || double(prm->batch) * prm->seqlen >= 2147483647.0 ||
+      rows >= 2147483647.0)
+    return fail(SA_ERR_UNSUPPORTED, "problem too large for 32-bit row indices");
+  return SA_OK;
+}
+
+static sa_status_t check_ptrs(const void* q, const void* k, const void* v, const void* out) {
+  if (!q || !k || !v || !out) return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(SA_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+  if (out == q || out == k || out == v) return fail(SA_ERR_INVALID_ARG, "out aliases an input");
+  return SA_OK;
+}
+
+static Problem make_problem(const sa_params_t* prm, const void* q, const void* k, const void* v,
+                            const int32_t* perm, void* out) {
+  Problem pb{};
+  pb.B = prm->batch;
+  pb.n = prm->seqlen;
+  pb.Hq = prm->num_q_heads;
+  pb.Hkv = prm->num_kv_heads;
+  pb.d = prm->head_dim;
+  pb.g = pb.Hq / pb.Hkv;
+  pb.window = prm->window;
+  pb.window_swa = prm->window_swa > 0 ? prm->window_swa : prm->window;
+  pb.causal = prm->causal ? 1 : 0;
+  pb.scale = prm->softmax_scale > 0.f ? prm->softmax_scale : 1.0f / std::sqrt(float(pb.d));
+  pb.q = q;
+  pb.k = k;
+  pb.v = v;
+  pb.perm = perm;
+  pb.out = out;
+  pb.err = prm->err ? prm->err : default_error_word();
+  return pb;
+}
+
+static sa_status_t finish(sa_status_t st, int32_t kernel, int32_t launches) {
+  if (st == SA_OK) {
+    g_last_kernel = kernel;
+    g_last_launches = launches;
+    g_msg[0] = '\0';
+  }
+  return st;
+}
+
+// Runs one single-path attention (SA or SWA) with the requested kernel.
+static sa_status_t run_single(const sa_params_t* prm, Problem& pb, Path path, cudaStream_t s) {
+  if (pb.err == nullptr) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  const bool tc_ok = tc_supported(pb, path);
+  if (prm->kernel == SA_KERNEL_TCGEN05 && !tc_ok)
+    return fail(SA_ERR_UNSUPPORTED, "shape does not fit the tcgen05 kernel (window too wide, "
+                "Hq/Hkv does not divide 128, or a device without tcgen05)");
+  if (prm->kernel != SA_KERNEL_SIMT && tc_ok) {
+    return finish(launch_tc(pb, path, nullptr, 0, s), SA_KERNEL_TCGEN05, 1);
+  }
+  return finish(launch_simt(pb, path, s), SA_KERNEL_SIMT, 1);
+}
+
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" sa_status_t sa_forward(const sa_params_t* params, const void* q, const void* k,
+                                  const void* v, const int32_t* perm, void* out,
+                                  cudaStream_t stream) {
+  sa_status_t st = check_params(params, true);
+  if (st != SA_OK) return st;
+  if ((st = check_ptrs(q, k, v, out)) != SA_OK) return st;
+  if (perm == nullptr) return fail(SA_ERR_INVALID_ARG, "perm must be non-NULL");
+  Problem pb = make_problem(params, q, k, v, perm, out);
+  return run_single(params, pb, kPathSA, stream);
+}
+
+extern "C" sa_status_t swa_forward(const sa_params_t* params, const void* q, const void* k,
+                                   const void* v, void* out, cudaStream_t stream) {
+  sa_status_t st = check_params(params, true);
+  if (st != SA_OK) return st;
+  if ((st = check_ptrs(q, k, v, out)) != SA_OK) return st;
+  Problem pb = make_problem(params, q, k, v, nullptr, out);
+  pb.window_swa = params->window;
+  return run_single(params, pb, kPathSWA, stream);
+}
+
+extern "C" size_t sa_gated_workspace_size(const sa_params_t*) { return 0; }
+
+extern "C" sa_status_t sa_swa_gated_forward(const sa_params_t* params, const void* q,
+                                            const void* k, const void* v, const int32_t* perm,
+                                            const float* gate_sa_logits,
+                                            const float* gate_swa_logits, void* out,
+                                            void* workspace, size_t workspace_bytes,
+                                            cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  sa_status_t st = check_params(params, true);
+  if (st != SA_OK) return st;
+  if ((st = check_ptrs(q, k, v, out)) != SA_OK) return st;
+  if (!perm || !gate_sa_logits || !gate_swa_logits)
+    return fail(SA_ERR_INVALID_ARG, "perm and both gate logit arrays must be non-NULL");
+  Problem pb = make_problem(params, q, k, v, perm, out);
+  pb.gate_sa = gate_sa_logits;
+  pb.gate_swa = gate_swa_logits;
+  if (pb.err == nullptr) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  const bool tc_ok = tc_supported(pb, kPathSA) && tc_supported(pb, kPathSWA);
+  if (params->kernel == SA_KERNEL_TCGEN05 && !tc_ok)
+    return fail(SA_ERR_UNSUPPORTED, "shape does not fit the tcgen05 kernel");
+  if (params->kernel != SA_KERNEL_SIMT && tc_ok) {
+    // Pass 1 writes sigmoid(a_swa) * Y_swa into out; pass 2 adds
+    // sigmoid(a_sa) * Y_sa row by row.  Stream order separates the passes and
+    // sigma being a bijection means each pass writes each row exactly once.
+    st = launch_tc(pb, kPathSWA, pb.gate_swa, 0, stream);
+    if (st != SA_OK) return st;
+    return finish(launch_tc(pb, kPathSA, pb.gate_sa, 1, stream), SA_KERNEL_TCGEN05, 2);
+  }
+  return finish(launch_simt(pb, kPathGated, stream), SA_KERNEL_SIMT, 1);
+}
+
+extern "C" sa_status_t sa_inverse_perm(const int32_t* perm, int32_t* inv, int32_t batch,
+                                       int32_t n, int32_t* d_err, cudaStream_t stream) {
+  if (!perm || !inv) return fail(SA_ERR_INVALID_ARG, "perm and inv must be non-NULL");
+  if (batch < 1 || n < 1) return fail(SA_ERR_INVALID_ARG, "batch and n must be >= 1");
+  if (double(batch) * n >= 2147483647.0) return fail(SA_ERR_UNSUPPORTED, "batch * n too large");
+  const int32_t* a = perm;
+  const int32_t* b = inv;
+  if (a < b + size_t(batch) * n && b < a + size_t(batch) * n)
+    return fail(SA_ERR_INVALID_ARG, "perm and inv overlap");
+  int32_t* err = d_err ? d_err : default_error_word();
+  if (!err) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  sa_status_t st = launch_inverse_perm(perm, inv, batch, n, err, stream);
+  if (st == SA_OK) g_msg[0] = '\0';
+  return st;
+}
+
+extern "C" sa_status_t sa_make_perm(uint64_t seed, int32_t layer, int32_t batch_index, int32_t n,
+                                    int32_t* perm_host) {
+  if (!perm_host) return fail(SA_ERR_INVALID_ARG, "perm_host must be non-NULL");
+  if (n < 1 || layer < 0 || batch_index < 0)
+    return fail(SA_ERR_INVALID_ARG, "n must be >= 1; layer and batch_index >= 0");
+  // splitmix64 (S. Vigna, public domain): add the golden-ratio increment, then
+  // two xor-shift-multiply rounds and a final xor-shift.
+  auto step = [](uint64_t& state) -> uint64_t {
+    state += 0x9E3779B97F4A7C15ull;
+    uint64_t z = state;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+  };
+  uint64_t start = seed + (uint64_t(uint32_t(layer)) << 32) + uint64_t(uint32_t(batch_index));
+  uint64_t state = step(start);  // the first output seeds this stream
+  for (int32_t p = 0; p < n; ++p) perm_host[p] = p;
+  for (int32_t i = n - 1; i >= 1; --i) {
+    const uint64_t x = step(state);
+    const uint64_t j = uint64_t((unsigned __int128)x * (unsigned __int128)(uint64_t(i) + 1) >> 64);
+    const int32_t t = perm_host[i];
+    perm_host[i] = perm_host[j];
+    perm_host[j] = t;
+  }
+  g_msg[0] = '\0';
+  return SA_OK;
+}
+
+extern "C" sa_status_t sa_check_error(const int32_t* d_err, cudaStream_t stream) {
+  const int32_t* err = d_err ? d_err : default_error_word();
+  if (!err) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  int32_t host = 0;
+  cudaError_t ce = cudaMemcpyAsync(&host, err, sizeof(host), cudaMemcpyDeviceToHost, stream);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(stream);
+  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(ce));
+  if (host & SA_ERRBIT_TIMEOUT) return fail(SA_ERR_TIMEOUT, "a device wait ran past its bound");
+  if (host & (SA_ERRBIT_RANGE | SA_ERRBIT_DUP))
+    return fail(SA_ERR_BAD_PERM, "perm is not a permutation (error bits 0x%x)", host);
+  return SA_OK;
+}
+
+extern "C" sa_status_t sa_clear_error(int32_t* d_err, cudaStream_t stream) {
+  int32_t* err = d_err ? d_err : default_error_word();
+  if (!err) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  cudaError_t ce = cudaMemsetAsync(err, 0, sizeof(int32_t), stream);
+  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(ce));
+  return SA_OK;
+}
+
+extern "C" const char* sa_status_string(sa_status_t status) {
+  switch (status) {
+    case SA_OK: return "SA_OK";
+    case SA_ERR_INVALID_ARG: return "SA_ERR_INVALID_ARG: invalid argument";
+    case SA_ERR_UNSUPPORTED: return "SA_ERR_UNSUPPORTED: not supported by this build";
+    case SA_ERR_CUDA: return "SA_ERR_CUDA: CUDA runtime error";
+    case SA_ERR_BAD_PERM: return "SA_ERR_BAD_PERM: perm is not a permutation";
+    case SA_ERR_TIMEOUT: return "SA_ERR_TIMEOUT: device wait ran past its bound";
+  }
+  return "unknown sa_status_t";
+}
+
+extern "C" const char* sa_last_error_message(void) { return g_msg; }
+extern "C" int32_t sa_last_kernel(void) { return g_last_kernel; }
+extern "C" int32_t sa_last_launch_count(void) { return g_last_launches; }

@@ -1,0 +1,59 @@
+// Internal interface between the C-ABI entry points (sa_api.cu) and the
+// kernel launchers (sa_perm.cu, sa_simt.cu, sa_tc.cu).  Not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "libsa.h"
+
+namespace sa {
+
+// Which attention a launch computes.
+enum Path : int {
+  kPathSA = 0,     // sliding window over the sigma-permuted rows
+  kPathSWA = 1,    // trailing window over the original order
+  kPathGated = 2,  // sigmoid-gated SA + SWA (SIMT kernel computes both in one pass)
+};
+
+// One attention problem, already validated on the host.
+struct Problem {
+  int B, n, Hq, Hkv, d, g;  // g = Hq / Hkv
+  int window;               // SA window w (h = w / 2)
+  int window_swa;           // SWA window
+  int causal;               // SA causal rule
+  float scale;              // softmax scale
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* perm;      // [B, n]; unused by SWA
+  const float* gate_sa;     // [B, n, Hq] logits (gated only)
+  const float* gate_swa;
+  void* out;
+  int32_t* err;             // device error word (never NULL here)
+};
+
+// Record a detail message for sa_last_error_message() and return `st`.
+sa_status_t fail(sa_status_t st, const char* fmt, ...);
+
+// Device error word owned by the library (used when the caller passes NULL).
+int32_t* default_error_word();
+
+// SIMT (CUDA-core) kernel: any window.  `path` selects SA, SWA or gated.
+sa_status_t launch_simt(const Problem& pb, Path path, cudaStream_t stream);
+
+// tcgen05 kernel.  `path` is kPathSA or kPathSWA.  gate != nullptr scales the
+// output by sigmoid(gate logit); accumulate != 0 adds the previous contents
+// of out (the gated merge's second pass).  Returns SA_ERR_UNSUPPORTED, with
+// nothing launched, when the shape does not fit the kernel.
+sa_status_t launch_tc(const Problem& pb, Path path, const float* gate, int accumulate,
+                      cudaStream_t stream);
+
+// True when launch_tc can run this problem / path.
+bool tc_supported(const Problem& pb, Path path);
+
+// sigma^{-1} kernels.
+sa_status_t launch_inverse_perm(const int32_t* perm, int32_t* inv, int batch, int n,
+                                int32_t* err, cudaStream_t stream);
+
+}  // namespace sa

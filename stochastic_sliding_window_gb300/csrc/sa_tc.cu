@@ -1,0 +1,722 @@
+// Tensor-core (tcgen05 / TMEM / TMA) kernel for SA and SWA on sm_103a.
+//
+// What one tile computes (Stochastic Attention summary, "Core mechanism"
+// steps 1-3; causal rule from "Theoretical properties"; SWA from "Problem
+// statement"):  a tile is Bt = 128/g consecutive PERMUTED positions
+// p0 .. p0+Bt-1 of one (sequence b, kv head) pair, stacked with the g query
+// heads that share that kv head, so the tile has M = 128 query rows
+// (row r = t*g + j: position p0+t, query head kvh*g + j).  Their keys are the
+// contiguous permuted span q in [p0 - left, p0 + Bt - 1 + right]
+// (SA: left = right = h = w/2; SWA: left = w-1, right = 0, sigma = identity).
+//
+//   1. gather    (warp 0, TMA tile::gather4): sigma of the span -> smem; the
+//                Q rows sigma[p0+t] and the K/V rows sigma[q] are fetched
+//                straight from the BSHD tensors into 128B-swizzled smem --
+//                the permuted copies never exist in HBM.
+//   2. S = Q K^T (warp 1, tcgen05.mma kind::f16, fp32 accumulator in TMEM),
+//                one 128 x span_pad tile: the whole window of every row.
+//   3. softmax   (warps 4-11, two warpgroups taking alternate tiles; thread
+//                r owns TMEM lane r): mask |p-q| <= h via the row's column
+//                band, the sequence ends, and for causal SA sigma[q] <=
+//                sigma[p]; exact row max, exp2, row sum; P (bf16) -> smem,
+//                over the dead Q/K bytes.
+//   4. O = P V   (warp 1, tcgen05.mma, V used MN-major), into the TMEM
+//                columns S occupied.
+//   5. epilogue  (same warpgroup): O / rowsum, optionally * sigmoid(gate)
+//                and + the previous out row (the gated merge), bf16, stored
+//                to out row sigma[p0+t] -- the sigma^{-1} scatter.
+// Because one tile holds the whole window of each row there is no online
+// rescaling.  The kernel is persistent (one CTA per SM, tiles strided by
+// gridDim.x so neighbouring tiles -- which share halo K/V rows -- run at the
+// same time and meet in L2).  Every mbarrier wait is bounded; on expiry the
+// CTA sets SA_ERRBIT_TIMEOUT, drains its own copies and MMAs, frees TMEM and
+// exits.
+#include <cuda.h>  // CUtensorMap and the tensor-map enums (types only)
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "sa_internal.h"
+
+namespace sa {
+namespace tc {
+
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kTmemWarp = 2;
+constexpr int kFirstSoftmaxWarp = 4;
+constexpr int kNumWG = 2;
+constexpr int kBM = 128;  // MMA M: query rows per tile
+constexpr int kMaxS = 2;  // smem stages
+constexpr int kMaxT = 4;  // TMEM stages
+constexpr uint32_t kMaxSmem = 232448;     // 227 KB per CTA on sm_100-class parts
+constexpr uint32_t kMinSmem = 118 * 1024; // forces one resident CTA per SM
+
+struct Params {
+  const int32_t* perm;  // [B, n]; unused when identity
+  const float* gate;    // [B, n, Hq] logits or nullptr
+  __nv_bfloat16* out;
+  int32_t* err;
+  int B, n, Hq, Hkv, g, Bt;
+  int left, right, span_pad;
+  int causal, accumulate, identity;
+  float scale_log2;
+  int tiles_per_seq, num_tiles;
+  int s_stages, t_stages, cols_stage, tmem_alloc;
+  uint32_t qk_bytes, stage_bytes, sig_off, bar_off;
+  long long timeout_cycles;
+};
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// Four arbitrary rows (one 64-element, 128-byte box each) of a 2-D bf16
+// tensor into 512 contiguous bytes of smem, 128B-swizzled.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tm), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
+// start >> 4 in [0,14), LBO >> 4 in [16,30), SBO >> 4 in [32,46),
+// version 1 at bit 46, layout SWIZZLE_128B = 2 in [61,64)).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, dense.
+// D format [4,6) = 1 (F32); A format [7,10) = 1 (BF16); B format [10,13) = 1;
+// B major [16] (1 = MN-major); N >> 3 in [17,23); M >> 4 in [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int nn, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn_major) << 16) |
+         (uint32_t(nn >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane; the wait is in the
+// same asm statement so no use of the outputs can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------ layout
+struct Bars {
+  uint32_t base;
+  // smem-stage barriers
+  __device__ uint32_t full(int s) const { return base + 8u * s; }
+  __device__ uint32_t empty(int s) const { return base + 8u * (kMaxS + s); }
+  __device__ uint32_t pfull(int s) const { return base + 8u * (2 * kMaxS + s); }
+  // TMEM-stage barriers
+  __device__ uint32_t sfull(int t) const { return base + 8u * (3 * kMaxS + t); }
+  __device__ uint32_t ofull(int t) const { return base + 8u * (3 * kMaxS + kMaxT + t); }
+  __device__ uint32_t tempty(int t) const { return base + 8u * (3 * kMaxS + 2 * kMaxT + t); }
+  __device__ uint32_t drain() const { return base + 8u * (3 * kMaxS + 3 * kMaxT); }
+  static constexpr uint32_t kBytes = 8u * (3 * kMaxS + 3 * kMaxT + 1);
+};
+
+struct TileCoord {
+  int b, kvh, p0;
+};
+
+__device__ __forceinline__ TileCoord decode(const Params& P, int tile) {
+  const int seq = tile / P.tiles_per_seq;
+  TileCoord c;
+  c.b = seq / P.Hkv;
+  c.kvh = seq - c.b * P.Hkv;
+  c.p0 = (tile - seq * P.tiles_per_seq) * P.Bt;
+  return c;
+}
+
+// Bounded wait.  Returns false if the wait expired (error bit set, abort
+// raised) or another role already aborted.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& P,
+                                          volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > P.timeout_cycles) {
+      *abort_flag = 1;
+      atomicOr(P.err, SA_ERRBIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Params& P,
+                                          volatile int* abort_flag) {
+  const bool ok = wait_bounded(bar, parity, P, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------------ roles
+template <int D>
+__device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUtensorMap* tk,
+                              const CUtensorMap* tv, uint8_t* smem, uint32_t sbase,
+                              const Bars& bars, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  bool issued[kMaxS] = {false, false};
+  uint32_t issued_par[kMaxS] = {0, 0};
+  int it = 0;
+  for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, ++it) {
+    const int s = it % P.s_stages;
+    const uint32_t ph = uint32_t(it / P.s_stages) & 1u;
+    if (!warp_wait(bars.empty(s), ph ^ 1u, P, abort_flag)) break;
+    const TileCoord tc = decode(P, tile);
+    int32_t* sig = reinterpret_cast<int32_t*>(smem + P.sig_off) + s * P.span_pad;
+    const int k0 = tc.p0 - P.left;
+    const int32_t* perm_b = P.identity ? nullptr : P.perm + size_t(tc.b) * P.n;
+    for (int c = lane; c < P.span_pad; c += 32) {
+      const int qpos = min(max(k0 + c, 0), P.n - 1);
+      int tok = perm_b ? __ldg(perm_b + qpos) : qpos;
+      if (unsigned(tok) >= unsigned(P.n)) {
+        atomicOr(P.err, SA_ERRBIT_RANGE);
+        tok = 0;
+      }
+      sig[c] = tok;
+    }
+    __threadfence_block();
+    __syncwarp();
+    const uint32_t full = bars.full(s);
+    if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(kBM + 2 * P.span_pad) * D * 2u);
+    __syncwarp();
+    const uint32_t q_dst = sbase + uint32_t(s) * P.stage_bytes;
+    const uint32_t k_dst = q_dst + kBM * D * 2;
+    const uint32_t v_dst = q_dst + P.qk_bytes;
+    const int row_base_q = tc.b * P.n;
+    {  // Q: 32 groups of four rows, one per lane
+      int rows[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = 4 * lane + u;
+        const int t = r / P.g;
+        const int j = r - t * P.g;
+        const int tok = sig[P.left + t];
+        rows[u] = (row_base_q + tok) * P.Hq + tc.kvh * P.g + j;
+      }
+#pragma unroll
+      for (int kb = 0; kb < D / 64; ++kb)
+        tma_gather4(q_dst + kb * (kBM * 128) + lane * 512, tq, kb * 64, rows[0], rows[1], rows[2],
+                    rows[3], full);
+    }
+    for (int grp = lane; grp < P.span_pad / 4; grp += 32) {  // K and V
+      int rows[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) rows[u] = (row_base_q + sig[4 * grp + u]) * P.Hkv + tc.kvh;
+#pragma unroll
+      for (int kb = 0; kb < D / 64; ++kb) {
+        const uint32_t off = kb * (P.span_pad * 128) + grp * 512;
+        tma_gather4(k_dst + off, tk, kb * 64, rows[0], rows[1], rows[2], rows[3], full);
+        tma_gather4(v_dst + off, tv, kb * 64, rows[0], rows[1], rows[2], rows[3], full);
+      }
+    }
+    issued[s] = true;
+    issued_par[s] = ph;
+  }
+  if (*abort_flag) {  // let this CTA's own copies land before smem is released
+    for (int s = 0; s < P.s_stages; ++s)
+      if (issued[s]) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bars.full(s), issued_par[s]) && clock64() - t0 < P.timeout_cycles) {
+        }
+      }
+  }
+}
+
+template <int D>
+__device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, const Bars& bars,
+                         volatile int* abort_flag) {
+  const int S = P.s_stages, T = P.t_stages;
+  const uint32_t q_bytes = kBM * D * 2;
+  auto qk = [&](int it) -> bool {
+    const int s = it % S, ts = it % T;
+    if (!wait_bounded(bars.full(s), uint32_t(it / S) & 1u, P, abort_flag)) return false;
+    if (!wait_bounded(bars.tempty(ts), (uint32_t(it / T) & 1u) ^ 1u, P, abort_flag)) return false;
+    tc_fence_after();
+    const uint32_t d = tmem_base + uint32_t(ts * P.cols_stage);
+    const uint32_t qa = sbase + uint32_t(s) * P.stage_bytes;
+    const uint32_t ka = qa + q_bytes;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t koff = uint32_t(kk & 3) * 32u;
+      const uint64_t a = sdesc_sw128(qa + (kk >> 2) * (kBM * 128) + koff, 16, 1024);
+      for (int n0 = 0; n0 < P.span_pad; n0 += 256) {
+        const int nn = min(256, P.span_pad - n0);
+        const uint64_t bd =
+            sdesc_sw128(ka + (kk >> 2) * (P.span_pad * 128) + n0 * 128 + koff, 16, 1024);
+        umma_bf16(d + n0, a, bd, idesc_bf16(kBM, nn, 0), kk > 0 ? 1u : 0u);
+      }
+    }
+    umma_commit(bars.sfull(ts));
+    return true;
+  };
+  auto pv = [&](int it) -> bool {
+    const int s = it % S, ts = it % T;
+    if (!wait_bounded(bars.pfull(s), uint32_t(it / S) & 1u, P, abort_flag)) return false;
+    tc_fence_after();
+    const uint32_t o = tmem_base + uint32_t(ts * P.cols_stage);
+    const uint32_t pa = sbase + uint32_t(s) * P.stage_bytes;
+    const uint32_t va = pa + P.qk_bytes;
+    const uint32_t idesc = idesc_bf16(kBM, D, 1);
+    const int ksteps = P.span_pad / 16;
+    for (int kk = 0; kk < ksteps; ++kk) {
+      const uint64_t a = sdesc_sw128(pa + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+      const uint64_t bd = sdesc_sw128(va + kk * 2048, P.span_pad * 128, 1024);
+      umma_bf16(o, a, bd, idesc, kk > 0 ? 1u : 0u);
+    }
+    umma_commit(bars.ofull(ts));
+    umma_commit(bars.empty(s));
+    return true;
+  };
+  const bool overlap = (S >= 2) && (T >= 2);
+  bool ok = true;
+  int it = 0;
+  for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, ++it) {
+    if (!overlap && it > 0 && !pv(it - 1)) { ok = false; break; }
+    if (!qk(it)) { ok = false; break; }
+    if (overlap && it > 0 && !pv(it - 1)) { ok = false; break; }
+  }
+  if (ok && it > 0) pv(it - 1);
+  // All MMAs this thread issued complete before TMEM can be released.
+  umma_commit(bars.drain());
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bars.drain(), 0) && clock64() - t0 < P.timeout_cycles) {
+  }
+}
+
+template <int D>
+__device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base, const Bars& bars,
+                             volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wg = (warp - kFirstSoftmaxWarp) >> 2;
+  const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+  const int r = quad * 32 + lane;
+  const int t = r / P.g;
+  const int j = r - t * P.g;
+  const int S = P.s_stages, T = P.t_stages;
+  const int nch = P.span_pad / 32;
+  int it = 0;
+  for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, ++it) {
+    if (it % kNumWG != wg) continue;
+    const int s = it % S, ts = it % T;
+    const uint32_t ph_s = uint32_t(it / S) & 1u, ph_t = uint32_t(it / T) & 1u;
+    const TileCoord tc = decode(P, tile);
+    if (!warp_wait(bars.sfull(ts), ph_t, P, abort_flag)) break;
+    if (!warp_wait(bars.full(s), ph_s, P, abort_flag)) break;  // sigma smem visibility
+    tc_fence_after();
+    const int32_t* sig = reinterpret_cast<const int32_t*>(smem + P.sig_off) + s * P.span_pad;
+    const bool row_valid = tc.p0 + t < P.n;
+    const int sig_p = sig[P.left + t];
+    const int lo = max(t, P.left - tc.p0);
+    const int hi = row_valid ? min(t + P.left + P.right, P.n - 1 - tc.p0 + P.left) : lo - 1;
+    const uint32_t trow = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(ts * P.cols_stage);
+
+    // pass 1: masked row max
+    float mx = -INFINITY;
+    for (int ch = 0; ch < nch; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(trow + ch * 32, v);
+      const int c0 = ch * 32;
+      const int4* sg4 = reinterpret_cast<const int4*>(sig + c0);
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const int4 sv = sg4[e4];
+        const int svv[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + e4 * 4 + u;
+          bool ok = (c >= lo) && (c <= hi);
+          if (P.causal) ok = ok && (svv[u] <= sig_p);
+          mx = ok ? fmaxf(mx, __uint_as_float(v[e4 * 4 + u])) : mx;
+        }
+      }
+    }
+    const float ms = (mx == -INFINITY) ? 0.f : mx * P.scale_log2;
+
+    // pass 2: p = exp2(s*scale*log2e - max), row sum, P (bf16) to smem
+    float l = 0.f;
+    uint8_t* pbase = smem + size_t(s) * P.stage_bytes;
+    for (int ch = 0; ch < nch; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(trow + ch * 32, v);
+      const int c0 = ch * 32;
+      const int4* sg4 = reinterpret_cast<const int4*>(sig + c0);
+      uint32_t pk[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const int4 sv = sg4[e4];
+        const int svv[4] = {sv.x, sv.y, sv.z, sv.w};
+        float pr[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + e4 * 4 + u;
+          bool ok = (c >= lo) && (c <= hi);
+          if (P.causal) ok = ok && (svv[u] <= sig_p);
+          pr[u] = ok ? exp2f(fmaf(__uint_as_float(v[e4 * 4 + u]), P.scale_log2, -ms)) : 0.f;
+          l += pr[u];
+        }
+        pk[e4 * 2] = pack_bf16x2(pr[0], pr[1]);
+        pk[e4 * 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int col8 = c0 + q4 * 8;
+        const int kb = col8 >> 6;
+        const int c16 = (col8 & 63) >> 3;
+        uint4* dst = reinterpret_cast<uint4*>(pbase + kb * (kBM * 128) + r * 128 +
+                                              ((c16 ^ (r & 7)) << 4));
+        *dst = make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.pfull(s));
+
+    // epilogue: O / l (* gate, + previous), bf16, row sigma[p0+t] of out
+    if (!warp_wait(bars.ofull(ts), ph_t, P, abort_flag)) break;
+    tc_fence_after();
+    float mul = l > 0.f ? 1.f / l : 0.f;
+    const size_t orow = (size_t(tc.b) * P.n + sig_p) * P.Hq + size_t(tc.kvh) * P.g + j;
+    if (P.gate != nullptr && row_valid) mul *= 1.f / (1.f + expf(-P.gate[orow]));
+    __nv_bfloat16* op = P.out + orow * D;
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(trow + ch * 32, v);
+      if (row_valid) {
+        uint4* dst = reinterpret_cast<uint4*>(op + ch * 32);
+        uint4 prev[4];
+        if (P.accumulate) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) prev[q4] = dst[q4];
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[q4 * 8 + e]) * mul;
+          if (P.accumulate) {
+            const __nv_bfloat162* pv2 = reinterpret_cast<const __nv_bfloat162*>(&prev[q4]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 pf = __bfloat1622float2(pv2[e]);
+              f[2 * e] += pf.x;
+              f[2 * e + 1] += pf.y;
+            }
+          }
+          dst[q4] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.tempty(ts));
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    sa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  Bars bars;
+  bars.base = sbase + P.bar_off;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.bar_off + Bars::kBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.bar_off + Bars::kBytes + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxS; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), 1);
+      mbar_init(bars.pfull(s), 4);
+    }
+    for (int t = 0; t < kMaxT; ++t) {
+      mbar_init(bars.sfull(t), 1);
+      mbar_init(bars.ofull(t), 1);
+      mbar_init(bars.tempty(t), 4);
+    }
+    mbar_init(bars.drain(), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kTmemWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(uint32_t(P.tmem_alloc))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    producer_role<D>(P, &tm_q, &tm_k, &tm_v, smem, sbase, bars, abort_flag);
+  } else if (warp == kMmaWarp) {
+    if ((threadIdx.x & 31) == 0) mma_role<D>(P, sbase, tmem_base, bars, abort_flag);
+  } else if (warp >= kFirstSoftmaxWarp) {
+    softmax_role<D>(P, smem, tmem_base, bars, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTmemWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(uint32_t(P.tmem_alloc))
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host
+struct Config {
+  int Bt, left, right, span_pad, s_stages, t_stages, cols_stage, tmem_alloc;
+  uint32_t qk_bytes, stage_bytes, sig_off, bar_off, smem_bytes;
+};
+
+static uint32_t round_up(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
+
+static bool device_has_tcgen05(int* sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (sm_count) cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev);
+  // This library is built for sm_103a only.
+  return major == 10 && minor == 3;
+}
+
+static bool make_config(const Problem& pb, Path path, Config& c) {
+  if (pb.d != 64 && pb.d != 128) return false;
+  if (kBM % pb.g != 0) return false;
+  c.Bt = kBM / pb.g;
+  if (path == kPathSA) {
+    c.left = c.right = pb.window / 2;
+  } else {
+    c.left = pb.window_swa - 1;
+    c.right = 0;
+  }
+  const long long span = (long long)c.Bt + c.left + c.right;
+  if (span > 512) return false;
+  c.span_pad = int(round_up(uint32_t(span), 32));
+  c.cols_stage = c.span_pad > pb.d ? c.span_pad : pb.d;
+  if (c.cols_stage > 512) return false;
+  c.t_stages = 512 / c.cols_stage;
+  if (c.t_stages > kMaxT) c.t_stages = kMaxT;
+  uint32_t alloc = 32;
+  while (alloc < uint32_t(c.t_stages * c.cols_stage)) alloc <<= 1;
+  c.tmem_alloc = int(alloc);
+  const uint32_t q_bytes = kBM * pb.d * 2;
+  const uint32_t k_bytes = uint32_t(c.span_pad) * pb.d * 2;
+  const uint32_t p_bytes = kBM * round_up(uint32_t(c.span_pad), 64) * 2;
+  c.qk_bytes = round_up(q_bytes + k_bytes > p_bytes ? q_bytes + k_bytes : p_bytes, 1024);
+  const uint32_t v_bytes = round_up(k_bytes, 1024);
+  c.stage_bytes = c.qk_bytes + v_bytes;
+  for (int s = kMaxS; s >= 1; --s) {
+    const uint32_t sig_off = uint32_t(s) * c.stage_bytes;
+    const uint32_t bar_off = round_up(sig_off + uint32_t(s) * c.span_pad * 4, 64);
+    const uint32_t total = bar_off + Bars::kBytes + 16 + 1024;  // + slot, flag, alignment slack
+    if (total <= kMaxSmem) {
+      c.s_stages = s;
+      c.sig_off = sig_off;
+      c.bar_off = bar_off;
+      c.smem_bytes = total < kMinSmem ? kMinSmem : total;
+      return true;
+    }
+  }
+  return false;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-gather view of a BSHD bf16 tensor: [rows, d] with 64-element boxes of
+// one row, 128-byte swizzle.
+static bool make_row_map(CUtensorMap* m, const void* base, uint64_t rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(d) * 2};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+bool tc_supported(const Problem& pb, Path path) {
+  if (path != kPathSA && path != kPathSWA) return false;
+  if (!tc::device_has_tcgen05(nullptr)) return false;
+  tc::Config c;
+  return tc::make_config(pb, path, c);
+}
+
+sa_status_t launch_tc(const Problem& pb, Path path, const float* gate, int accumulate,
+                      cudaStream_t stream) {
+  using namespace tc;
+  int sms = 0;
+  if (!device_has_tcgen05(&sms)) return fail(SA_ERR_UNSUPPORTED, "device is not sm_103");
+  Config c;
+  if (!make_config(pb, path, c)) return fail(SA_ERR_UNSUPPORTED, "shape does not fit the tcgen05 kernel");
+  CUtensorMap mq, mk, mv;
+  const uint64_t rows_q = uint64_t(pb.B) * pb.n * pb.Hq;
+  const uint64_t rows_kv = uint64_t(pb.B) * pb.n * pb.Hkv;
+  if (!make_row_map(&mq, pb.q, rows_q, pb.d) || !make_row_map(&mk, pb.k, rows_kv, pb.d) ||
+      !make_row_map(&mv, pb.v, rows_kv, pb.d))
+    return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  P.perm = pb.perm;
+  P.gate = gate;
+  P.out = static_cast<__nv_bfloat16*>(pb.out);
+  P.err = pb.err;
+  P.B = pb.B;
+  P.n = pb.n;
+  P.Hq = pb.Hq;
+  P.Hkv = pb.Hkv;
+  P.g = pb.g;
+  P.Bt = c.Bt;
+  P.left = c.left;
+  P.right = c.right;
+  P.span_pad = c.span_pad;
+  P.causal = (path == kPathSA) ? pb.causal : 0;
+  P.accumulate = accumulate;
+  P.identity = (path == kPathSWA) ? 1 : 0;
+  P.scale_log2 = pb.scale * 1.4426950408889634f;
+  P.tiles_per_seq = (pb.n + c.Bt - 1) / c.Bt;
+  P.num_tiles = P.tiles_per_seq * pb.B * pb.Hkv;
+  P.s_stages = c.s_stages;
+  P.t_stages = c.t_stages;
+  P.cols_stage = c.cols_stage;
+  P.tmem_alloc = c.tmem_alloc;
+  P.qk_bytes = c.qk_bytes;
+  P.stage_bytes = c.stage_bytes;
+  P.sig_off = c.sig_off;
+  P.bar_off = c.bar_off;
+  P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock
+  const int grid = P.num_tiles < sms ? P.num_tiles : sms;
+  cudaError_t ce;
+  if (pb.d == 128) {
+    ce = cudaFuncSetAttribute(sa_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(c.smem_bytes));
+    if (ce == cudaSuccess)
+      sa_tc_kernel<128><<<grid, kThreads, c.smem_bytes, stream>>>(mq, mk, mv, P);
+  } else {
+    ce = cudaFuncSetAttribute(sa_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(c.smem_bytes));
+    if (ce == cudaSuccess)
+      sa_tc_kernel<64><<<grid, kThreads, c.smem_bytes, stream>>>(mq, mk, mv, P);
+  }
+  if (ce == cudaSuccess) ce = cudaGetLastError();
+  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "tcgen05 kernel launch: %s", cudaGetErrorString(ce));
+  return SA_OK;
+}
+
+}  // namespace sa

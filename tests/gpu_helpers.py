@@ -1,0 +1,71 @@
+"""Shared helpers of the GPU parity tests (inputs, comparison, tolerances)."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import stochastic_sliding_window_gb300 as sa
+from sa_synth import make_case
+
+# bf16 kernels against the fp64 oracle: max-abs and relative-L2 bounds.
+MAX_ABS = 2e-2
+REL_L2 = 5e-3
+
+KERNELS = [sa.KERNEL_SIMT, sa.KERNEL_TCGEN05]
+KERNEL_IDS = ["simt", "tcgen05"]
+
+
+def dev_bf16(x: np.ndarray) -> torch.Tensor:
+    """Upload fp32 values that are already bf16-exact (conversion is exact)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to("cuda").to(torch.bfloat16)
+
+
+def dev_f32(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to("cuda")
+
+
+def perms(seed: int, layer: int, batch: int, n: int) -> tuple[np.ndarray, torch.Tensor]:
+    """sigma from the oracle's generator and the library's; they must agree."""
+    ora = np.stack([oracle.make_perm(seed, layer, b, n) for b in range(batch)])
+    lib = sa.make_perms(seed, layer, batch, n)
+    assert np.array_equal(ora, lib.astype(np.int64))
+    return ora, torch.from_numpy(lib).to("cuda")
+
+
+class Inputs:
+    def __init__(self, batch, n, hq, hkv, d, seed=0, std=None, gates=True):
+        self.case = make_case(batch, n, hq, hkv, d, seed, std=std, gates=gates)
+        c = self.case
+        self.q, self.k, self.v = dev_bf16(c.q), dev_bf16(c.k), dev_bf16(c.v)
+        if gates:
+            self.ga, self.gw = dev_f32(c.gate_sa), dev_f32(c.gate_swa)
+        self.shape = (batch, n, hq, hkv, d)
+
+
+def compare(got: torch.Tensor, want: np.ndarray, what: str = ""):
+    g = got.float().cpu().numpy().astype(np.float64)
+    assert g.shape == want.shape, (g.shape, want.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - want)
+    max_abs = float(err.max()) if err.size else 0.0
+    denom = float(np.linalg.norm(want))
+    rel = float(np.linalg.norm(g - want)) / denom if denom > 0 else float(np.linalg.norm(g))
+    assert max_abs <= MAX_ABS and rel <= REL_L2, f"{what}: max_abs={max_abs:.3e} rel_l2={rel:.3e}"
+    return max_abs, rel
+
+
+def sample_rows(batch: int, n: int, count: int, seed: int = 0) -> list[tuple[int, int]]:
+    """Seeded sample of (b, i) rows that always includes both sequence ends."""
+    rng = np.random.default_rng(seed)
+    rows = {(0, 0), (0, n - 1), (batch - 1, 0), (batch - 1, n - 1), (0, min(1, n - 1))}
+    while len(rows) < min(count, batch * n):
+        rows.add((int(rng.integers(batch)), int(rng.integers(n))))
+    return sorted(rows)
+
+
+def gather_rows(y: torch.Tensor, rows) -> torch.Tensor:
+    b = torch.tensor([r[0] for r in rows], device=y.device)
+    i = torch.tensor([r[1] for r in rows], device=y.device)
+    return y[b, i]

@@ -1,0 +1,172 @@
+"""GPU parity: libsa's kernels (called through the C ABI) against the fp64
+oracle on the same seeded inputs.
+
+Bar: max-abs <= 2e-2 and relative-L2 <= 5e-3 for bf16 outputs; sigma and
+sigma^{-1} bit-exact.  Small shapes compare every output element (several
+tiles and a ragged tail); the workload shapes compare seeded samples of rows
+that always include both sequence ends.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import stochastic_sliding_window_gb300 as sa
+from gpu_helpers import (KERNEL_IDS, KERNELS, Inputs, compare, gather_rows, perms,
+                         sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _run(path, inp, perm_d, w, causal, kernel, err, window_swa=0):
+    if path == "sa":
+        return sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=causal, kernel=kernel, err=err)
+    if path == "swa":
+        return sa.swa_forward(inp.q, inp.k, inp.v, w, kernel=kernel, err=err)
+    return sa.sa_swa_gated_forward(inp.q, inp.k, inp.v, perm_d, inp.ga, inp.gw, w,
+                                   window_swa=window_swa, causal=causal, kernel=kernel, err=err)
+
+
+def _want(path, inp, perm, w, causal, rows=None, window_swa=0):
+    c = inp.case
+    if path == "sa":
+        return oracle.sa_rows(c.q, c.k, c.v, perm, w, causal, rows=rows)
+    if path == "swa":
+        return oracle.swa_rows(c.q, c.k, c.v, w, rows=rows)
+    return oracle.gated_rows(c.q, c.k, c.v, perm, c.gate_sa, c.gate_swa, w,
+                             window_swa or None, causal, rows=rows)
+
+
+def _check_full(path, inp, perm, perm_d, w, causal, kernel, window_swa=0):
+    err = _err()
+    y = _run(path, inp, perm_d, w, causal, kernel, err, window_swa)
+    assert sa.check_error(err) == sa.SA_OK
+    assert sa.last_kernel() == kernel
+    b, n, hq, _, d = inp.shape
+    want = _want(path, inp, perm, w, causal, window_swa=window_swa).reshape(b, n, hq, d)
+    return compare(y, want, f"{path} w={w} causal={causal}")
+
+
+# ------------------------------------------------------------ tiny case, all paths
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
+@pytest.mark.parametrize("path,causal", [("sa", False), ("sa", True), ("swa", True),
+                                         ("gated", True), ("gated", False)])
+def test_tiny_case_all_paths(kernel, path, causal):
+    inp = Inputs(1, 256, 2, 2, 64, seed=0, std=1.0 / 8.0)
+    perm, perm_d = perms(0, 0, 1, 256)
+    _check_full(path, inp, perm, perm_d, 32, causal, kernel)
+
+
+# ------------------------------------------------------------ ragged / edge shapes
+
+EDGE = [
+    # n, hq, hkv, d, w
+    (1, 8, 2, 128, 4),
+    (7, 8, 2, 128, 1),
+    (100, 4, 4, 64, 7),
+    (333, 8, 2, 128, 64),
+    (513, 32, 8, 128, 128),
+    (1000, 16, 2, 64, 32),
+    (200, 8, 1, 128, 16),
+    (129, 2, 2, 64, 256),
+    (300, 8, 8, 128, 600),   # window wider than the sequence
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
+@pytest.mark.parametrize("n,hq,hkv,d,w", EDGE)
+@pytest.mark.parametrize("path,causal", [("sa", True), ("sa", False), ("swa", True), ("gated", True)])
+def test_ragged_and_edge_shapes(kernel, n, hq, hkv, d, w, path, causal):
+    inp = Inputs(2, n, hq, hkv, d, seed=n + w)
+    perm, perm_d = perms(5, 1, 2, n)
+    if kernel == sa.KERNEL_TCGEN05:
+        try:
+            _check_full(path, inp, perm, perm_d, w, causal, kernel)
+        except sa.SaError as e:
+            assert e.status == sa.SA_ERR_UNSUPPORTED  # window too wide for one tile
+            assert w >= 256 or path == "gated" and w >= 256
+        return
+    _check_full(path, inp, perm, perm_d, w, causal, kernel)
+
+
+def test_gated_separate_swa_window():
+    inp = Inputs(1, 700, 8, 2, 128, seed=3)
+    perm, perm_d = perms(3, 0, 1, 700)
+    for kernel in KERNELS:
+        _check_full("gated", inp, perm, perm_d, 64, True, kernel, window_swa=24)
+
+
+# ------------------------------------------------------------ pretraining-layer shape
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
+def test_pretraining_layer_gated(kernel):
+    """B4 n2048, 16 MHA heads, d64, w128, causal gated, N(0,1)/8 inputs."""
+    inp = Inputs(4, 2048, 16, 16, 64, seed=11, std=1.0 / 8.0)
+    perm, perm_d = perms(11, 0, 4, 2048)
+    rows = sample_rows(4, 2048, 600, seed=1)
+    err = _err()
+    y = _run("gated", inp, perm_d, 128, True, kernel, err)
+    assert sa.check_error(err) == sa.SA_OK
+    compare(gather_rows(y, rows), _want("gated", inp, perm, 128, True, rows=rows), "pretrain gated")
+
+
+# ------------------------------------------------------------ long-prefill GQA sweep
+
+@pytest.fixture(scope="module")
+def long_prefill():
+    return Inputs(1, 32768, 32, 8, 128, seed=21, gates=False)
+
+
+@pytest.mark.parametrize("w", [32, 64, 128, 256])
+def test_long_prefill_gqa_causal_sa(long_prefill, w):
+    inp = long_prefill
+    perm, perm_d = perms(21 + w, 0, 1, 32768)
+    rows = sample_rows(1, 32768, 300, seed=w)
+    err = _err()
+    y = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, err=err)
+    assert sa.check_error(err) == sa.SA_OK
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05
+    compare(gather_rows(y, rows), oracle.sa_rows(inp.case.q, inp.case.k, inp.case.v, perm, w, True,
+                                                 rows=rows), f"c3 w={w}")
+    # the CUDA-core kernel agrees on the same rows
+    y2 = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_SIMT, err=err)
+    assert sa.check_error(err) == sa.SA_OK
+    compare(gather_rows(y2, rows), oracle.sa_rows(inp.case.q, inp.case.k, inp.case.v, perm, w,
+                                                  True, rows=rows), f"c3 simt w={w}")
+
+
+# ------------------------------------------------------------ very long context
+
+@pytest.mark.parametrize("w", [1024, 2048])
+def test_very_long_context_gated(w):
+    inp = Inputs(1, 131072, 32, 4, 128, seed=31)
+    perm, perm_d = perms(31, 0, 1, 131072)
+    rows = sample_rows(1, 131072, 40, seed=w)
+    err = _err()
+    y = sa.sa_swa_gated_forward(inp.q, inp.k, inp.v, perm_d, inp.ga, inp.gw, w, causal=True, err=err)
+    assert sa.check_error(err) == sa.SA_OK
+    compare(gather_rows(y, rows), _want("gated", inp, perm, w, True, rows=rows), f"c4 w={w}")
+
+
+# ------------------------------------------------------------ length sweep
+
+@pytest.mark.parametrize("n", [2048, 8192, 262144])
+def test_length_sweep_causal_sa(n):
+    layers = 8 if n <= 8192 else 1
+    for layer in range(layers):
+        inp = Inputs(1, n, 16, 16, 128, seed=1000 * layer + n, gates=False)
+        perm, perm_d = perms(41, layer, 1, n)
+        rows = sample_rows(1, n, 64 if n > 8192 else 128, seed=layer)
+        err = _err()
+        y = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 128, causal=True, err=err)
+        assert sa.check_error(err) == sa.SA_OK
+        compare(gather_rows(y, rows), oracle.sa_rows(inp.case.q, inp.case.k, inp.case.v, perm, 128,
+                                                     True, rows=rows), f"c5 n={n} layer={layer}")
