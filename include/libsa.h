@@ -60,7 +60,8 @@ typedef enum sa_status {
   SA_ERR_UNSUPPORTED = 2, /* valid request this build cannot run (head_dim, alignment, kernel) */
   SA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
   SA_ERR_BAD_PERM = 4,    /* device check found perm entries out of range or repeated */
-  SA_ERR_TIMEOUT = 5      /* a device pipeline wait ran past its bound; results are invalid */
+  SA_ERR_TIMEOUT = 5,     /* a device pipeline wait ran past its bound; results are invalid */
+  SA_ERR_INTERNAL = 6     /* a device self-check of an internal index failed (a library bug) */
 } sa_status_t;
 
 /* Kernel choice (sa_params_t.kernel). */
@@ -74,6 +75,7 @@ enum {
 #define SA_ERRBIT_RANGE 1   /* a perm entry outside [0, seqlen) */
 #define SA_ERRBIT_DUP 2     /* two positions of perm name the same token */
 #define SA_ERRBIT_TIMEOUT 4 /* a bounded pipeline wait gave up */
+#define SA_ERRBIT_INTERNAL 8 /* an internal index self-check failed (a library bug); access skipped */
 
 typedef struct sa_params {
   int32_t batch;        /* B >= 1 */
@@ -151,8 +153,9 @@ sa_status_t sa_make_perm(uint64_t seed, int32_t layer, int32_t batch_index, int3
 
 /*
  * Synchronise `stream`, read the device error word (NULL: the library's own)
- * and map it to a status: SA_ERR_TIMEOUT if SA_ERRBIT_TIMEOUT is set, else
- * SA_ERR_BAD_PERM if a perm bit is set, else SA_OK.  The word is left as is.
+ * and map it to a status: SA_ERR_INTERNAL if SA_ERRBIT_INTERNAL is set, else
+ * SA_ERR_TIMEOUT if SA_ERRBIT_TIMEOUT is set, else SA_ERR_BAD_PERM if a perm
+ * bit is set, else SA_OK.  The word is left as is.
  */
 sa_status_t sa_check_error(const int32_t* d_err, cudaStream_t stream);
 

@@ -213,6 +213,8 @@ extern "C" sa_status_t sa_check_error(const int32_t* d_err, cudaStream_t stream)
   cudaError_t ce = cudaMemcpyAsync(&host, err, sizeof(host), cudaMemcpyDeviceToHost, stream);
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(stream);
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(ce));
+  if (host & SA_ERRBIT_INTERNAL)
+    return fail(SA_ERR_INTERNAL, "a device self-check of an internal index failed");
   if (host & SA_ERRBIT_TIMEOUT) return fail(SA_ERR_TIMEOUT, "a device wait ran past its bound");
   if (host & (SA_ERRBIT_RANGE | SA_ERRBIT_DUP))
     return fail(SA_ERR_BAD_PERM, "perm is not a permutation (error bits 0x%x)", host);
@@ -235,6 +237,7 @@ extern "C" const char* sa_status_string(sa_status_t status) {
     case SA_ERR_CUDA: return "SA_ERR_CUDA: CUDA runtime error";
     case SA_ERR_BAD_PERM: return "SA_ERR_BAD_PERM: perm is not a permutation";
     case SA_ERR_TIMEOUT: return "SA_ERR_TIMEOUT: device wait ran past its bound";
+    case SA_ERR_INTERNAL: return "SA_ERR_INTERNAL: device self-check failed";
   }
   return "unknown sa_status_t";
 }

@@ -155,6 +155,10 @@ __global__ void __launch_bounds__(kWarps * 32) sa_simt_kernel(const SimtArgs a) 
     }
   }
   const size_t out_row = (size_t(b) * a.n + i) * a.Hq + hq;
+  if (out_row >= size_t(total)) {  // never expected: record and skip
+    if (lane == 0) atomicOr(a.err, SA_ERRBIT_INTERNAL);
+    return;
+  }
   const __nv_bfloat16* qr = a.q + out_row * D;
   float* qs = qsm[warp];
   for (int e = lane; e < D; e += 32) qs[e] = __bfloat162float(qr[e]) * a.scale_log2;

@@ -66,7 +66,9 @@ struct Params {
   float scale_log2;
   int tiles_per_seq, num_tiles;
   int s_stages, t_stages, cols_stage, tmem_alloc;
+  int num_wg;  // softmax warpgroups taking alternate tiles (1 or 2)
   uint32_t qk_bytes, stage_bytes, sig_off, bar_off;
+  long long rows_q;  // B * n * Hq: bound of the scatter row index
   long long timeout_cycles;
 };
 
@@ -378,7 +380,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
   const int nch = P.span_pad / 32;
   int it = 0;
   for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, ++it) {
-    if (it % kNumWG != wg) continue;
+    if (wg >= P.num_wg || it % P.num_wg != wg) continue;
     const int s = it % S, ts = it % T;
     const uint32_t ph_s = uint32_t(it / S) & 1u, ph_t = uint32_t(it / T) & 1u;
     const TileCoord tc = decode(P, tile);
@@ -386,8 +388,12 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     if (!warp_wait(bars.full(s), ph_s, P, abort_flag)) break;  // sigma smem visibility
     tc_fence_after();
     const int32_t* sig = reinterpret_cast<const int32_t*>(smem + P.sig_off) + s * P.span_pad;
-    const bool row_valid = tc.p0 + t < P.n;
+    bool row_valid = tc.p0 + t < P.n;
     const int sig_p = sig[P.left + t];
+    if (row_valid && unsigned(sig_p) >= unsigned(P.n)) {  // never expected: record and skip
+      atomicOr(P.err, SA_ERRBIT_INTERNAL);
+      row_valid = false;
+    }
     const int lo = max(t, P.left - tc.p0);
     const int hi = row_valid ? min(t + P.left + P.right, P.n - 1 - tc.p0 + P.left) : lo - 1;
     const uint32_t trow = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(ts * P.cols_stage);
@@ -458,7 +464,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     if (!warp_wait(bars.ofull(ts), ph_t, P, abort_flag)) break;
     tc_fence_after();
     float mul = l > 0.f ? 1.f / l : 0.f;
-    const size_t orow = (size_t(tc.b) * P.n + sig_p) * P.Hq + size_t(tc.kvh) * P.g + j;
+    const size_t orow = row_valid ? (size_t(tc.b) * P.n + sig_p) * P.Hq + size_t(tc.kvh) * P.g + j : 0;
     if (P.gate != nullptr && row_valid) mul *= 1.f / (1.f + expf(-P.gate[orow]));
     __nv_bfloat16* op = P.out + orow * D;
 #pragma unroll
@@ -558,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host
 struct Config {
-  int Bt, left, right, span_pad, s_stages, t_stages, cols_stage, tmem_alloc;
+  int Bt, left, right, span_pad, s_stages, t_stages, cols_stage, tmem_alloc, num_wg;
   uint32_t qk_bytes, stage_bytes, sig_off, bar_off, smem_bytes;
 };
 
@@ -610,6 +616,12 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
       c.sig_off = sig_off;
       c.bar_off = bar_off;
       c.smem_bytes = total < kMinSmem ? kMinSmem : total;
+      // Tile `it` goes to warpgroup it % num_wg, smem stage it % S and TMEM
+      // stage it % T.  Each warpgroup must see every phase of the barriers
+      // it waits on, in order (a parity wait cannot tell phase k from k+2),
+      // so two warpgroups need S and T both multiples of 2.
+      c.num_wg = (c.s_stages >= 2 && c.t_stages >= 2) ? kNumWG : 1;
+      if (c.num_wg == 2) c.t_stages &= ~1;
       return true;
     }
   }
@@ -696,6 +708,8 @@ sa_status_t launch_tc(const Problem& pb, Path path, const float* gate, int accum
   P.t_stages = c.t_stages;
   P.cols_stage = c.cols_stage;
   P.tmem_alloc = c.tmem_alloc;
+  P.num_wg = c.num_wg;
+  P.rows_q = (long long)pb.B * pb.n * pb.Hq;
   P.qk_bytes = c.qk_bytes;
   P.stage_bytes = c.stage_bytes;
   P.sig_off = c.sig_off;

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings():
     lib = sa.load()
-    for st in range(6):
+    for st in range(7):
         s = lib.sa_status_string(st).decode()
         assert s.startswith("SA_")
     assert "unknown" in lib.sa_status_string(99).decode()
