@@ -356,7 +356,8 @@ def run_ours(args):
         config={k: wl[k] for k in ("workload", "batch", "seq_len", "num_q_heads", "num_kv_heads",
                                    "head_dim", "window", "causal", "path")}
         | dict(l2="flushed between steps (256 MB write); inputs 671 MB > L2",
-               kernel="tcgen05" if kernel == sa.KERNEL_TCGEN05 else "simt",
+               kernel={sa.KERNEL_SIMT: "simt", sa.KERNEL_TCGEN05_GATHER: "tcgen05-gather",
+                       sa.KERNEL_TCGEN05_RING: "tcgen05-ring"}.get(kernel, str(kernel)),
                parallelism="replicas" if world > 1 else "single-gpu"),
         roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
                       frac=achieved / peaks["hbm_gbs"], traffic=traffic,

@@ -66,9 +66,11 @@ typedef enum sa_status {
 
 /* Kernel choice (sa_params_t.kernel). */
 enum {
-  SA_KERNEL_AUTO = 0,   /* tcgen05 tensor-core kernel when the shape fits it, else SIMT */
-  SA_KERNEL_SIMT = 1,   /* CUDA-core kernel: any window, the correctness baseline */
-  SA_KERNEL_TCGEN05 = 2 /* tcgen05/TMEM kernel; SA_ERR_UNSUPPORTED if the shape does not fit */
+  SA_KERNEL_AUTO = 0,    /* a tcgen05 tensor-core kernel when the shape fits one, else SIMT */
+  SA_KERNEL_SIMT = 1,    /* CUDA-core kernel: any window, the correctness baseline */
+  SA_KERNEL_TCGEN05 = 2, /* the better-fitting tcgen05 kernel; SA_ERR_UNSUPPORTED if none fits */
+  SA_KERNEL_TCGEN05_GATHER = 3, /* tcgen05 kernel that gathers every window with TMA */
+  SA_KERNEL_TCGEN05_RING = 4    /* tcgen05 kernel with a sliding K/V ring (spans <= 160 keys) */
 };
 
 /* Bits of the device error word. */
@@ -168,8 +170,9 @@ const char* sa_status_string(sa_status_t status);
 /* Detail of the last failing call on this thread ("" if none). */
 const char* sa_last_error_message(void);
 
-/* SA_KERNEL_SIMT or SA_KERNEL_TCGEN05: the kernel the last successful forward
- * call on this thread launched (0 before any). */
+/* SA_KERNEL_SIMT, SA_KERNEL_TCGEN05_GATHER or SA_KERNEL_TCGEN05_RING: the
+ * kernel the last successful forward call on this thread launched (0 before
+ * any). */
 int32_t sa_last_kernel(void);
 
 /* Number of kernel launches the last successful forward call on this thread

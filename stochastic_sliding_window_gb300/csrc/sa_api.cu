@@ -43,7 +43,7 @@ static sa_status_t check_params(const sa_params_t* prm, bool need_window) {
   if (prm->head_dim != 64 && prm->head_dim != 128)
     return fail(SA_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", prm->head_dim);
   if (need_window && prm->window < 1) return fail(SA_ERR_INVALID_ARG, "window must be >= 1");
-  if (prm->kernel < SA_KERNEL_AUTO || prm->kernel > SA_KERNEL_TCGEN05)
+  if (prm->kernel < SA_KERNEL_AUTO || prm->kernel > SA_KERNEL_TCGEN05_RING)
     return fail(SA_ERR_INVALID_ARG, "unknown kernel selector %d", prm->kernel);
   const double rows = double(prm->batch) * prm->seqlen * prm->num_q_heads;
   if (rows * prm->head_dim >= 9.0e18 || double(prm->batch) * prm->seqlen >= 2147483647.0 ||
@@ -91,17 +91,37 @@ static sa_status_t finish(sa_status_t st, int32_t kernel, int32_t launches) {
   return st;
 }
 
+// The concrete kernel a request maps to for one path (SIMT, gather, ring),
+// or 0 when the requested tcgen05 variant cannot run this shape.
+static int32_t pick_kernel(const sa_params_t* prm, const Problem& pb, Path path) {
+  const bool ring = ring_supported(pb, path);
+  const bool gather = tc_supported(pb, path);
+  switch (prm->kernel) {
+    case SA_KERNEL_SIMT: return SA_KERNEL_SIMT;
+    case SA_KERNEL_TCGEN05_RING: return ring ? SA_KERNEL_TCGEN05_RING : 0;
+    case SA_KERNEL_TCGEN05_GATHER: return gather ? SA_KERNEL_TCGEN05_GATHER : 0;
+    case SA_KERNEL_TCGEN05:
+      return ring ? SA_KERNEL_TCGEN05_RING : gather ? SA_KERNEL_TCGEN05_GATHER : 0;
+    default:
+      return ring ? SA_KERNEL_TCGEN05_RING : gather ? SA_KERNEL_TCGEN05_GATHER : SA_KERNEL_SIMT;
+  }
+}
+
+static sa_status_t launch_kernel(int32_t kernel, const Problem& pb, Path path, const float* gate,
+                                 int accumulate, cudaStream_t s) {
+  if (kernel == SA_KERNEL_TCGEN05_RING) return launch_ring(pb, path, gate, accumulate, s);
+  return launch_tc(pb, path, gate, accumulate, s);
+}
+
 // Runs one single-path attention (SA or SWA) with the requested kernel.
 static sa_status_t run_single(const sa_params_t* prm, Problem& pb, Path path, cudaStream_t s) {
   if (pb.err == nullptr) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
-  const bool tc_ok = tc_supported(pb, path);
-  if (prm->kernel == SA_KERNEL_TCGEN05 && !tc_ok)
-    return fail(SA_ERR_UNSUPPORTED, "shape does not fit the tcgen05 kernel (window too wide, "
-                "Hq/Hkv does not divide 128, or a device without tcgen05)");
-  if (prm->kernel != SA_KERNEL_SIMT && tc_ok) {
-    return finish(launch_tc(pb, path, nullptr, 0, s), SA_KERNEL_TCGEN05, 1);
-  }
-  return finish(launch_simt(pb, path, s), SA_KERNEL_SIMT, 1);
+  const int32_t kernel = pick_kernel(prm, pb, path);
+  if (kernel == 0)
+    return fail(SA_ERR_UNSUPPORTED, "shape does not fit the requested tcgen05 kernel (window "
+                "too wide, Hq/Hkv does not divide 128, or a device without tcgen05)");
+  if (kernel == SA_KERNEL_SIMT) return finish(launch_simt(pb, path, s), SA_KERNEL_SIMT, 1);
+  return finish(launch_kernel(kernel, pb, path, nullptr, 0, s), kernel, 1);
 }
 
 }  // namespace sa
@@ -148,16 +168,17 @@ extern "C" sa_status_t sa_swa_gated_forward(const sa_params_t* params, const voi
   pb.gate_sa = gate_sa_logits;
   pb.gate_swa = gate_swa_logits;
   if (pb.err == nullptr) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
-  const bool tc_ok = tc_supported(pb, kPathSA) && tc_supported(pb, kPathSWA);
-  if (params->kernel == SA_KERNEL_TCGEN05 && !tc_ok)
-    return fail(SA_ERR_UNSUPPORTED, "shape does not fit the tcgen05 kernel");
-  if (params->kernel != SA_KERNEL_SIMT && tc_ok) {
+  const int32_t k_swa = pick_kernel(params, pb, kPathSWA);
+  const int32_t k_sa = pick_kernel(params, pb, kPathSA);
+  if (k_swa == 0 || k_sa == 0)
+    return fail(SA_ERR_UNSUPPORTED, "shape does not fit the requested tcgen05 kernel");
+  if (k_swa != SA_KERNEL_SIMT && k_sa != SA_KERNEL_SIMT) {
     // Pass 1 writes sigmoid(a_swa) * Y_swa into out; pass 2 adds
     // sigmoid(a_sa) * Y_sa row by row.  Stream order separates the passes and
     // sigma being a bijection means each pass writes each row exactly once.
-    st = launch_tc(pb, kPathSWA, pb.gate_swa, 0, stream);
+    st = launch_kernel(k_swa, pb, kPathSWA, pb.gate_swa, 0, stream);
     if (st != SA_OK) return st;
-    return finish(launch_tc(pb, kPathSA, pb.gate_sa, 1, stream), SA_KERNEL_TCGEN05, 2);
+    return finish(launch_kernel(k_sa, pb, kPathSA, pb.gate_sa, 1, stream), k_sa, 2);
   }
   return finish(launch_simt(pb, kPathGated, stream), SA_KERNEL_SIMT, 1);
 }

@@ -52,6 +52,13 @@ sa_status_t launch_tc(const Problem& pb, Path path, const float* gate, int accum
 // True when launch_tc can run this problem / path.
 bool tc_supported(const Problem& pb, Path path);
 
+// tcgen05 kernel with a sliding K/V ring in shared memory (each CTA walks a
+// contiguous run of tiles and fetches only the new rows of each window).
+// Same contract as launch_tc; narrower spans only.
+sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int accumulate,
+                        cudaStream_t stream);
+bool ring_supported(const Problem& pb, Path path);
+
 // sigma^{-1} kernels.
 sa_status_t launch_inverse_perm(const int32_t* perm, int32_t* inv, int batch, int n,
                                 int32_t* err, cudaStream_t stream);

@@ -39,19 +39,30 @@
 #include <mutex>
 
 #include "sa_internal.h"
+#include "sa_tc_common.cuh"
 
 namespace sa {
 namespace tc {
 
-constexpr int kThreads = 384;
+using namespace tcc;
+
+constexpr int kThreads = 384;  // three warpgroups
 constexpr int kProducerWarp = 0;
-constexpr int kMmaWarp = 1;
-constexpr int kTmemWarp = 2;
-constexpr int kFirstSoftmaxWarp = 4;
+constexpr int kMmaWarp = 1;  // also allocates and frees TMEM
+constexpr int kTmemWarp = 1;
+constexpr int kFirstSoftmaxWarp = 4;  // warpgroups 1 and 2 (warps 4-7, 8-11)
+// Register split: launched at kLaunchRegs per thread (384 x 168 = 64512),
+// warpgroup 0 (producer, MMA) gives registers back and the two softmax
+// warpgroups take them: 128 x 64 + 256 x 216 = 63488 <= 64512.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 64;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kNumWG = 2;
-constexpr int kBM = 128;  // MMA M: query rows per tile
 constexpr int kMaxS = 2;  // smem stages
 constexpr int kMaxT = 4;  // TMEM stages
+constexpr int kMaxRegChunks = 5;  // rows up to 160 columns are held in registers
 constexpr uint32_t kMaxSmem = 232448;     // 227 KB per CTA on sm_100-class parts
 constexpr uint32_t kMinSmem = 118 * 1024; // forces one resident CTA per SM
 
@@ -71,114 +82,6 @@ struct Params {
   long long rows_q;  // B * n * Hq: bound of the scatter row index
   long long timeout_cycles;
 };
-
-// ------------------------------------------------------------------ PTX
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-// Four arbitrary rows (one 64-element, 128-byte box each) of a 2-D bf16
-// tensor into 512 contiguous bytes of smem, 128B-swizzled.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(tm), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
-// start >> 4 in [0,14), LBO >> 4 in [16,30), SBO >> 4 in [32,46),
-// version 1 at bit 46, layout SWIZZLE_128B = 2 in [61,64)).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
-  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
-  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
-
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, dense.
-// D format [4,6) = 1 (F32); A format [7,10) = 1 (BF16); B format [10,13) = 1;
-// B major [16] (1 = MN-major); N >> 3 in [17,23); M >> 4 in [24,29).
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int nn, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn_major) << 16) |
-         (uint32_t(nn >> 3) << 17) | (uint32_t(m >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane; the wait is in the
-// same asm statement so no use of the outputs can be scheduled before it.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 // ------------------------------------------------------------------ layout
 struct Bars {
@@ -208,21 +111,10 @@ __device__ __forceinline__ TileCoord decode(const Params& P, int tile) {
   return c;
 }
 
-// Bounded wait.  Returns false if the wait expired (error bit set, abort
-// raised) or another role already aborted.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& P,
-                                          volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > P.timeout_cycles) {
-      *abort_flag = 1;
-      atomicOr(P.err, SA_ERRBIT_TIMEOUT);
-      return false;
-    }
-  }
+// Bounded wait on this kernel's timeout and error word.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& P,
+                                             volatile int* abort_flag) {
+  return bounded_wait(bar, parity, P.timeout_cycles, P.err, abort_flag);
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Params& P,
@@ -366,7 +258,10 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, co
   }
 }
 
-template <int D>
+// Softmax + epilogue warpgroups.  NCH > 0: the row's NCH*32 columns are read
+// from TMEM once and kept in registers; NCH == 0: wider spans, two passes
+// over TMEM in 32-column chunks.
+template <int D, int NCH, bool kCausal>
 __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base, const Bars& bars,
                              volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5;
@@ -377,7 +272,6 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
   const int t = r / P.g;
   const int j = r - t * P.g;
   const int S = P.s_stages, T = P.t_stages;
-  const int nch = P.span_pad / 32;
   int it = 0;
   for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, ++it) {
     if (wg >= P.num_wg || it % P.num_wg != wg) continue;
@@ -389,72 +283,57 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     tc_fence_after();
     const int32_t* sig = reinterpret_cast<const int32_t*>(smem + P.sig_off) + s * P.span_pad;
     bool row_valid = tc.p0 + t < P.n;
-    const int sig_p = sig[P.left + t];
-    if (row_valid && unsigned(sig_p) >= unsigned(P.n)) {  // never expected: record and skip
+    RowCtx rc;
+    rc.sig_p = sig[P.left + t];
+    if (row_valid && unsigned(rc.sig_p) >= unsigned(P.n)) {  // never expected: record and skip
       atomicOr(P.err, SA_ERRBIT_INTERNAL);
       row_valid = false;
     }
-    const int lo = max(t, P.left - tc.p0);
-    const int hi = row_valid ? min(t + P.left + P.right, P.n - 1 - tc.p0 + P.left) : lo - 1;
+    rc.lo = max(t, P.left - tc.p0);
+    rc.hi = row_valid ? min(t + P.left + P.right, P.n - 1 - tc.p0 + P.left) : rc.lo - 1;
+    rc.wlo = rc.lo;
+    rc.whi = rc.hi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      rc.wlo = max(rc.wlo, __shfl_xor_sync(0xffffffffu, rc.wlo, o));
+      rc.whi = min(rc.whi, __shfl_xor_sync(0xffffffffu, rc.whi, o));
+    }
+    rc.scale_log2 = P.scale_log2;
     const uint32_t trow = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(ts * P.cols_stage);
-
-    // pass 1: masked row max
-    float mx = -INFINITY;
-    for (int ch = 0; ch < nch; ++ch) {
-      uint32_t v[32];
-      tmem_ld32(trow + ch * 32, v);
-      const int c0 = ch * 32;
-      const int4* sg4 = reinterpret_cast<const int4*>(sig + c0);
-#pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const int4 sv = sg4[e4];
-        const int svv[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = c0 + e4 * 4 + u;
-          bool ok = (c >= lo) && (c <= hi);
-          if (P.causal) ok = ok && (svv[u] <= sig_p);
-          mx = ok ? fmaxf(mx, __uint_as_float(v[e4 * 4 + u])) : mx;
-        }
-      }
-    }
-    const float ms = (mx == -INFINITY) ? 0.f : mx * P.scale_log2;
-
-    // pass 2: p = exp2(s*scale*log2e - max), row sum, P (bf16) to smem
-    float l = 0.f;
     uint8_t* pbase = smem + size_t(s) * P.stage_bytes;
-    for (int ch = 0; ch < nch; ++ch) {
-      uint32_t v[32];
-      tmem_ld32(trow + ch * 32, v);
-      const int c0 = ch * 32;
-      const int4* sg4 = reinterpret_cast<const int4*>(sig + c0);
-      uint32_t pk[16];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+
+    if constexpr (NCH > 0) {
+      uint32_t v[NCH][32];
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const int4 sv = sg4[e4];
-        const int svv[4] = {sv.x, sv.y, sv.z, sv.w};
-        float pr[4];
+      for (int ch = 0; ch < NCH; ++ch) tmem_ld32_async(trow + ch * 32, v[ch]);
+      tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = c0 + e4 * 4 + u;
-          bool ok = (c >= lo) && (c <= hi);
-          if (P.causal) ok = ok && (svv[u] <= sig_p);
-          pr[u] = ok ? exp2f(fmaf(__uint_as_float(v[e4 * 4 + u]), P.scale_log2, -ms)) : 0.f;
-          l += pr[u];
-        }
-        pk[e4 * 2] = pack_bf16x2(pr[0], pr[1]);
-        pk[e4 * 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+      for (int ch = 0; ch < NCH; ++ch) reg_fence(v[ch]);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) mx = fmaxf(mx, mask_chunk<kCausal>(v[ch], sig, ch * 32, rc));
+      const float ms = (mx == -INFINITY) ? 0.f : mx * rc.scale_log2;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+        exp_store_chunk(v[ch], ms, rc.scale_log2, pbase, r, ch * 32, acc);
+    } else {
+      const int nch = P.span_pad / 32;
+      float mx = -INFINITY;
+      for (int ch = 0; ch < nch; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(trow + ch * 32, v);
+        mx = fmaxf(mx, mask_chunk<kCausal>(v, sig, ch * 32, rc));
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int col8 = c0 + q4 * 8;
-        const int kb = col8 >> 6;
-        const int c16 = (col8 & 63) >> 3;
-        uint4* dst = reinterpret_cast<uint4*>(pbase + kb * (kBM * 128) + r * 128 +
-                                              ((c16 ^ (r & 7)) << 4));
-        *dst = make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+      const float ms = (mx == -INFINITY) ? 0.f : mx * rc.scale_log2;
+      for (int ch = 0; ch < nch; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(trow + ch * 32, v);
+        mask_chunk<kCausal>(v, sig, ch * 32, rc);
+        exp_store_chunk(v, ms, rc.scale_log2, pbase, r, ch * 32, acc);
       }
     }
+    const float l = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncwarp();
@@ -464,14 +343,22 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     if (!warp_wait(bars.ofull(ts), ph_t, P, abort_flag)) break;
     tc_fence_after();
     float mul = l > 0.f ? 1.f / l : 0.f;
-    const size_t orow = row_valid ? (size_t(tc.b) * P.n + sig_p) * P.Hq + size_t(tc.kvh) * P.g + j : 0;
+    const size_t orow =
+        row_valid ? (size_t(tc.b) * P.n + rc.sig_p) * P.Hq + size_t(tc.kvh) * P.g + j : 0;
     if (P.gate != nullptr && row_valid) mul *= 1.f / (1.f + expf(-P.gate[orow]));
     __nv_bfloat16* op = P.out + orow * D;
+    uint32_t o[D / 32][32];
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t v[32];
-      tmem_ld32(trow + ch * 32, v);
-      if (row_valid) {
+    for (int ch = 0; ch < D / 32; ++ch) tmem_ld32_async(trow + ch * 32, o[ch]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) reg_fence(o[ch]);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.tempty(ts));  // O is in registers: TMEM stage free
+    if (row_valid) {
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
         uint4* dst = reinterpret_cast<uint4*>(op + ch * 32);
         uint4 prev[4];
         if (P.accumulate) {
@@ -482,7 +369,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
         for (int q4 = 0; q4 < 4; ++q4) {
           float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[q4 * 8 + e]) * mul;
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[ch][q4 * 8 + e]) * mul;
           if (P.accumulate) {
             const __nv_bfloat162* pv2 = reinterpret_cast<const __nv_bfloat162*>(&prev[q4]);
 #pragma unroll
@@ -497,13 +384,20 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
         }
       }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars.tempty(ts));
   }
 }
 
-template <int D>
+template <int D, int NCH>
+__device__ __forceinline__ void softmax_dispatch(const Params& P, uint8_t* smem,
+                                                 uint32_t tmem_base, const Bars& bars,
+                                                 volatile int* abort_flag) {
+  if (P.causal)
+    softmax_role<D, NCH, true>(P, smem, tmem_base, bars, abort_flag);
+  else
+    softmax_role<D, NCH, false>(P, smem, tmem_base, bars, abort_flag);
+}
+
+template <int D, int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
     sa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ Params P) {
@@ -544,21 +438,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == kProducerWarp) {
-    producer_role<D>(P, &tm_q, &tm_k, &tm_v, smem, sbase, bars, abort_flag);
-  } else if (warp == kMmaWarp) {
-    if ((threadIdx.x & 31) == 0) mma_role<D>(P, sbase, tmem_base, bars, abort_flag);
-  } else if (warp >= kFirstSoftmaxWarp) {
-    softmax_role<D>(P, smem, tmem_base, bars, abort_flag);
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kTmemWarp) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(uint32_t(P.tmem_alloc))
-                 : "memory");
+  // Each branch ends with the CTA-wide barrier of its own so that no code
+  // runs after the branches under two register limits.
+  if (warp >= kFirstSoftmaxWarp) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    softmax_dispatch<D, NCH>(P, smem, tmem_base, bars, abort_flag);
+    tc_fence_before();
+    __syncthreads();
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+    if (warp == kProducerWarp) {
+      producer_role<D>(P, &tm_q, &tm_k, &tm_v, smem, sbase, bars, abort_flag);
+    } else if (warp == kMmaWarp) {
+      if ((threadIdx.x & 31) == 0) mma_role<D>(P, sbase, tmem_base, bars, abort_flag);
+      __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTmemWarp) {
+      tc_fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(uint32_t(P.tmem_alloc))
+                   : "memory");
+    }
   }
 }
 
@@ -661,6 +563,41 @@ static bool make_row_map(CUtensorMap* m, const void* base, uint64_t rows, int d)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int D, int NCH>
+static cudaError_t launch_one(int grid, uint32_t smem, cudaStream_t stream, const CUtensorMap& mq,
+                              const CUtensorMap& mk, const CUtensorMap& mv, const Params& P) {
+  cudaError_t ce = cudaFuncSetAttribute(sa_tc_kernel<D, NCH>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (ce != cudaSuccess) return ce;
+  cudaFuncAttributes fa;
+  ce = cudaFuncGetAttributes(&fa, sa_tc_kernel<D, NCH>);
+  if (ce != cudaSuccess) return ce;
+  // The register split assumes the launch allocation; never launch otherwise.
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  int resident = 0;  // a CTA of this variant must fit on an SM (registers and smem)
+  ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, sa_tc_kernel<D, NCH>, kThreads,
+                                                     smem);
+  if (ce != cudaSuccess) return ce;
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  sa_tc_kernel<D, NCH><<<grid, kThreads, smem, stream>>>(mq, mk, mv, P);
+  return cudaGetLastError();
+}
+
+// NCH = span_pad / 32 when the whole row fits in registers, else 0.
+template <int D>
+static cudaError_t launch_variant(int nch, int grid, uint32_t smem, cudaStream_t stream,
+                                  const CUtensorMap& mq, const CUtensorMap& mk,
+                                  const CUtensorMap& mv, const Params& P) {
+  switch (nch) {
+    case 1: return launch_one<D, 1>(grid, smem, stream, mq, mk, mv, P);
+    case 2: return launch_one<D, 2>(grid, smem, stream, mq, mk, mv, P);
+    case 3: return launch_one<D, 3>(grid, smem, stream, mq, mk, mv, P);
+    case 4: return launch_one<D, 4>(grid, smem, stream, mq, mk, mv, P);
+    case 5: return launch_one<D, 5>(grid, smem, stream, mq, mk, mv, P);
+    default: return launch_one<D, 0>(grid, smem, stream, mq, mk, mv, P);
+  }
+}
+
 }  // namespace tc
 
 bool tc_supported(const Problem& pb, Path path) {
@@ -716,18 +653,12 @@ sa_status_t launch_tc(const Problem& pb, Path path, const float* gate, int accum
   P.bar_off = c.bar_off;
   P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock
   const int grid = P.num_tiles < sms ? P.num_tiles : sms;
+  const int nch = c.span_pad / 32 <= kMaxRegChunks ? c.span_pad / 32 : 0;
   cudaError_t ce;
-  if (pb.d == 128) {
-    ce = cudaFuncSetAttribute(sa_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(c.smem_bytes));
-    if (ce == cudaSuccess)
-      sa_tc_kernel<128><<<grid, kThreads, c.smem_bytes, stream>>>(mq, mk, mv, P);
-  } else {
-    ce = cudaFuncSetAttribute(sa_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(c.smem_bytes));
-    if (ce == cudaSuccess)
-      sa_tc_kernel<64><<<grid, kThreads, c.smem_bytes, stream>>>(mq, mk, mv, P);
-  }
+  if (pb.d == 128)
+    ce = launch_variant<128>(nch, grid, c.smem_bytes, stream, mq, mk, mv, P);
+  else
+    ce = launch_variant<64>(nch, grid, c.smem_bytes, stream, mq, mk, mv, P);
   if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "tcgen05 kernel launch: %s", cudaGetErrorString(ce));
   return SA_OK;

@@ -1,0 +1,244 @@
+// Device helpers shared by the tcgen05 kernels: inline PTX wrappers for
+// mbarriers, TMA, cp.async, tcgen05 (MMA, TMEM loads, fences), the shared
+// memory / instruction descriptors, and the per-row softmax pieces.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only)
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "libsa.h"  // SA_ERRBIT_*
+
+namespace sa {
+namespace tcc {
+
+constexpr int kBM = 128;  // MMA M: query rows per tile
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// Four arbitrary rows (one 64-element, 128-byte box each) of a 2-D bf16
+// tensor into 512 contiguous bytes of smem, 128B-swizzled.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tm), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
+// start >> 4 in [0,14), LBO >> 4 in [16,30), SBO >> 4 in [32,46),
+// version 1 at bit 46, layout SWIZZLE_128B = 2 in [61,64)).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, dense.
+// D format [4,6) = 1 (F32); A format [7,10) = 1 (BF16); B format [10,13) = 1;
+// B major [16] (1 = MN-major); N >> 3 in [17,23); M >> 4 in [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int nn, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn_major) << 16) |
+         (uint32_t(nn >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane; the wait is in the
+// same asm statement so no use of the outputs can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 16-byte global -> shared copy through L2 only (cp.async.cg).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival counts against the barrier's initial count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Wait on `bar` for the phase of the given parity, for at most `limit`
+// SM cycles.  On expiry sets SA_ERRBIT_TIMEOUT in *err and the CTA's abort
+// flag; returns false then, or when another role has already aborted.
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, long long limit,
+                                             int32_t* err, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(err, SA_ERRBIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// 2^x on the SFU (ex2.approx.ftz.f32); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Issue a 32-column TMEM load without waiting; pair with tmem_wait_ld()
+// followed by reg_fence() on every destination before the values are used.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Orders every later use of r after the preceding tmem_wait_ld().
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// Per-row state of one tile, shared by the softmax variants.
+struct RowCtx {
+  int lo, hi;      // attended column band of this row (sequence ends folded in)
+  int wlo, whi;    // band that holds for every row of the warp
+  int sig_p;       // original index of this row's query token
+  float scale_log2;
+};
+
+// Mask one 32-column chunk in registers: out-of-band and (causal) later
+// tokens become -inf.  Returns the chunk's masked maximum.
+template <bool kCausal>
+__device__ __forceinline__ float mask_chunk(uint32_t (&v)[32], const int32_t* sig, int c0,
+                                            const RowCtx& rc) {
+  const bool need_band = !(c0 >= rc.wlo && c0 + 31 <= rc.whi);  // warp-uniform
+  float m0 = -INFINITY, m1 = -INFINITY;
+  const int4* sg4 = reinterpret_cast<const int4*>(sig + c0);
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    int sv[4] = {0, 0, 0, 0};
+    if (kCausal) {
+      const int4 q4 = sg4[e4];
+      sv[0] = q4.x; sv[1] = q4.y; sv[2] = q4.z; sv[3] = q4.w;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + e4 * 4 + u;
+      bool ok = kCausal ? (sv[u] <= rc.sig_p) : true;
+      if (need_band) ok = ok && (c >= rc.lo) && (c <= rc.hi);
+      const float x = ok ? __uint_as_float(v[e4 * 4 + u]) : -INFINITY;
+      v[e4 * 4 + u] = __float_as_uint(x);
+      if (u & 1) m1 = fmaxf(m1, x); else m0 = fmaxf(m0, x);
+    }
+  }
+  return fmaxf(m0, m1);
+}
+
+// p = 2^(s * scale * log2 e - max) for one masked chunk; bf16 P to smem in
+// the K-major 128B-swizzled layout the PV MMA reads; adds to the row sums.
+__device__ __forceinline__ void exp_store_chunk(const uint32_t (&v)[32], float ms, float sl2,
+                                                uint8_t* pbase, int r, int c0, float (&acc)[4]) {
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const float p0 = fast_exp2(fmaf(__uint_as_float(v[q4 * 8 + 2 * e2]), sl2, -ms));
+      const float p1 = fast_exp2(fmaf(__uint_as_float(v[q4 * 8 + 2 * e2 + 1]), sl2, -ms));
+      acc[e2] += p0 + p1;
+      pk[e2] = pack_bf16x2(p0, p1);
+    }
+    const int col8 = c0 + q4 * 8;
+    const int kb = col8 >> 6;
+    const int c16 = (col8 & 63) >> 3;
+    uint4* dst = reinterpret_cast<uint4*>(pbase + kb * (kBM * 128) + r * 128 +
+                                          ((c16 ^ (r & 7)) << 4));
+    *dst = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+}  // namespace tcc
+}  // namespace sa

@@ -1,0 +1,590 @@
+// tcgen05 kernel for SA / SWA with a sliding K/V ring in shared memory.
+//
+// Same attention as sa_tc.cu (Stochastic Attention summary, "Core mechanism"
+// steps 1-3; causal rule from "Theoretical properties"; SWA from "Problem
+// statement"): a tile is Bt = 128/g consecutive permuted positions of one
+// (sequence, kv head) pair stacked with the g query heads of that kv head
+// (M = 128 rows), attending over the contiguous permuted key span
+// [p0 - left, p0 + Bt - 1 + right].
+//
+// What differs from the gather kernel is how the operands reach shared
+// memory.  Each CTA takes a CONTIGUOUS run of tiles.  Consecutive tiles of a
+// sequence share all but Bt rows of their key span, so K and V live in a
+// ring of R = span + Bt rows and each tile fetches only its Bt new rows
+// (plus its 128 Q rows); the first tile of a run fetches the whole span.
+// Three producer warps fetch rows with 16-byte cp.async copies, computing
+// the 128-byte swizzle themselves, so a gathered row costs one coalesced
+// 256-byte request and no per-row TMA descriptor walk.  The key tokens
+// sigma[q] of the ring are kept twice (slots s and s + R) so that a tile's
+// span is always a plain contiguous array.
+//
+// Roles (three warpgroups, 384 threads):
+//   warps 0-2   producers: sigma of new positions, cp.async of Q / K / V rows
+//   warp 3      lane 0 issues the MMAs; the warp owns TMEM
+//   warps 4-7   softmax + epilogue of even tiles (TMEM stage 0)
+//   warps 8-11  softmax + epilogue of odd tiles  (TMEM stage 1)
+// Per tile: S = Q K^T (one or two MMAs when the span wraps the ring) into
+// TMEM; the row's whole window is read once into registers, masked (band,
+// sequence ends, causal sigma[q] <= sigma[p]), exponentiated and written as
+// bf16 P to shared memory; O = P V (V used MN-major straight from the ring)
+// into TMEM; the epilogue scales by 1/rowsum, optionally applies the gate
+// and the previous out row, and scatters row sigma[p0+t].
+// Every wait is bounded (SA_ERRBIT_TIMEOUT); producer copies are drained
+// before exit.
+#include "sa_internal.h"
+#include "sa_tc_common.cuh"
+
+#include <cstring>
+
+namespace sa {
+namespace ring {
+
+using namespace tcc;
+
+constexpr int kThreads = 384;
+constexpr int kProducers = 96;  // warps 0-2
+constexpr int kMmaWarp = 3;
+constexpr int kFirstSoftmaxWarp = 4;
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 64;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr int kMaxChunks = 5;  // spans up to 160 columns (whole row in registers)
+constexpr uint32_t kMaxSmem = 232448;
+
+struct Params {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const int32_t* perm;  // [B, n]; unused when identity
+  const float* gate;    // [B, n, Hq] logits or nullptr
+  __nv_bfloat16* out;
+  int32_t* err;
+  int B, n, Hq, Hkv, g, log2g, Bt;
+  int left, right, span_pad, R;
+  int causal, accumulate, identity;
+  float scale_log2;
+  int tiles_per_seq, num_tiles;
+  int cols_stage, tmem_alloc;
+  uint32_t q_bytes, off_k, off_v, off_p, off_sig, off_bar;
+  long long timeout_cycles;
+};
+
+// Barrier slots (8 bytes each) after off_bar.
+enum : uint32_t {
+  kFull = 0,     // [2] Q stage + new ring rows of tile it landed (and sigma written)
+  kEmpty = 2,    // [2] tile it retired (PV done): Q stage and its oldest ring rows free
+  kSfull = 4,    // [2] S of tile it in TMEM stage it & 1
+  kOfull = 6,    // [2] O of tile it in TMEM stage it & 1
+  kTempty = 8,   // [2] TMEM stage read out by the epilogue
+  kPfull = 10,   // P of the current tile written
+  kPfree = 11,   // P buffer consumed by the PV of the previous tile
+  kDrain = 12,   // final MMA completion
+  kNumBars = 13,
+};
+
+__device__ __forceinline__ uint32_t mod_ring(int x, int R) {
+  const int m = x % R;
+  return uint32_t(m < 0 ? m + R : m);
+}
+
+// Tiles of this CTA: a contiguous range, split evenly over the grid.
+__device__ __forceinline__ void cta_range(const Params& P, int& begin, int& end) {
+  begin = int((long long)blockIdx.x * P.num_tiles / gridDim.x);
+  end = int((long long)(blockIdx.x + 1) * P.num_tiles / gridDim.x);
+}
+
+// Walks this CTA's tiles keeping the ring mapping: a run of one sequence
+// maps key position q to ring slot (q - seg_q0) mod R.
+struct TileWalk {
+  int seq = -1, seg_q0 = 0;
+  int b, kvh, p0, slot_a;
+  bool new_seg;
+  __device__ __forceinline__ void step(const Params& P, int tile) {
+    const int s = tile / P.tiles_per_seq;
+    p0 = (tile - s * P.tiles_per_seq) * P.Bt;
+    b = s / P.Hkv;
+    kvh = s - b * P.Hkv;
+    new_seg = (s != seq);
+    if (new_seg) {
+      seq = s;
+      seg_q0 = p0 - P.left;
+    }
+    slot_a = int(mod_ring(p0 - P.left - seg_q0, P.R));
+  }
+};
+
+template <int D>
+__device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, uint32_t bars,
+                              volatile int* abort_flag, volatile int* vote) {
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  constexpr int RPP = kProducers / CPR;  // rows per pass of the 96 threads
+  const int tid = threadIdx.x;
+  const int c = tid % CPR;
+  const int r_first = tid / CPR;
+  const int kb = c >> 3;
+  const int c8 = c & 7;
+  int32_t* sig2 = reinterpret_cast<int32_t*>(smem + P.off_sig);
+  const uint32_t sk = sbase + P.off_k, sv = sbase + P.off_v;
+  int begin, end;
+  cta_range(P, begin, end);
+  TileWalk tw;
+  int it = 0;
+  for (int tile = begin; tile < end; ++tile, ++it) {
+    const int s = it & 1;
+    tw.step(P, tile);
+    // tile it-2 retired (its Q stage and the ring rows this load overwrites);
+    // a new run reloads the whole span, so tile it-1 must be done as well.
+    if (tid == 0) {
+      bool ok = bounded_wait(bars + 8 * (kEmpty + s), ((it >> 1) & 1) ^ 1, P.timeout_cycles,
+                             P.err, abort_flag);
+      if (ok && tw.new_seg && it > 0)
+        ok = bounded_wait(bars + 8 * (kEmpty + (s ^ 1)), ((it - 1) >> 1) & 1, P.timeout_cycles,
+                          P.err, abort_flag);
+      *vote = ok ? 1 : 0;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
+    if (!*vote) break;
+    const int win0 = tw.p0 - P.left;
+    const int ld0 = tw.new_seg ? win0 : win0 + P.span_pad - P.Bt;
+    const int nld = tw.new_seg ? P.span_pad : P.Bt;
+    const int32_t* perm_b = P.identity ? nullptr : P.perm + size_t(tw.b) * P.n;
+    for (int i = tid; i < nld; i += kProducers) {
+      const int qpos = ld0 + i;
+      const int qc = min(max(qpos, 0), P.n - 1);
+      int tok = perm_b ? __ldg(perm_b + qc) : qc;
+      if (unsigned(tok) >= unsigned(P.n)) {
+        atomicOr(P.err, SA_ERRBIT_RANGE);
+        tok = 0;
+      }
+      const uint32_t sl = mod_ring(qpos - tw.seg_q0, P.R);
+      sig2[sl] = tok;
+      sig2[sl + P.R] = tok;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
+    const uint32_t full = bars + 8 * (kFull + s);
+    if (tid == 0) mbar_arrive(full);  // releases the sigma writes above
+    // Q: 128 rows (r = t*g + j), 2 K-blocks of [128 rows x 128 B], swizzled
+    const uint32_t sq = sbase + uint32_t(s) * P.q_bytes;
+    const int32_t* sig_win = sig2 + tw.slot_a;
+    const size_t rowbase = size_t(tw.b) * P.n;
+    for (int r = r_first; r < kBM; r += RPP) {
+      const int t = r >> P.log2g;
+      const int j = r & (P.g - 1);
+      const int tok = sig_win[P.left + t];
+      const __nv_bfloat16* src = P.q + ((rowbase + tok) * P.Hq + tw.kvh * P.g + j) * D + c * 8;
+      cp_async16(sq + kb * (kBM * 128) + r * 128 + ((c8 ^ (r & 7)) << 4), src);
+    }
+    // K and V: the new positions of the span
+    for (int i = r_first; i < nld; i += RPP) {
+      const uint32_t sl = mod_ring(ld0 + i - tw.seg_q0, P.R);
+      const int tok = sig2[sl];
+      const size_t off = ((rowbase + tok) * P.Hkv + tw.kvh) * D + c * 8;
+      const uint32_t d = kb * (P.R * 128) + sl * 128 + ((c8 ^ (sl & 7)) << 4);
+      cp_async16(sk + d, P.k + off);
+      cp_async16(sv + d, P.v + off);
+    }
+    cp_async_arrive_noinc(full);
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // own copies land before exit
+}
+
+template <int D>
+__device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, uint32_t bars,
+                         volatile int* abort_flag) {
+  int begin, end;
+  cta_range(P, begin, end);
+  const uint32_t ka = sbase + P.off_k, va = sbase + P.off_v, pa = sbase + P.off_p;
+  const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
+  auto wait = [&](uint32_t bar, uint32_t par) {
+    return bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
+  };
+  auto qk = [&](int it, int slot_a) -> bool {
+    const int s = it & 1;
+    if (!wait(bars + 8 * (kFull + s), (it >> 1) & 1)) return false;
+    fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
+    if (!wait(bars + 8 * (kTempty + s), ((it >> 1) & 1) ^ 1)) return false;
+    tc_fence_after();
+    const uint32_t d = tmem_base + uint32_t(s * P.cols_stage);
+    const uint32_t qa = sbase + uint32_t(s) * P.q_bytes;
+    const int n1 = min(P.span_pad, P.R - slot_a);
+    const int n2 = P.span_pad - n1;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t koff = uint32_t(kk & 3) * 32u;
+      const uint64_t a = sdesc_sw128(qa + (kk >> 2) * (kBM * 128) + koff, 16, 1024);
+      const uint32_t kblk = ka + (kk >> 2) * (P.R * 128) + koff;
+      umma_bf16(d, a, sdesc_sw128(kblk + slot_a * 128, 16, 1024), idesc_bf16(kBM, n1, 0),
+                kk > 0 ? 1u : 0u);
+      if (n2 > 0)
+        umma_bf16(d + n1, a, sdesc_sw128(kblk, 16, 1024), idesc_bf16(kBM, n2, 0),
+                  kk > 0 ? 1u : 0u);
+    }
+    umma_commit(bars + 8 * (kSfull + s));
+    return true;
+  };
+  auto pv = [&](int it, int slot_a) -> bool {
+    const int s = it & 1;
+    if (!wait(bars + 8 * kPfull, it & 1)) return false;
+    tc_fence_after();
+    const uint32_t o = tmem_base + uint32_t(s * P.cols_stage);
+    const int ksteps = P.span_pad / 16;
+    for (int kk = 0; kk < ksteps; ++kk) {
+      const uint64_t a = sdesc_sw128(pa + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+      const uint32_t vs = mod_ring(slot_a + 16 * kk, P.R);
+      const uint64_t bd = sdesc_sw128(va + vs * 128, P.R * 128, 1024);
+      umma_bf16(o, a, bd, idesc_pv, kk > 0 ? 1u : 0u);
+    }
+    umma_commit(bars + 8 * kPfree);
+    umma_commit(bars + 8 * (kOfull + s));
+    umma_commit(bars + 8 * (kEmpty + s));
+    return true;
+  };
+  TileWalk tw;
+  bool ok = true;
+  int it = 0, prev_slot = 0;
+  for (int tile = begin; tile < end; ++tile, ++it) {
+    tw.step(P, tile);
+    // A new run reloads the whole ring, which waits for the previous tile's
+    // PV: issue that PV before waiting for this tile's operands.
+    const bool pv_first = it > 0 && tw.new_seg;
+    if (pv_first && !pv(it - 1, prev_slot)) { ok = false; break; }
+    if (!qk(it, tw.slot_a)) { ok = false; break; }
+    if (it > 0 && !pv_first && !pv(it - 1, prev_slot)) { ok = false; break; }
+    prev_slot = tw.slot_a;
+  }
+  if (ok && it > 0) pv(it - 1, prev_slot);
+  umma_commit(bars + 8 * kDrain);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bars + 8 * kDrain, 0) && clock64() - t0 < P.timeout_cycles) {
+  }
+}
+
+template <int D, int NCH, bool kCausal>
+__device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base, uint32_t bars,
+                             volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wg = (warp - kFirstSoftmaxWarp) >> 2;  // also this warpgroup's TMEM stage
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;
+  const int t = r >> P.log2g;
+  const int j = r & (P.g - 1);
+  const int32_t* sig2 = reinterpret_cast<const int32_t*>(smem + P.off_sig);
+  uint8_t* pbase = smem + P.off_p;
+  const uint32_t trow = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(wg * P.cols_stage);
+  auto wwait = [&](uint32_t bar, uint32_t par) {
+    const bool ok = bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+  };
+  int begin, end;
+  cta_range(P, begin, end);
+  TileWalk tw;
+  int it = 0;
+  for (int tile = begin; tile < end; ++tile, ++it) {
+    tw.step(P, tile);
+    if ((it & 1) != wg) continue;
+    const uint32_t ph = uint32_t(it >> 1) & 1u;
+    if (!wwait(bars + 8 * (kSfull + wg), ph)) break;
+    if (!wwait(bars + 8 * (kFull + wg), ph)) break;  // sigma of the ring is visible
+    tc_fence_after();
+    const int32_t* sig = sig2 + tw.slot_a;  // sigma of span column c is sig[c]
+    bool row_valid = tw.p0 + t < P.n;
+    RowCtx rc;
+    rc.sig_p = sig[P.left + t];
+    if (row_valid && unsigned(rc.sig_p) >= unsigned(P.n)) {  // never expected: record, skip
+      atomicOr(P.err, SA_ERRBIT_INTERNAL);
+      row_valid = false;
+    }
+    rc.lo = max(t, P.left - tw.p0);
+    rc.hi = row_valid ? min(t + P.left + P.right, P.n - 1 - tw.p0 + P.left) : rc.lo - 1;
+    rc.wlo = rc.lo;
+    rc.whi = rc.hi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      rc.wlo = max(rc.wlo, __shfl_xor_sync(0xffffffffu, rc.wlo, o));
+      rc.whi = min(rc.whi, __shfl_xor_sync(0xffffffffu, rc.whi, o));
+    }
+    rc.scale_log2 = P.scale_log2;
+
+    uint32_t v[NCH][32];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) tmem_ld32_async(trow + ch * 32, v[ch]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) reg_fence(v[ch]);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) mx = fmaxf(mx, mask_chunk<kCausal>(v[ch], sig, ch * 32, rc));
+    const float ms = (mx == -INFINITY) ? 0.f : mx * rc.scale_log2;
+    // The single P buffer is free once the previous tile's PV has run (phase
+    // it-1 of kPfree).  This warpgroup saw PV(it-2) finish (its epilogue), and
+    // PV(it) needs this tile's P, so the barrier's current phase is it-1 or
+    // it: the parity wait on phase it-1 is unambiguous.  (Waiting on an older
+    // phase as well would alias onto phase it and never return.)
+    if (it >= 1 && !wwait(bars + 8 * kPfree, uint32_t(it - 1) & 1u)) break;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) exp_store_chunk(v[ch], ms, rc.scale_log2, pbase, r, ch * 32, acc);
+    const float l = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * kPfull);
+
+    // epilogue
+    if (!wwait(bars + 8 * (kOfull + wg), ph)) break;
+    tc_fence_after();
+    float mul = l > 0.f ? 1.f / l : 0.f;
+    const size_t orow =
+        row_valid ? (size_t(tw.b) * P.n + rc.sig_p) * P.Hq + size_t(tw.kvh) * P.g + j : 0;
+    if (P.gate != nullptr && row_valid) mul *= 1.f / (1.f + expf(-P.gate[orow]));
+    uint32_t o[D / 32][32];
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) tmem_ld32_async(trow + ch * 32, o[ch]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) reg_fence(o[ch]);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kTempty + wg));
+    if (row_valid) {
+      __nv_bfloat16* op = P.out + orow * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint4* dst = reinterpret_cast<uint4*>(op + ch * 32);
+        uint4 prev[4];
+        if (P.accumulate) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) prev[q4] = dst[q4];
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[ch][q4 * 8 + e]) * mul;
+          if (P.accumulate) {
+            const __nv_bfloat162* pv2 = reinterpret_cast<const __nv_bfloat162*>(&prev[q4]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 pf = __bfloat1622float2(pv2[e]);
+              f[2 * e] += pf.x;
+              f[2 * e + 1] += pf.y;
+            }
+          }
+          dst[q4] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        }
+      }
+    }
+  }
+}
+
+template <int D, int NCH>
+__global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_constant__ Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + P.off_bar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.off_bar + 8 * kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 4);
+  volatile int* vote = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 8);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bars + 8 * (kFull + s), kProducers + 1);
+      mbar_init(bars + 8 * (kEmpty + s), 1);
+      mbar_init(bars + 8 * (kSfull + s), 1);
+      mbar_init(bars + 8 * (kOfull + s), 1);
+      mbar_init(bars + 8 * (kTempty + s), 4);
+    }
+    mbar_init(bars + 8 * kPfull, 4);
+    mbar_init(bars + 8 * kPfree, 1);
+    mbar_init(bars + 8 * kDrain, 1);
+    *abort_flag = 0;
+    *vote = 1;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(uint32_t(P.tmem_alloc))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Each branch ends with its own CTA-wide barrier: no code runs after the
+  // branches under two register limits.
+  if (warp >= kFirstSoftmaxWarp) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    if (P.causal)
+      softmax_role<D, NCH, true>(P, smem, tmem_base, bars, abort_flag);
+    else
+      softmax_role<D, NCH, false>(P, smem, tmem_base, bars, abort_flag);
+    tc_fence_before();
+    __syncthreads();
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+    if (warp < kMmaWarp) {
+      producer_role<D>(P, smem, sbase, bars, abort_flag, vote);
+    } else {
+      if ((threadIdx.x & 31) == 0) mma_role<D>(P, sbase, tmem_base, bars, abort_flag);
+      __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+      tc_fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(uint32_t(P.tmem_alloc))
+                   : "memory");
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host
+struct Config {
+  int Bt, log2g, left, right, span_pad, R, cols_stage, tmem_alloc;
+  uint32_t q_bytes, off_k, off_v, off_p, off_sig, off_bar, smem_bytes;
+};
+
+static uint32_t round_up(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
+
+static bool make_config(const Problem& pb, Path path, Config& c) {
+  if (pb.d != 64 && pb.d != 128) return false;
+  if (kBM % pb.g != 0) return false;
+  c.Bt = kBM / pb.g;
+  if (c.Bt % 16 != 0) return false;  // ring offsets must be whole 16-row MMA steps
+  c.log2g = 0;
+  while ((1 << c.log2g) < pb.g) ++c.log2g;
+  if (path == kPathSA) {
+    c.left = c.right = pb.window / 2;
+  } else {
+    c.left = pb.window_swa - 1;
+    c.right = 0;
+  }
+  const long long span = (long long)c.Bt + c.left + c.right;
+  if (span > 32LL * kMaxChunks) return false;
+  c.span_pad = int(round_up(uint32_t(span), 32));
+  c.R = int(round_up(uint32_t(c.span_pad + c.Bt), 16));
+  c.cols_stage = int(round_up(uint32_t(c.span_pad > pb.d ? c.span_pad : pb.d), 32));
+  uint32_t alloc = 32;
+  while (alloc < uint32_t(2 * c.cols_stage)) alloc <<= 1;
+  if (alloc > 512) return false;
+  c.tmem_alloc = int(alloc);
+  c.q_bytes = kBM * pb.d * 2;
+  const uint32_t ring_bytes = uint32_t(c.R) * pb.d * 2;
+  c.off_k = 2 * c.q_bytes;
+  c.off_v = c.off_k + ring_bytes;
+  c.off_p = c.off_v + ring_bytes;
+  c.off_sig = c.off_p + kBM * round_up(uint32_t(c.span_pad), 64) * 2;
+  c.off_bar = round_up(c.off_sig + 2u * c.R * 4, 64);
+  c.smem_bytes = c.off_bar + 8 * kNumBars + 16 + 1024;  // + slot, flags, alignment slack
+  return c.smem_bytes <= kMaxSmem;
+}
+
+static bool device_sm103(int* sms) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (sms) cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  return major == 10 && minor == 3;
+}
+
+template <int D, int NCH>
+static cudaError_t launch_one(int grid, uint32_t smem, cudaStream_t stream, const Params& P) {
+  cudaError_t ce = cudaFuncSetAttribute(sa_ring_kernel<D, NCH>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (ce != cudaSuccess) return ce;
+  cudaFuncAttributes fa;
+  ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, NCH>);
+  if (ce != cudaSuccess) return ce;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;  // register split
+  int resident = 0;
+  ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, sa_ring_kernel<D, NCH>, kThreads,
+                                                     smem);
+  if (ce != cudaSuccess) return ce;
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  sa_ring_kernel<D, NCH><<<grid, kThreads, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_variant(int nch, int grid, uint32_t smem, cudaStream_t stream,
+                                  const Params& P) {
+  switch (nch) {
+    case 1: return launch_one<D, 1>(grid, smem, stream, P);
+    case 2: return launch_one<D, 2>(grid, smem, stream, P);
+    case 3: return launch_one<D, 3>(grid, smem, stream, P);
+    case 4: return launch_one<D, 4>(grid, smem, stream, P);
+    default: return launch_one<D, 5>(grid, smem, stream, P);
+  }
+}
+
+}  // namespace ring
+
+bool ring_supported(const Problem& pb, Path path) {
+  if (path != kPathSA && path != kPathSWA) return false;
+  if (!ring::device_sm103(nullptr)) return false;
+  ring::Config c;
+  return ring::make_config(pb, path, c);
+}
+
+sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int accumulate,
+                        cudaStream_t stream) {
+  using namespace ring;
+  int sms = 0;
+  if (!device_sm103(&sms)) return fail(SA_ERR_UNSUPPORTED, "device is not sm_103");
+  Config c;
+  if (!make_config(pb, path, c)) return fail(SA_ERR_UNSUPPORTED, "shape does not fit the ring kernel");
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  P.q = static_cast<const __nv_bfloat16*>(pb.q);
+  P.k = static_cast<const __nv_bfloat16*>(pb.k);
+  P.v = static_cast<const __nv_bfloat16*>(pb.v);
+  P.perm = pb.perm;
+  P.gate = gate;
+  P.out = static_cast<__nv_bfloat16*>(pb.out);
+  P.err = pb.err;
+  P.B = pb.B;
+  P.n = pb.n;
+  P.Hq = pb.Hq;
+  P.Hkv = pb.Hkv;
+  P.g = pb.g;
+  P.log2g = c.log2g;
+  P.Bt = c.Bt;
+  P.left = c.left;
+  P.right = c.right;
+  P.span_pad = c.span_pad;
+  P.R = c.R;
+  P.causal = (path == kPathSA) ? pb.causal : 0;
+  P.accumulate = accumulate;
+  P.identity = (path == kPathSWA) ? 1 : 0;
+  P.scale_log2 = pb.scale * 1.4426950408889634f;
+  P.tiles_per_seq = (pb.n + c.Bt - 1) / c.Bt;
+  P.num_tiles = P.tiles_per_seq * pb.B * pb.Hkv;
+  P.cols_stage = c.cols_stage;
+  P.tmem_alloc = c.tmem_alloc;
+  P.q_bytes = c.q_bytes;
+  P.off_k = c.off_k;
+  P.off_v = c.off_v;
+  P.off_p = c.off_p;
+  P.off_sig = c.off_sig;
+  P.off_bar = c.off_bar;
+  P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock
+  const int grid = P.num_tiles < sms ? P.num_tiles : sms;
+  const int nch = c.span_pad / 32;
+  const cudaError_t ce = (pb.d == 128) ? launch_variant<128>(nch, grid, c.smem_bytes, stream, P)
+                                       : launch_variant<64>(nch, grid, c.smem_bytes, stream, P);
+  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "ring kernel launch: %s", cudaGetErrorString(ce));
+  return SA_OK;
+}
+
+}  // namespace sa

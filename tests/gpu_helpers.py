@@ -13,8 +13,44 @@ from sa_synth import make_case
 MAX_ABS = 2e-2
 REL_L2 = 5e-3
 
-KERNELS = [sa.KERNEL_SIMT, sa.KERNEL_TCGEN05]
-KERNEL_IDS = ["simt", "tcgen05"]
+KERNELS = [sa.KERNEL_SIMT, sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING]
+KERNEL_IDS = ["simt", "gather", "ring"]
+
+
+def span(path: str, g: int, w: int) -> int:
+    """Keys of one tile's window: Bt = 128/g positions plus the halo."""
+    bt = 128 // g
+    return bt + 2 * (w // 2) if path == "sa" else bt + w - 1
+
+
+def _ring_fits(sp: int, g: int, d: int) -> bool:
+    """The ring kernel's shared memory: 2 Q stages, K and V rings of
+    span + Bt rows, a bf16 P tile and the doubled sigma ring (227 KB max)."""
+    pad = -(-sp // 32) * 32
+    r = -(-(pad + 128 // g) // 16) * 16
+    smem = 2 * 128 * d * 2 + 2 * r * d * 2 + 128 * (-(-pad // 64) * 64) * 2
+    smem = -(-(smem + 8 * r) // 64) * 64 + 13 * 8 + 16 + 1024
+    return pad <= 160 and smem <= 232448
+
+
+def must_support(kernel: int, path: str, g: int, w: int, w_swa: int = 0, d: int = 128) -> bool:
+    """Shapes each tcgen05 variant is required to accept (the ring kernel
+    exactly; the gather kernel at least up to 256-key windows)."""
+    if kernel == sa.KERNEL_SIMT:
+        return True
+    if 128 % g:
+        return False
+    paths = [("sa", w), ("swa", w_swa or w)] if path == "gated" else [(path, w)]
+    if kernel == sa.KERNEL_TCGEN05_RING:
+        return (128 // g) % 16 == 0 and all(_ring_fits(span(pp, g, ww), g, d) for pp, ww in paths)
+    return all(span(pp, g, ww) <= 256 for pp, ww in paths)
+
+
+def kernel_ran(requested: int) -> bool:
+    got = sa.last_kernel()
+    if requested == sa.KERNEL_TCGEN05:
+        return got in (sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING)
+    return got == requested
 
 
 def dev_bf16(x: np.ndarray) -> torch.Tensor:

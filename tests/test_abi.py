@@ -78,7 +78,7 @@ def _params(**kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(batch=0), 1), (dict(seqlen=0), 1), (dict(num_q_heads=3), 1), (dict(head_dim=96), 2),
-    (dict(window=0), 1), (dict(kernel=7), 1),
+    (dict(window=0), 1), (dict(kernel=7), 1), (dict(kernel=-1), 1),
 ])
 def test_forward_argument_validation_without_gpu(kw, status):
     lib = sa.load()

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import stochastic_sliding_window_gb300 as sa
-from gpu_helpers import KERNEL_IDS, KERNELS, Inputs, compare, dev_bf16, perms
+from gpu_helpers import KERNEL_IDS, KERNELS, Inputs, compare, dev_bf16, must_support, perms
 
 pytestmark = pytest.mark.gpu
 
@@ -64,7 +64,7 @@ def test_full_window_is_full_attention(kernel):
         try:
             y = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2 * n, causal=causal, kernel=kernel)
         except sa.SaError as e:
-            assert kernel == sa.KERNEL_TCGEN05 and e.status == sa.SA_ERR_UNSUPPORTED
+            assert e.status == sa.SA_ERR_UNSUPPORTED and not must_support(kernel, "sa", 2, 2 * n, d=64)
             continue
         want = oracle.full_attention(inp.case.q, inp.case.k, inp.case.v, causal)
         compare(y, want, f"full window causal={causal}")
@@ -92,6 +92,12 @@ def test_tensor_core_and_simt_kernels_agree():
     n = 4096
     inp = Inputs(1, n, 32, 8, 128, seed=17, gates=True)
     perm, perm_d = perms(17, 0, 1, n)
+    for w in (32, 64, 128):
+        # ring and gather run the same MMAs and the same softmax code
+        a = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_TCGEN05_RING)
+        b = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
+                          kernel=sa.KERNEL_TCGEN05_GATHER)
+        assert torch.equal(a, b)
     for w in (32, 128, 256):
         a = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_TCGEN05)
         b = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_SIMT)
@@ -108,11 +114,17 @@ def test_auto_kernel_choice():
     inp = Inputs(1, 2048, 32, 8, 128, seed=1, gates=False)
     _, perm_d = perms(1, 0, 1, 2048)
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 128)
-    assert sa.last_kernel() == sa.KERNEL_TCGEN05 and sa.last_launch_count() == 1
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_RING and sa.last_launch_count() == 1
+    sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 256)
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_GATHER
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2048)
     assert sa.last_kernel() == sa.KERNEL_SIMT
+    for k in (sa.KERNEL_TCGEN05, sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING):
+        with pytest.raises(sa.SaError) as ei:
+            sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2048, kernel=k)
+        assert ei.value.status == sa.SA_ERR_UNSUPPORTED
     with pytest.raises(sa.SaError) as ei:
-        sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2048, kernel=sa.KERNEL_TCGEN05)
+        sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 256, kernel=sa.KERNEL_TCGEN05_RING)
     assert ei.value.status == sa.SA_ERR_UNSUPPORTED
 
 
