@@ -402,8 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sa_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // Align by pointer arithmetic on the shared array (not through an integer)
+  // so the compiler keeps the shared address space: ld/st.shared, not generic.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   Bars bars;

@@ -23,11 +23,26 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in the instruction
+// until the phase completes or ~1 ms passes, instead of spinning.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -213,6 +228,29 @@ __device__ __forceinline__ float mask_chunk(uint32_t (&v)[32], const int32_t* si
       v[e4 * 4 + u] = __float_as_uint(x);
       if (u & 1) m1 = fmaxf(m1, x); else m0 = fmaxf(m0, x);
     }
+  }
+  return fmaxf(m0, m1);
+}
+
+// Mask one 32-column chunk given the row's causal bits for it (bit e set:
+// column c0+e is allowed) and the band: excluded columns become -inf.
+// Returns the chunk's masked maximum.
+__device__ __forceinline__ float mask_chunk_bits(uint32_t (&v)[32], uint32_t bits, int c0,
+                                                 const RowCtx& rc) {
+  const bool need_band = !(c0 >= rc.wlo && c0 + 31 <= rc.whi);  // warp-uniform
+  if (need_band) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int c = c0 + e;
+      if (c < rc.lo || c > rc.hi) bits &= ~(1u << e);
+    }
+  }
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float x = (bits >> e) & 1u ? __uint_as_float(v[e]) : -INFINITY;
+    v[e] = __float_as_uint(x);
+    if (e & 1) m1 = fmaxf(m1, x); else m0 = fmaxf(m0, x);
   }
   return fmaxf(m0, m1);
 }

@@ -67,7 +67,7 @@ struct Params {
   float scale_log2;
   int tiles_per_seq, num_tiles;
   int cols_stage, tmem_alloc;
-  uint32_t q_bytes, off_k, off_v, off_p, off_sig, off_bar;
+  uint32_t q_bytes, off_k, off_v, off_p, off_sig, off_bits, off_bar;
   long long timeout_cycles;
 };
 
@@ -81,7 +81,8 @@ enum : uint32_t {
   kPfull = 10,   // P of the current tile written
   kPfree = 11,   // P buffer consumed by the PV of the previous tile
   kDrain = 12,   // final MMA completion
-  kNumBars = 13,
+  kWsync = 13,   // [2] a softmax warpgroup's mask words of the tile are written
+  kNumBars = 15,
 };
 
 __device__ __forceinline__ uint32_t mod_ring(int x, int R) {
@@ -165,25 +166,50 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
     asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
     const uint32_t full = bars + 8 * (kFull + s);
     if (tid == 0) mbar_arrive(full);  // releases the sigma writes above
-    // Q: 128 rows (r = t*g + j), 2 K-blocks of [128 rows x 128 B], swizzled
+    // Q: 128 rows (r = t*g + j), 2 K-blocks of [128 rows x 128 B], swizzled.
+    // Row tokens are read from shared memory a batch at a time so that one
+    // load latency covers the batch, then the copies are issued.
     const uint32_t sq = sbase + uint32_t(s) * P.q_bytes;
     const int32_t* sig_win = sig2 + tw.slot_a;
     const size_t rowbase = size_t(tw.b) * P.n;
-    for (int r = r_first; r < kBM; r += RPP) {
-      const int t = r >> P.log2g;
-      const int j = r & (P.g - 1);
-      const int tok = sig_win[P.left + t];
-      const __nv_bfloat16* src = P.q + ((rowbase + tok) * P.Hq + tw.kvh * P.g + j) * D + c * 8;
-      cp_async16(sq + kb * (kBM * 128) + r * 128 + ((c8 ^ (r & 7)) << 4), src);
+    constexpr int kBatch = 8;
+    for (int r0 = r_first; r0 < kBM; r0 += RPP * kBatch) {
+      int tok[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int r = r0 + RPP * k;
+        tok[k] = r < kBM ? sig_win[P.left + (r >> P.log2g)] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int r = r0 + RPP * k;
+        if (r < kBM) {
+          const int j = r & (P.g - 1);
+          const __nv_bfloat16* src =
+              P.q + ((rowbase + tok[k]) * P.Hq + tw.kvh * P.g + j) * D + c * 8;
+          cp_async16(sq + kb * (kBM * 128) + r * 128 + ((c8 ^ (r & 7)) << 4), src);
+        }
+      }
     }
     // K and V: the new positions of the span
-    for (int i = r_first; i < nld; i += RPP) {
-      const uint32_t sl = mod_ring(ld0 + i - tw.seg_q0, P.R);
-      const int tok = sig2[sl];
-      const size_t off = ((rowbase + tok) * P.Hkv + tw.kvh) * D + c * 8;
-      const uint32_t d = kb * (P.R * 128) + sl * 128 + ((c8 ^ (sl & 7)) << 4);
-      cp_async16(sk + d, P.k + off);
-      cp_async16(sv + d, P.v + off);
+    for (int i0 = r_first; i0 < nld; i0 += RPP * kBatch) {
+      int tok[kBatch];
+      uint32_t sl[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int i = i0 + RPP * k;
+        sl[k] = mod_ring(ld0 + i - tw.seg_q0, P.R);
+        tok[k] = i < nld ? sig2[sl[k]] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (i0 + RPP * k < nld) {
+          const size_t off = ((rowbase + tok[k]) * P.Hkv + tw.kvh) * D + c * 8;
+          const uint32_t d = kb * (P.R * 128) + sl[k] * 128 + ((c8 ^ (sl[k] & 7)) << 4);
+          cp_async16(sk + d, P.k + off);
+          cp_async16(sv + d, P.v + off);
+        }
+      }
     }
     cp_async_arrive_noinc(full);
   }
@@ -241,20 +267,46 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
     umma_commit(bars + 8 * (kEmpty + s));
     return true;
   };
-  TileWalk tw;
+  // Issue QK(qk_it) and PV(pv_it) in whichever order their operands become
+  // ready (pv_it <= qk_it): a PV whose P is written never waits behind the
+  // next tile's loads.  Both walks follow the same tile sequence.
+  const int ntiles = end - begin;
+  TileWalk tq;
+  int qk_it = 0, pv_it = 0;
+  int slot_ring[4] = {0, 0, 0, 0};  // slot_a of tiles in flight (QK at most 2 ahead)
+  long long last = clock64();
   bool ok = true;
-  int it = 0, prev_slot = 0;
-  for (int tile = begin; tile < end; ++tile, ++it) {
-    tw.step(P, tile);
-    // A new run reloads the whole ring, which waits for the previous tile's
-    // PV: issue that PV before waiting for this tile's operands.
-    const bool pv_first = it > 0 && tw.new_seg;
-    if (pv_first && !pv(it - 1, prev_slot)) { ok = false; break; }
-    if (!qk(it, tw.slot_a)) { ok = false; break; }
-    if (it > 0 && !pv_first && !pv(it - 1, prev_slot)) { ok = false; break; }
-    prev_slot = tw.slot_a;
+  while (pv_it < ntiles) {
+    bool progress = false;
+    if (qk_it < ntiles && qk_it <= pv_it + 1) {
+      const int s = qk_it & 1;
+      if (mbar_test_wait(bars + 8 * (kFull + s), (qk_it >> 1) & 1) &&
+          mbar_test_wait(bars + 8 * (kTempty + s), ((qk_it >> 1) & 1) ^ 1)) {
+        tq.step(P, begin + qk_it);
+        slot_ring[qk_it & 3] = tq.slot_a;
+        ok = qk(qk_it, tq.slot_a);
+        ++qk_it;
+        progress = true;
+      }
+    }
+    if (ok && pv_it < qk_it && mbar_test_wait(bars + 8 * kPfull, pv_it & 1)) {
+      ok = pv(pv_it, slot_ring[pv_it & 3]);
+      ++pv_it;
+      progress = true;
+    }
+    if (!ok) break;
+    if (progress) {
+      last = clock64();
+    } else {
+      if (*abort_flag) break;
+      if (clock64() - last > P.timeout_cycles) {
+        *abort_flag = 1;
+        atomicOr(P.err, SA_ERRBIT_TIMEOUT);
+        break;
+      }
+      __nanosleep(20);
+    }
   }
-  if (ok && it > 0) pv(it - 1, prev_slot);
   umma_commit(bars + 8 * kDrain);
   const long long t0 = clock64();
   while (!mbar_try_wait(bars + 8 * kDrain, 0) && clock64() - t0 < P.timeout_cycles) {
@@ -308,6 +360,42 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     }
     rc.scale_log2 = P.scale_log2;
 
+    // Causal rule sigma[q] <= sigma[p]: the warpgroup first builds one 32-bit
+    // word per (token of the tile, 32-key chunk), each thread reading its
+    // chunk's sigma in one burst; every thread then fetches just its token's
+    // NCH words, so the per-element mask needs no memory access.
+    uint32_t mw[NCH];
+    if constexpr (kCausal) {
+      uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem + P.off_bits) +
+                       (wg * 2 + ((it >> 1) & 1)) * (kBM * NCH);
+      const int nwords = P.Bt * NCH;
+      for (int w = r; w < nwords; w += kBM) {
+        const int tt = w / NCH, ch = w - tt * NCH;
+        const int sp = sig[P.left + tt];
+        const int4* s4p = reinterpret_cast<const int4*>(sig + ch * 32);
+        int4 s4[8];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) s4[e4] = s4p[e4];
+        uint32_t word = 0;
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          word |= (s4[e4].x <= sp ? 1u : 0u) << (4 * e4);
+          word |= (s4[e4].y <= sp ? 1u : 0u) << (4 * e4 + 1);
+          word |= (s4[e4].z <= sp ? 1u : 0u) << (4 * e4 + 2);
+          word |= (s4[e4].w <= sp ? 1u : 0u) << (4 * e4 + 3);
+        }
+        wbuf[w] = word;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (kWsync + wg));
+      if (!wwait(bars + 8 * (kWsync + wg), ph)) break;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) mw[ch] = wbuf[t * NCH + ch];
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) mw[ch] = 0xffffffffu;
+    }
+
     uint32_t v[NCH][32];
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) tmem_ld32_async(trow + ch * 32, v[ch]);
@@ -316,7 +404,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     for (int ch = 0; ch < NCH; ++ch) reg_fence(v[ch]);
     float mx = -INFINITY;
 #pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) mx = fmaxf(mx, mask_chunk<kCausal>(v[ch], sig, ch * 32, rc));
+    for (int ch = 0; ch < NCH; ++ch) mx = fmaxf(mx, mask_chunk_bits(v[ch], mw[ch], ch * 32, rc));
     const float ms = (mx == -INFINITY) ? 0.f : mx * rc.scale_log2;
     // The single P buffer is free once the previous tile's PV has run (phase
     // it-1 of kPfree).  This warpgroup saw PV(it-2) finish (its epilogue), and
@@ -384,8 +472,9 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
 template <int D, int NCH>
 __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // Align by pointer arithmetic on the shared array (not through an integer)
+  // so the compiler keeps the shared address space: ld/st.shared, not generic.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + P.off_bar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.off_bar + 8 * kNumBars);
@@ -401,6 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
       mbar_init(bars + 8 * (kTempty + s), 4);
     }
     mbar_init(bars + 8 * kPfull, 4);
+    mbar_init(bars + 8 * (kWsync + 0), 4);
+    mbar_init(bars + 8 * (kWsync + 1), 4);
     mbar_init(bars + 8 * kPfree, 1);
     mbar_init(bars + 8 * kDrain, 1);
     *abort_flag = 0;
@@ -451,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
 // ------------------------------------------------------------------ host
 struct Config {
   int Bt, log2g, left, right, span_pad, R, cols_stage, tmem_alloc;
-  uint32_t q_bytes, off_k, off_v, off_p, off_sig, off_bar, smem_bytes;
+  uint32_t q_bytes, off_k, off_v, off_p, off_sig, off_bits, off_bar, smem_bytes;
 };
 
 static uint32_t round_up(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
@@ -484,7 +575,8 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
   c.off_v = c.off_k + ring_bytes;
   c.off_p = c.off_v + ring_bytes;
   c.off_sig = c.off_p + kBM * round_up(uint32_t(c.span_pad), 64) * 2;
-  c.off_bar = round_up(c.off_sig + 2u * c.R * 4, 64);
+  c.off_bits = round_up(c.off_sig + 2u * c.R * 4, 16);
+  c.off_bar = round_up(c.off_bits + 4u * kBM * (c.span_pad / 32) * 4, 64);
   c.smem_bytes = c.off_bar + 8 * kNumBars + 16 + 1024;  // + slot, flags, alignment slack
   return c.smem_bytes <= kMaxSmem;
 }
@@ -577,6 +669,7 @@ sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int acc
   P.off_v = c.off_v;
   P.off_p = c.off_p;
   P.off_sig = c.off_sig;
+  P.off_bits = c.off_bits;
   P.off_bar = c.off_bar;
   P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock
   const int grid = P.num_tiles < sms ? P.num_tiles : sms;
