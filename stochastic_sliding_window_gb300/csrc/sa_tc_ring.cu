@@ -7,28 +7,32 @@
 // (M = 128 rows), attending over the contiguous permuted key span
 // [p0 - left, p0 + Bt - 1 + right].
 //
-// What differs from the gather kernel is how the operands reach shared
-// memory.  Each CTA takes a CONTIGUOUS run of tiles.  Consecutive tiles of a
+// What differs from the gather kernel is how the operands reach the tensor
+// cores.  Each CTA takes a CONTIGUOUS run of tiles.  Consecutive tiles of a
 // sequence share all but Bt rows of their key span, so K and V live in a
-// ring of R = span + Bt rows and each tile fetches only its Bt new rows
+// ring of R = span + 2*Bt rows and each tile fetches only its Bt new rows
 // (plus its 128 Q rows); the first tile of a run fetches the whole span.
-// Three producer warps fetch rows with 16-byte cp.async copies, computing
-// the 128-byte swizzle themselves, so a gathered row costs one coalesced
-// 256-byte request and no per-row TMA descriptor walk.  The key tokens
-// sigma[q] of the ring are kept twice (slots s and s + R) so that a tile's
-// span is always a plain contiguous array.
+// Three producer warps fetch rows with 16-byte cp.async copies (the widest
+// random-row gather path measured on this part), computing the 128-byte
+// swizzle themselves; three Q stages and the 2*Bt ring slack let the loads
+// run two tiles ahead of the tensor cores.  The key tokens sigma[q] of the
+// ring are kept twice (slots s and s + R) so that a tile's span is always a
+// plain contiguous array.
 //
 // Roles (three warpgroups, 384 threads):
 //   warps 0-2   producers: sigma of new positions, cp.async of Q / K / V rows
-//   warp 3      lane 0 issues the MMAs; the warp owns TMEM
+//   warp 3      lane 0 issues the MMAs (in whichever order their operands
+//               become ready); the warp owns TMEM
 //   warps 4-7   softmax + epilogue of even tiles (TMEM stage 0)
 //   warps 8-11  softmax + epilogue of odd tiles  (TMEM stage 1)
 // Per tile: S = Q K^T (one or two MMAs when the span wraps the ring) into
-// TMEM; the row's whole window is read once into registers, masked (band,
-// sequence ends, causal sigma[q] <= sigma[p]), exponentiated and written as
-// bf16 P to shared memory; O = P V (V used MN-major straight from the ring)
-// into TMEM; the epilogue scales by 1/rowsum, optionally applies the gate
-// and the previous out row, and scatters row sigma[p0+t].
+// TMEM; the warpgroup builds the causal mask words of the tile (one 32-bit
+// word per token and 32-key chunk) from sigma; each row's whole window is
+// read once from TMEM into registers, masked, exponentiated, and written
+// back to TMEM as bf16 P over its own S columns; O = P V with P taken from
+// TMEM and V used MN-major straight from the ring; the epilogue scales by
+// 1/rowsum, optionally applies the gate and the previous out row, and
+// scatters row sigma[p0+t].
 // Every wait is bounded (SA_ERRBIT_TIMEOUT); producer copies are drained
 // before exit.
 #include "sa_internal.h"
@@ -51,6 +55,7 @@ constexpr int kSoftmaxRegs = 216;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kMaxChunks = 5;  // spans up to 160 columns (whole row in registers)
+constexpr int kQStages = 3;
 constexpr uint32_t kMaxSmem = 232448;
 
 struct Params {
@@ -66,23 +71,24 @@ struct Params {
   int causal, accumulate, identity;
   float scale_log2;
   int tiles_per_seq, num_tiles;
-  int cols_stage, tmem_alloc;
-  uint32_t q_bytes, off_k, off_v, off_p, off_sig, off_bits, off_bar;
+  int cols_stage, tmem_alloc;  // TMEM stage width; S at 0, P over S, O at span_pad/2
+  uint32_t q_bytes, off_k, off_v, off_sig, off_bits, off_bar;
   long long timeout_cycles;
 };
 
 // Barrier slots (8 bytes each) after off_bar.
 enum : uint32_t {
-  kFull = 0,     // [2] Q stage + new ring rows of tile it landed (and sigma written)
-  kEmpty = 2,    // [2] tile it retired (PV done): Q stage and its oldest ring rows free
-  kSfull = 4,    // [2] S of tile it in TMEM stage it & 1
-  kOfull = 6,    // [2] O of tile it in TMEM stage it & 1
-  kTempty = 8,   // [2] TMEM stage read out by the epilogue
-  kPfull = 10,   // P of the current tile written
-  kPfree = 11,   // P buffer consumed by the PV of the previous tile
-  kDrain = 12,   // final MMA completion
-  kWsync = 13,   // [2] a softmax warpgroup's mask words of the tile are written
-  kNumBars = 15,
+  kFull = 0,     // [3] Q stage + new ring rows of tile it landed (cp.async)
+  kEmpty = 3,    // [3] tile it retired (PV done): Q stage and its oldest ring rows free
+  kSready = 6,   // [2] sigma of tile it written (per softmax warpgroup)
+  kSfree = 8,    // [2] the warpgroup has read the sigma it needs for tile it
+  kSfull = 10,   // [2] S of tile it in TMEM stage it & 1
+  kPfull = 12,   // [2] P of tile it written to TMEM
+  kOfull = 14,   // [2] O of tile it in TMEM
+  kTempty = 16,  // [2] TMEM stage read out by the epilogue
+  kWsync = 18,   // [2] a warpgroup's mask words of the tile are written
+  kDrain = 20,   // final MMA completion
+  kNumBars = 21,
 };
 
 __device__ __forceinline__ uint32_t mod_ring(int x, int R) {
@@ -116,6 +122,30 @@ struct TileWalk {
   }
 };
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// A from TMEM (P), B from shared memory (V), D in TMEM (O).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 template <int D>
 __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, uint32_t bars,
                               volatile int* abort_flag, volatile int* vote) {
@@ -128,21 +158,27 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
   const int c8 = c & 7;
   int32_t* sig2 = reinterpret_cast<int32_t*>(smem + P.off_sig);
   const uint32_t sk = sbase + P.off_k, sv = sbase + P.off_v;
+  auto wait = [&](uint32_t bar, uint32_t par) {
+    return bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
+  };
   int begin, end;
   cta_range(P, begin, end);
   TileWalk tw;
   int it = 0;
   for (int tile = begin; tile < end; ++tile, ++it) {
-    const int s = it & 1;
+    const int s = it % kQStages;
     tw.step(P, tile);
-    // tile it-2 retired (its Q stage and the ring rows this load overwrites);
-    // a new run reloads the whole span, so tile it-1 must be done as well.
+    // Tile it-3 retired: its Q stage and the ring rows this load overwrites
+    // are free.  A new run reloads the whole span, so every tile still in
+    // flight must be done as well.
     if (tid == 0) {
-      bool ok = bounded_wait(bars + 8 * (kEmpty + s), ((it >> 1) & 1) ^ 1, P.timeout_cycles,
-                             P.err, abort_flag);
-      if (ok && tw.new_seg && it > 0)
-        ok = bounded_wait(bars + 8 * (kEmpty + (s ^ 1)), ((it - 1) >> 1) & 1, P.timeout_cycles,
-                          P.err, abort_flag);
+      bool ok = wait(bars + 8 * (kEmpty + s), ((it / kQStages) & 1) ^ 1);
+      if (ok && tw.new_seg) {
+        for (int back = 2; back >= 1 && ok; --back) {
+          const int pit = it - back;
+          if (pit >= 0) ok = wait(bars + 8 * (kEmpty + pit % kQStages), (pit / kQStages) & 1);
+        }
+      }
       *vote = ok ? 1 : 0;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
@@ -164,8 +200,13 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
       sig2[sl + P.R] = tok;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
-    const uint32_t full = bars + 8 * (kFull + s);
-    if (tid == 0) mbar_arrive(full);  // releases the sigma writes above
+    if (tid == 0) {
+      // Hand sigma to the softmax warpgroup of this tile once it has read
+      // what it needed from its previous tile (so this barrier is never two
+      // phases ahead of its waiter).
+      const int w = it & 1;
+      if (wait(bars + 8 * (kSfree + w), ((it >> 1) & 1) ^ 1)) mbar_arrive(bars + 8 * (kSready + w));
+    }
     // Q: 128 rows (r = t*g + j), 2 K-blocks of [128 rows x 128 B], swizzled.
     // Row tokens are read from shared memory a batch at a time so that one
     // load latency covers the batch, then the copies are issued.
@@ -211,7 +252,7 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
         }
       }
     }
-    cp_async_arrive_noinc(full);
+    cp_async_arrive_noinc(bars + 8 * (kFull + s));
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // own copies land before exit
 }
@@ -221,18 +262,14 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
                          volatile int* abort_flag) {
   int begin, end;
   cta_range(P, begin, end);
-  const uint32_t ka = sbase + P.off_k, va = sbase + P.off_v, pa = sbase + P.off_p;
+  const uint32_t ka = sbase + P.off_k, va = sbase + P.off_v;
   const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
-  auto wait = [&](uint32_t bar, uint32_t par) {
-    return bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
-  };
-  auto qk = [&](int it, int slot_a) -> bool {
-    const int s = it & 1;
-    if (!wait(bars + 8 * (kFull + s), (it >> 1) & 1)) return false;
+  const uint32_t p_col = 0, o_col = uint32_t(P.span_pad / 2);
+  auto qk = [&](int it, int slot_a) {
+    const int s = it % kQStages, ts = it & 1;
     fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
-    if (!wait(bars + 8 * (kTempty + s), ((it >> 1) & 1) ^ 1)) return false;
     tc_fence_after();
-    const uint32_t d = tmem_base + uint32_t(s * P.cols_stage);
+    const uint32_t d = tmem_base + uint32_t(ts * P.cols_stage);
     const uint32_t qa = sbase + uint32_t(s) * P.q_bytes;
     const int n1 = min(P.span_pad, P.R - slot_a);
     const int n2 = P.span_pad - n1;
@@ -247,54 +284,47 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
         umma_bf16(d + n1, a, sdesc_sw128(kblk, 16, 1024), idesc_bf16(kBM, n2, 0),
                   kk > 0 ? 1u : 0u);
     }
-    umma_commit(bars + 8 * (kSfull + s));
-    return true;
+    umma_commit(bars + 8 * (kSfull + ts));
   };
-  auto pv = [&](int it, int slot_a) -> bool {
-    const int s = it & 1;
-    if (!wait(bars + 8 * kPfull, it & 1)) return false;
+  auto pv = [&](int it, int slot_a) {
+    const int s = it % kQStages, ts = it & 1;
     tc_fence_after();
-    const uint32_t o = tmem_base + uint32_t(s * P.cols_stage);
+    const uint32_t stage = tmem_base + uint32_t(ts * P.cols_stage);
     const int ksteps = P.span_pad / 16;
     for (int kk = 0; kk < ksteps; ++kk) {
-      const uint64_t a = sdesc_sw128(pa + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
       const uint32_t vs = mod_ring(slot_a + 16 * kk, P.R);
       const uint64_t bd = sdesc_sw128(va + vs * 128, P.R * 128, 1024);
-      umma_bf16(o, a, bd, idesc_pv, kk > 0 ? 1u : 0u);
+      umma_bf16_ts(stage + o_col, stage + p_col + 8 * kk, bd, idesc_pv, kk > 0 ? 1u : 0u);
     }
-    umma_commit(bars + 8 * kPfree);
-    umma_commit(bars + 8 * (kOfull + s));
+    umma_commit(bars + 8 * (kOfull + ts));
     umma_commit(bars + 8 * (kEmpty + s));
-    return true;
   };
   // Issue QK(qk_it) and PV(pv_it) in whichever order their operands become
   // ready (pv_it <= qk_it): a PV whose P is written never waits behind the
-  // next tile's loads.  Both walks follow the same tile sequence.
+  // next tile's loads.
   const int ntiles = end - begin;
   TileWalk tq;
   int qk_it = 0, pv_it = 0;
   int slot_ring[4] = {0, 0, 0, 0};  // slot_a of tiles in flight (QK at most 2 ahead)
   long long last = clock64();
-  bool ok = true;
   while (pv_it < ntiles) {
     bool progress = false;
-    if (qk_it < ntiles && qk_it <= pv_it + 1) {
-      const int s = qk_it & 1;
-      if (mbar_test_wait(bars + 8 * (kFull + s), (qk_it >> 1) & 1) &&
-          mbar_test_wait(bars + 8 * (kTempty + s), ((qk_it >> 1) & 1) ^ 1)) {
+    if (qk_it < ntiles && qk_it < pv_it + 2) {
+      if (mbar_test_wait(bars + 8 * (kFull + qk_it % kQStages), (qk_it / kQStages) & 1) &&
+          mbar_test_wait(bars + 8 * (kTempty + (qk_it & 1)), ((qk_it >> 1) & 1) ^ 1)) {
         tq.step(P, begin + qk_it);
         slot_ring[qk_it & 3] = tq.slot_a;
-        ok = qk(qk_it, tq.slot_a);
+        qk(qk_it, tq.slot_a);
         ++qk_it;
         progress = true;
       }
     }
-    if (ok && pv_it < qk_it && mbar_test_wait(bars + 8 * kPfull, pv_it & 1)) {
-      ok = pv(pv_it, slot_ring[pv_it & 3]);
+    if (pv_it < qk_it &&
+        mbar_test_wait(bars + 8 * (kPfull + (pv_it & 1)), (pv_it >> 1) & 1)) {
+      pv(pv_it, slot_ring[pv_it & 3]);
       ++pv_it;
       progress = true;
     }
-    if (!ok) break;
     if (progress) {
       last = clock64();
     } else {
@@ -324,8 +354,8 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
   const int t = r >> P.log2g;
   const int j = r & (P.g - 1);
   const int32_t* sig2 = reinterpret_cast<const int32_t*>(smem + P.off_sig);
-  uint8_t* pbase = smem + P.off_p;
   const uint32_t trow = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(wg * P.cols_stage);
+  const uint32_t o_col = uint32_t(P.span_pad / 2);
   auto wwait = [&](uint32_t bar, uint32_t par) {
     const bool ok = bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
     return __all_sync(0xffffffffu, ok);
@@ -338,10 +368,8 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     tw.step(P, tile);
     if ((it & 1) != wg) continue;
     const uint32_t ph = uint32_t(it >> 1) & 1u;
-    if (!wwait(bars + 8 * (kSfull + wg), ph)) break;
-    if (!wwait(bars + 8 * (kFull + wg), ph)) break;  // sigma of the ring is visible
-    tc_fence_after();
-    const int32_t* sig = sig2 + tw.slot_a;  // sigma of span column c is sig[c]
+    if (!wwait(bars + 8 * (kSready + wg), ph)) break;  // sigma of the tile is visible
+    const int32_t* sig = sig2 + tw.slot_a;            // sigma of span column c is sig[c]
     bool row_valid = tw.p0 + t < P.n;
     RowCtx rc;
     rc.sig_p = sig[P.left + t];
@@ -395,7 +423,11 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) mw[ch] = 0xffffffffu;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kSfree + wg));  // sigma no longer read
 
+    if (!wwait(bars + 8 * (kSfull + wg), ph)) break;
+    tc_fence_after();
     uint32_t v[NCH][32];
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) tmem_ld32_async(trow + ch * 32, v[ch]);
@@ -406,20 +438,26 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) mx = fmaxf(mx, mask_chunk_bits(v[ch], mw[ch], ch * 32, rc));
     const float ms = (mx == -INFINITY) ? 0.f : mx * rc.scale_log2;
-    // The single P buffer is free once the previous tile's PV has run (phase
-    // it-1 of kPfree).  This warpgroup saw PV(it-2) finish (its epilogue), and
-    // PV(it) needs this tile's P, so the barrier's current phase is it-1 or
-    // it: the parity wait on phase it-1 is unambiguous.  (Waiting on an older
-    // phase as well would alias onto phase it and never return.)
-    if (it >= 1 && !wwait(bars + 8 * kPfree, uint32_t(it - 1) & 1u)) break;
+    // p = 2^(s*scale*log2e - max); bf16 P overwrites this row's own S columns
+    // (already in registers): P column pair c/2 holds keys c and c+1.
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) exp_store_chunk(v[ch], ms, rc.scale_log2, pbase, r, ch * 32, acc);
+    for (int ch = 0; ch < NCH; ++ch) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e2 = 0; e2 < 16; ++e2) {
+        const float p0 = fast_exp2(fmaf(__uint_as_float(v[ch][2 * e2]), rc.scale_log2, -ms));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(v[ch][2 * e2 + 1]), rc.scale_log2, -ms));
+        acc[e2 & 3] += p0 + p1;
+        pk[e2] = pack_bf16x2(p0, p1);
+      }
+      tmem_st16(trow + ch * 16, pk);
+    }
     const float l = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-    fence_proxy_async_smem();
+    tmem_wait_st();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars + 8 * kPfull);
+    if (lane == 0) mbar_arrive(bars + 8 * (kPfull + wg));
 
     // epilogue
     if (!wwait(bars + 8 * (kOfull + wg), ph)) break;
@@ -430,7 +468,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     if (P.gate != nullptr && row_valid) mul *= 1.f / (1.f + expf(-P.gate[orow]));
     uint32_t o[D / 32][32];
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) tmem_ld32_async(trow + ch * 32, o[ch]);
+    for (int ch = 0; ch < D / 32; ++ch) tmem_ld32_async(trow + o_col + ch * 32, o[ch]);
     tmem_wait_ld();
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) reg_fence(o[ch]);
@@ -482,17 +520,19 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
   volatile int* vote = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 8);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bars + 8 * (kFull + s), kProducers + 1);
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(bars + 8 * (kFull + s), kProducers);
       mbar_init(bars + 8 * (kEmpty + s), 1);
-      mbar_init(bars + 8 * (kSfull + s), 1);
-      mbar_init(bars + 8 * (kOfull + s), 1);
-      mbar_init(bars + 8 * (kTempty + s), 4);
     }
-    mbar_init(bars + 8 * kPfull, 4);
-    mbar_init(bars + 8 * (kWsync + 0), 4);
-    mbar_init(bars + 8 * (kWsync + 1), 4);
-    mbar_init(bars + 8 * kPfree, 1);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(bars + 8 * (kSready + w), 1);
+      mbar_init(bars + 8 * (kSfree + w), 4);
+      mbar_init(bars + 8 * (kSfull + w), 1);
+      mbar_init(bars + 8 * (kPfull + w), 4);
+      mbar_init(bars + 8 * (kOfull + w), 1);
+      mbar_init(bars + 8 * (kTempty + w), 4);
+      mbar_init(bars + 8 * (kWsync + w), 4);
+    }
     mbar_init(bars + 8 * kDrain, 1);
     *abort_flag = 0;
     *vote = 1;
@@ -542,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
 // ------------------------------------------------------------------ host
 struct Config {
   int Bt, log2g, left, right, span_pad, R, cols_stage, tmem_alloc;
-  uint32_t q_bytes, off_k, off_v, off_p, off_sig, off_bits, off_bar, smem_bytes;
+  uint32_t q_bytes, off_k, off_v, off_sig, off_bits, off_bar, smem_bytes;
 };
 
 static uint32_t round_up(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
@@ -563,18 +603,20 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
   const long long span = (long long)c.Bt + c.left + c.right;
   if (span > 32LL * kMaxChunks) return false;
   c.span_pad = int(round_up(uint32_t(span), 32));
-  c.R = int(round_up(uint32_t(c.span_pad + c.Bt), 16));
-  c.cols_stage = int(round_up(uint32_t(c.span_pad > pb.d ? c.span_pad : pb.d), 32));
+  c.R = int(round_up(uint32_t(c.span_pad + 2 * c.Bt), 16));
+  // TMEM stage: S [0, span_pad); P (bf16 pairs) over S [0, span_pad/2);
+  // O [span_pad/2, span_pad/2 + d).
+  const int width = c.span_pad > c.span_pad / 2 + pb.d ? c.span_pad : c.span_pad / 2 + pb.d;
+  c.cols_stage = int(round_up(uint32_t(width), 32));
   uint32_t alloc = 32;
   while (alloc < uint32_t(2 * c.cols_stage)) alloc <<= 1;
   if (alloc > 512) return false;
   c.tmem_alloc = int(alloc);
   c.q_bytes = kBM * pb.d * 2;
   const uint32_t ring_bytes = uint32_t(c.R) * pb.d * 2;
-  c.off_k = 2 * c.q_bytes;
+  c.off_k = kQStages * c.q_bytes;
   c.off_v = c.off_k + ring_bytes;
-  c.off_p = c.off_v + ring_bytes;
-  c.off_sig = c.off_p + kBM * round_up(uint32_t(c.span_pad), 64) * 2;
+  c.off_sig = c.off_v + ring_bytes;
   c.off_bits = round_up(c.off_sig + 2u * c.R * 4, 16);
   c.off_bar = round_up(c.off_bits + 4u * kBM * (c.span_pad / 32) * 4, 64);
   c.smem_bytes = c.off_bar + 8 * kNumBars + 16 + 1024;  // + slot, flags, alignment slack
@@ -667,7 +709,6 @@ sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int acc
   P.q_bytes = c.q_bytes;
   P.off_k = c.off_k;
   P.off_v = c.off_v;
-  P.off_p = c.off_p;
   P.off_sig = c.off_sig;
   P.off_bits = c.off_bits;
   P.off_bar = c.off_bar;
