@@ -35,8 +35,11 @@ sys.path.insert(0, ROOT)
 WORKLOAD = dict(workload="long_prefill_gqa", batch=1, seq_len=32768, num_q_heads=32,
                 num_kv_heads=8, head_dim=128, window=128, causal=True, path="sa", seed=0)
 METRIC = "SA fwd tokens/s and % roofline (bf16, n=32K, w=128, GQA 32q/8kv, d=128)"
-PROFILE = os.path.join(ROOT, "profiles", "sa_tc_kernel_long_prefill_gqa_w128.md")
-TC_SOURCE = os.path.join(ROOT, "stochastic_sliding_window_gb300", "csrc", "sa_tc.cu")
+PROFILE = os.path.join(ROOT, "profiles", "sa_ring_kernel_long_prefill_gqa_w128.md")
+# the ring kernel and the tcgen05 helpers it inlines: the profile's DRAM
+# counters hold only while these files are unchanged
+KERNEL_SOURCES = [os.path.join(ROOT, "stochastic_sliding_window_gb300", "csrc", f)
+                  for f in ("sa_tc_ring.cu", "sa_tc_common.cuh")]
 
 _G: dict = {}  # arrays shared with forked oracle workers
 
@@ -67,12 +70,20 @@ def load_peaks() -> dict:
         return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
 
 
+def kernel_source_sha256() -> str:
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profiled_traffic() -> int | None:
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (its sha256 is recorded in the summary)."""
     try:
         text = open(PROFILE).read()
-        src = hashlib.sha256(open(TC_SOURCE, "rb").read()).hexdigest()
+        src = kernel_source_sha256()
     except OSError:
         return None
     m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)

@@ -14,8 +14,13 @@
 // (plus its 128 Q rows); the first tile of a run fetches the whole span.
 // Three producer warps fetch rows with 16-byte cp.async copies (the widest
 // random-row gather path measured on this part), computing the 128-byte
-// swizzle themselves; three Q stages and the 2*Bt ring slack let the loads
-// run two tiles ahead of the tensor cores.  The key tokens sigma[q] of the
+// swizzle themselves.  Q and K of a tile are needed only by S = Q K^T, V only
+// by O = P V, so they land on separate barriers and are released separately:
+// a Q stage and the K rows a tile overwrites are free once the S MMA of the
+// tile three back has completed, V rows once its O MMA has.  V is fetched one tile behind Q and K (it is not needed
+// until the softmax is done), so the loads of Q and K run ahead of the
+// tensor cores without waiting for the softmax.  The sigma values of the next tile's new positions
+// are loaded into registers one tile ahead.  The key tokens sigma[q] of the
 // ring are kept twice (slots s and s + R) so that a tile's span is always a
 // plain contiguous array.
 //
@@ -50,12 +55,13 @@ constexpr int kProducers = 96;  // warps 0-2
 constexpr int kMmaWarp = 3;
 constexpr int kFirstSoftmaxWarp = 4;
 constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 64;
-constexpr int kSoftmaxRegs = 216;
+constexpr int kCtrlRegs = 128;
+constexpr int kSoftmaxRegs = 184;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kMaxChunks = 5;  // spans up to 160 columns (whole row in registers)
-constexpr int kQStages = 3;
+constexpr int kQStages = 3;  // Q buffers; a stage is free once its S MMA is done
+constexpr int kVDepth = 3;   // V (and K) rows of tile x overwrite those of tile x - 3
 constexpr uint32_t kMaxSmem = 232448;
 
 struct Params {
@@ -72,29 +78,29 @@ struct Params {
   float scale_log2;
   int tiles_per_seq, num_tiles;
   int cols_stage, tmem_alloc;  // TMEM stage width; S at 0, P over S, O at span_pad/2
-  uint32_t q_bytes, off_k, off_v, off_sig, off_bits, off_bar;
+  uint32_t q_bytes, off_k, off_v, off_sig, off_vtok, off_bits, off_bar;
   long long timeout_cycles;
 };
 
-// Barrier slots (8 bytes each) after off_bar.
+// Barrier slots (8 bytes each) after off_bar.  Q families are indexed by
+// it % kQStages, V families by it % kVDepth, warpgroup families by it & 1.
 enum : uint32_t {
-  kFull = 0,     // [3] Q stage + new ring rows of tile it landed (cp.async)
-  kEmpty = 3,    // [3] tile it retired (PV done): Q stage and its oldest ring rows free
-  kSready = 6,   // [2] sigma of tile it written (per softmax warpgroup)
-  kSfree = 8,    // [2] the warpgroup has read the sigma it needs for tile it
-  kSfull = 10,   // [2] S of tile it in TMEM stage it & 1
-  kPfull = 12,   // [2] P of tile it written to TMEM
-  kOfull = 14,   // [2] O of tile it in TMEM
-  kTempty = 16,  // [2] TMEM stage read out by the epilogue
-  kWsync = 18,   // [2] a warpgroup's mask words of the tile are written
-  kDrain = 20,   // final MMA completion
-  kNumBars = 21,
+  kFullQK = 0,   // [kQStages] Q stage and new K rows of tile it landed (cp.async)
+  kQKdone = 3,   // [kQStages] S MMA of tile it done: its Q stage and K rows are free
+  kFullV = 6,    // [kVDepth] new V rows of tile it landed (cp.async)
+  kPVdone = 9,   // [kVDepth] O MMA of tile it done: its V rows are free
+  kSready = 12,  // [2] sigma of tile it written (per softmax warpgroup)
+  kSfree = 14,   // [2] the warpgroup has read the sigma it needs for tile it
+  kSfull = 16,   // [2] S of tile it in TMEM stage it & 1
+  kPfull = 18,   // [2] P of tile it written to TMEM
+  kOfull = 20,   // [2] O of tile it in TMEM
+  kTempty = 22,  // [2] TMEM stage read out by the epilogue
+  kWsync = 24,   // [2] a warpgroup's mask words of the tile are written
+  kDrain = 26,   // final MMA completion
+  kNumBars = 27,
 };
-
-__device__ __forceinline__ uint32_t mod_ring(int x, int R) {
-  const int m = x % R;
-  return uint32_t(m < 0 ? m + R : m);
-}
+static_assert(kFullQK + kQStages <= kQKdone && kQKdone + kQStages <= kFullV, "barrier slots");
+static_assert(32 * kMaxChunks <= 2 * kProducers, "a tile's new positions: two per producer thread");
 
 // Tiles of this CTA: a contiguous range, split evenly over the grid.
 __device__ __forceinline__ void cta_range(const Params& P, int& begin, int& end) {
@@ -102,13 +108,51 @@ __device__ __forceinline__ void cta_range(const Params& P, int& begin, int& end)
   end = int((long long)(blockIdx.x + 1) * P.num_tiles / gridDim.x);
 }
 
-// Walks this CTA's tiles keeping the ring mapping: a run of one sequence
-// maps key position q to ring slot (q - seg_q0) mod R.
+// Walks this CTA's tiles in order keeping the ring mapping: a run of one
+// sequence maps key position q to ring slot (q - seg_q0) mod R.  The first
+// step locates its tile by division; every later step advances by one tile.
 struct TileWalk {
   int seq = -1, seg_q0 = 0;
-  int b, kvh, p0, slot_a;
-  bool new_seg;
+  int b = 0, kvh = 0, p0 = 0, slot_a = 0;
+  int ld0 = 0, nld = 0, ld_slot = 0;  // positions the tile loads, slot of the first
+  bool new_seg = false;
   __device__ __forceinline__ void step(const Params& P, int tile) {
+    if (seq < 0) {
+      seq = tile / P.tiles_per_seq;
+      p0 = (tile - seq * P.tiles_per_seq) * P.Bt;
+      b = seq / P.Hkv;
+      kvh = seq - b * P.Hkv;
+      new_seg = true;
+    } else {
+      p0 += P.Bt;
+      new_seg = p0 >= P.n;
+      if (new_seg) {
+        p0 = 0;
+        ++seq;
+        if (++kvh == P.Hkv) {
+          kvh = 0;
+          ++b;
+        }
+      }
+    }
+    if (new_seg) {  // a new run: the whole span, from slot 0
+      seg_q0 = p0 - P.left;
+      slot_a = 0;
+      ld0 = seg_q0;
+      nld = P.span_pad;
+      ld_slot = 0;
+    } else {  // Bt new positions at the right end of the span
+      slot_a += P.Bt;
+      if (slot_a >= P.R) slot_a -= P.R;
+      ld0 = p0 - P.left + P.span_pad - P.Bt;
+      nld = P.Bt;
+      ld_slot = slot_a + P.span_pad - P.Bt;
+      if (ld_slot >= P.R) ld_slot -= P.R;
+    }
+  }
+  // Locates a tile from scratch (few registers live across tiles; divides).
+  // Sets b, kvh, p0, slot_a and new_seg only.
+  __device__ __forceinline__ void locate(const Params& P, int tile) {
     const int s = tile / P.tiles_per_seq;
     p0 = (tile - s * P.tiles_per_seq) * P.Bt;
     b = s / P.Hkv;
@@ -118,7 +162,12 @@ struct TileWalk {
       seq = s;
       seg_q0 = p0 - P.left;
     }
-    slot_a = int(mod_ring(p0 - P.left - seg_q0, P.R));
+    slot_a = (p0 - P.left - seg_q0) % P.R;  // non-negative within a run
+  }
+  // ring slot of the tile's i-th loaded position (i < nld <= span_pad < R)
+  __device__ __forceinline__ int slot_of(const Params& P, int i) const {
+    const int sl = ld_slot + i;
+    return sl >= P.R ? sl - P.R : sl;
   }
 };
 
@@ -148,72 +197,123 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 
 template <int D>
 __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, uint32_t bars,
-                              volatile int* abort_flag, volatile int* vote) {
-  constexpr int CPR = D / 8;  // 16-byte chunks per row
+                              volatile int* abort_flag, volatile int* votes) {
+  constexpr int CPR = D / 8;             // 16-byte chunks per row
   constexpr int RPP = kProducers / CPR;  // rows per pass of the 96 threads
+  constexpr int kBatch = 8;              // rows whose tokens are read before their copies
   const int tid = threadIdx.x;
   const int c = tid % CPR;
   const int r_first = tid / CPR;
   const int kb = c >> 3;
   const int c8 = c & 7;
   int32_t* sig2 = reinterpret_cast<int32_t*>(smem + P.off_sig);
+  int32_t* vtok = reinterpret_cast<int32_t*>(smem + P.off_vtok);  // [2][span_pad] new tokens
   const uint32_t sk = sbase + P.off_k, sv = sbase + P.off_v;
   auto wait = [&](uint32_t bar, uint32_t par) {
     return bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
   };
-  int begin, end;
-  cta_range(P, begin, end);
-  TileWalk tw;
-  int it = 0;
-  for (int tile = begin; tile < end; ++tile, ++it) {
-    const int s = it % kQStages;
-    tw.step(P, tile);
-    // Tile it-3 retired: its Q stage and the ring rows this load overwrites
-    // are free.  A new run reloads the whole span, so every tile still in
-    // flight must be done as well.
-    if (tid == 0) {
-      bool ok = wait(bars + 8 * (kEmpty + s), ((it / kQStages) & 1) ^ 1);
-      if (ok && tw.new_seg) {
-        for (int back = 2; back >= 1 && ok; --back) {
-          const int pit = it - back;
-          if (pit >= 0) ok = wait(bars + 8 * (kEmpty + pit % kQStages), (pit / kQStages) & 1);
+  // Thread 0 waits for tiles to retire on a [3] family, each tile once and in
+  // order (so no wait is ever two phases behind its barrier).
+  int qk_seen = -1, pv_seen = -1;
+  auto retire = [&](uint32_t fam, int depth, int& seen, int upto) {
+    bool ok = true;
+    for (int z = seen + 1; z <= upto && ok; ++z)
+      ok = wait(bars + 8 * (fam + z % depth), (z / depth) & 1);
+    if (ok && upto > seen) seen = upto;
+    return ok;
+  };
+  // Thread 0's verdict, shared with the other producers.
+  auto agree = [&](volatile int* slot, bool ok) {
+    if (tid == 0) *slot = ok ? 1 : 0;
+    asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
+    return *slot != 0;
+  };
+  // sigma of a tile's new positions (two per thread at most), into registers
+  auto fetch = [&](const TileWalk& w, int (&pre)[2]) {
+    const int32_t* perm_b = P.identity ? nullptr : P.perm + size_t(w.b) * P.n;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = tid + kProducers * k;
+      if (i < w.nld) {
+        const int qc = min(max(w.ld0 + i, 0), P.n - 1);
+        pre[k] = perm_b ? __ldg(perm_b + qc) : qc;
+      }
+    }
+  };
+
+  // V rows of tile x: they overwrite those of tile x - 3 (a new run: of
+  // every tile in flight).
+  auto load_v = [&](int x, const TileWalk& w) {
+    bool ok = true;
+    if (tid == 0) ok = retire(kPVdone, kVDepth, pv_seen, w.new_seg ? x - 1 : x - kVDepth);
+    if (!agree(votes + 1, ok)) return false;
+    const int32_t* vt = vtok + (x & 1) * P.span_pad;
+    const size_t rowbase = size_t(w.b) * P.n;
+    for (int i0 = r_first; i0 < w.nld; i0 += RPP * kBatch) {
+      int tok[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int i = i0 + RPP * k;
+        tok[k] = i < w.nld ? vt[i] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int i = i0 + RPP * k;
+        if (i < w.nld) {
+          const int sl = w.slot_of(P, i);
+          const size_t off = ((rowbase + tok[k]) * P.Hkv + w.kvh) * D + c * 8;
+          cp_async16(sv + kb * (P.R * 128) + sl * 128 + ((c8 ^ (sl & 7)) << 4), P.v + off);
         }
       }
-      *vote = ok ? 1 : 0;
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
-    if (!*vote) break;
-    const int win0 = tw.p0 - P.left;
-    const int ld0 = tw.new_seg ? win0 : win0 + P.span_pad - P.Bt;
-    const int nld = tw.new_seg ? P.span_pad : P.Bt;
-    const int32_t* perm_b = P.identity ? nullptr : P.perm + size_t(tw.b) * P.n;
-    for (int i = tid; i < nld; i += kProducers) {
-      const int qpos = ld0 + i;
-      const int qc = min(max(qpos, 0), P.n - 1);
-      int tok = perm_b ? __ldg(perm_b + qc) : qc;
-      if (unsigned(tok) >= unsigned(P.n)) {
-        atomicOr(P.err, SA_ERRBIT_RANGE);
-        tok = 0;
+    cp_async_arrive_noinc(bars + 8 * (kFullV + x % kVDepth));
+    return true;
+  };
+
+  // sigma, Q and K of tile it.  Its Q stage belongs to tile it - kQStages and
+  // the K rows it overwrites to tile it - 3 (a new run: to every tile in
+  // flight, and it rewrites the whole sigma ring, which the warpgroups of
+  // those tiles must have read: their O MMA being done implies it).
+  auto load_qk = [&](int it, const TileWalk& w, TileWalk& nx, int (&pre)[2], bool has_next) {
+    const int s = it % kQStages;
+    bool ok = true;
+    if (tid == 0) {
+      ok = retire(kQKdone, kQStages, qk_seen, w.new_seg ? it - 1 : it - kQStages);
+      if (ok && w.new_seg) ok = retire(kPVdone, kVDepth, pv_seen, it - 1);
+    }
+    if (!agree(votes, ok)) return false;
+    int32_t* vt = vtok + (it & 1) * P.span_pad;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = tid + kProducers * k;
+      if (i < w.nld) {
+        int tok = pre[k];
+        if (unsigned(tok) >= unsigned(P.n)) {
+          atomicOr(P.err, SA_ERRBIT_RANGE);
+          tok = 0;
+        }
+        const int sl = w.slot_of(P, i);
+        sig2[sl] = tok;
+        sig2[sl + P.R] = tok;
+        vt[i] = tok;
       }
-      const uint32_t sl = mod_ring(qpos - tw.seg_q0, P.R);
-      sig2[sl] = tok;
-      sig2[sl + P.R] = tok;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
+    if (has_next) {  // loaded now, stored at the next tile
+      nx.step(P, 0);
+      fetch(nx, pre);
+    }
     if (tid == 0) {
       // Hand sigma to the softmax warpgroup of this tile once it has read
       // what it needed from its previous tile (so this barrier is never two
       // phases ahead of its waiter).
-      const int w = it & 1;
-      if (wait(bars + 8 * (kSfree + w), ((it >> 1) & 1) ^ 1)) mbar_arrive(bars + 8 * (kSready + w));
+      const int wg = it & 1;
+      if (wait(bars + 8 * (kSfree + wg), ((it >> 1) & 1) ^ 1)) mbar_arrive(bars + 8 * (kSready + wg));
     }
     // Q: 128 rows (r = t*g + j), 2 K-blocks of [128 rows x 128 B], swizzled.
-    // Row tokens are read from shared memory a batch at a time so that one
-    // load latency covers the batch, then the copies are issued.
     const uint32_t sq = sbase + uint32_t(s) * P.q_bytes;
-    const int32_t* sig_win = sig2 + tw.slot_a;
-    const size_t rowbase = size_t(tw.b) * P.n;
-    constexpr int kBatch = 8;
+    const int32_t* sig_win = sig2 + w.slot_a;
+    const size_t rowbase = size_t(w.b) * P.n;
     for (int r0 = r_first; r0 < kBM; r0 += RPP * kBatch) {
       int tok[kBatch];
 #pragma unroll
@@ -227,32 +327,53 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
         if (r < kBM) {
           const int j = r & (P.g - 1);
           const __nv_bfloat16* src =
-              P.q + ((rowbase + tok[k]) * P.Hq + tw.kvh * P.g + j) * D + c * 8;
+              P.q + ((rowbase + tok[k]) * P.Hq + w.kvh * P.g + j) * D + c * 8;
           cp_async16(sq + kb * (kBM * 128) + r * 128 + ((c8 ^ (r & 7)) << 4), src);
         }
       }
     }
-    // K and V: the new positions of the span
-    for (int i0 = r_first; i0 < nld; i0 += RPP * kBatch) {
+    // K: the new positions of the span
+    for (int i0 = r_first; i0 < w.nld; i0 += RPP * kBatch) {
       int tok[kBatch];
-      uint32_t sl[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int i = i0 + RPP * k;
-        sl[k] = mod_ring(ld0 + i - tw.seg_q0, P.R);
-        tok[k] = i < nld ? sig2[sl[k]] : 0;
+        tok[k] = i < w.nld ? vt[i] : 0;
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        if (i0 + RPP * k < nld) {
-          const size_t off = ((rowbase + tok[k]) * P.Hkv + tw.kvh) * D + c * 8;
-          const uint32_t d = kb * (P.R * 128) + sl[k] * 128 + ((c8 ^ (sl[k] & 7)) << 4);
-          cp_async16(sk + d, P.k + off);
-          cp_async16(sv + d, P.v + off);
+        const int i = i0 + RPP * k;
+        if (i < w.nld) {
+          const int sl = w.slot_of(P, i);
+          const size_t off = ((rowbase + tok[k]) * P.Hkv + w.kvh) * D + c * 8;
+          cp_async16(sk + kb * (P.R * 128) + sl * 128 + ((c8 ^ (sl & 7)) << 4), P.k + off);
         }
       }
     }
-    cp_async_arrive_noinc(bars + 8 * (kFull + s));
+    cp_async_arrive_noinc(bars + 8 * (kFullQK + s));
+    return true;
+  };
+
+  int begin, end;
+  cta_range(P, begin, end);
+  const int ntiles = end - begin;
+  TileWalk cur, nxt;
+  int pre[2] = {0, 0};
+  if (ntiles > 0) {
+    nxt.step(P, begin);
+    fetch(nxt, pre);
+  }
+  // Iteration it loads sigma/Q/K of tile it and V of tile it - 1; before a
+  // new run the V of the previous tile goes first (the run's loads wait for
+  // every tile in flight, that tile's O MMA included).
+  for (int it = 0; it <= ntiles; ++it) {
+    const TileWalk prev = cur;
+    const bool has_cur = it < ntiles;
+    if (has_cur) cur = nxt;
+    const bool v_first = has_cur && cur.new_seg;
+    if (it >= 1 && v_first && !load_v(it - 1, prev)) break;
+    if (has_cur && !load_qk(it, cur, nxt, pre, it + 1 < ntiles)) break;
+    if (it >= 1 && !v_first && !load_v(it - 1, prev)) break;
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // own copies land before exit
 }
@@ -285,43 +406,47 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
                   kk > 0 ? 1u : 0u);
     }
     umma_commit(bars + 8 * (kSfull + ts));
+    umma_commit(bars + 8 * (kQKdone + s));
   };
   auto pv = [&](int it, int slot_a) {
-    const int s = it % kQStages, ts = it & 1;
+    const int s = it % kVDepth, ts = it & 1;
+    fence_proxy_async_smem();  // V rows landed by cp.async
     tc_fence_after();
     const uint32_t stage = tmem_base + uint32_t(ts * P.cols_stage);
     const int ksteps = P.span_pad / 16;
+    int vs = slot_a;
     for (int kk = 0; kk < ksteps; ++kk) {
-      const uint32_t vs = mod_ring(slot_a + 16 * kk, P.R);
       const uint64_t bd = sdesc_sw128(va + vs * 128, P.R * 128, 1024);
       umma_bf16_ts(stage + o_col, stage + p_col + 8 * kk, bd, idesc_pv, kk > 0 ? 1u : 0u);
+      vs += 16;
+      if (vs >= P.R) vs -= P.R;
     }
     umma_commit(bars + 8 * (kOfull + ts));
-    umma_commit(bars + 8 * (kEmpty + s));
+    umma_commit(bars + 8 * (kPVdone + s));
   };
   // Issue QK(qk_it) and PV(pv_it) in whichever order their operands become
   // ready (pv_it <= qk_it): a PV whose P is written never waits behind the
   // next tile's loads.
   const int ntiles = end - begin;
-  TileWalk tq;
+  TileWalk tq, tp;
   int qk_it = 0, pv_it = 0;
-  int slot_ring[4] = {0, 0, 0, 0};  // slot_a of tiles in flight (QK at most 2 ahead)
   long long last = clock64();
   while (pv_it < ntiles) {
     bool progress = false;
     if (qk_it < ntiles && qk_it < pv_it + 2) {
-      if (mbar_test_wait(bars + 8 * (kFull + qk_it % kQStages), (qk_it / kQStages) & 1) &&
+      if (mbar_test_wait(bars + 8 * (kFullQK + qk_it % kQStages), (qk_it / kQStages) & 1) &&
           mbar_test_wait(bars + 8 * (kTempty + (qk_it & 1)), ((qk_it >> 1) & 1) ^ 1)) {
         tq.step(P, begin + qk_it);
-        slot_ring[qk_it & 3] = tq.slot_a;
         qk(qk_it, tq.slot_a);
         ++qk_it;
         progress = true;
       }
     }
     if (pv_it < qk_it &&
-        mbar_test_wait(bars + 8 * (kPfull + (pv_it & 1)), (pv_it >> 1) & 1)) {
-      pv(pv_it, slot_ring[pv_it & 3]);
+        mbar_test_wait(bars + 8 * (kPfull + (pv_it & 1)), (pv_it >> 1) & 1) &&
+        mbar_test_wait(bars + 8 * (kFullV + pv_it % kVDepth), (pv_it / kVDepth) & 1)) {
+      tp.step(P, begin + pv_it);
+      pv(pv_it, tp.slot_a);
       ++pv_it;
       progress = true;
     }
@@ -365,7 +490,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
   TileWalk tw;
   int it = 0;
   for (int tile = begin; tile < end; ++tile, ++it) {
-    tw.step(P, tile);
+    tw.locate(P, tile);
     if ((it & 1) != wg) continue;
     const uint32_t ph = uint32_t(it >> 1) & 1u;
     if (!wwait(bars + 8 * (kSready + wg), ph)) break;  // sigma of the tile is visible
@@ -392,10 +517,10 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     // word per (token of the tile, 32-key chunk), each thread reading its
     // chunk's sigma in one burst; every thread then fetches just its token's
     // NCH words, so the per-element mask needs no memory access.
-    uint32_t mw[NCH];
+    const uint32_t* wrow = nullptr;  // this row's token's NCH mask words
     if constexpr (kCausal) {
       uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem + P.off_bits) +
-                       (wg * 2 + ((it >> 1) & 1)) * (kBM * NCH);
+                       (wg * 2 + ((it >> 1) & 1)) * (P.Bt * NCH);
       const int nwords = P.Bt * NCH;
       for (int w = r; w < nwords; w += kBM) {
         const int tt = w / NCH, ch = w - tt * NCH;
@@ -417,37 +542,37 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8 * (kWsync + wg));
       if (!wwait(bars + 8 * (kWsync + wg), ph)) break;
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) mw[ch] = wbuf[t * NCH + ch];
-    } else {
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) mw[ch] = 0xffffffffu;
+      wrow = wbuf + t * NCH;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kSfree + wg));  // sigma no longer read
 
     if (!wwait(bars + 8 * (kSfull + wg), ph)) break;
     tc_fence_after();
-    uint32_t v[NCH][32];
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) tmem_ld32_async(trow + ch * 32, v[ch]);
-    tmem_wait_ld();
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) reg_fence(v[ch]);
+    // Two passes over the row's 32-column chunks, loops kept rolled so the
+    // code stays small (three roles share each SM's instruction cache):
+    // the masked row maximum, then p = 2^(s*scale*log2e - max) written back
+    // to TMEM as bf16 over the row's own S columns (P column pair c/2 holds
+    // keys c and c+1; chunk ch's P lands on S columns already consumed).
     float mx = -INFINITY;
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) mx = fmaxf(mx, mask_chunk_bits(v[ch], mw[ch], ch * 32, rc));
-    const float ms = (mx == -INFINITY) ? 0.f : mx * rc.scale_log2;
-    // p = 2^(s*scale*log2e - max); bf16 P overwrites this row's own S columns
-    // (already in registers): P column pair c/2 holds keys c and c+1.
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
     for (int ch = 0; ch < NCH; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(trow + ch * 32, v);
+      mx = fmaxf(mx, mask_chunk_bits(v, kCausal ? wrow[ch] : ~0u, ch * 32, rc));
+    }
+    const float ms = (mx == -INFINITY) ? 0.f : mx * rc.scale_log2;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int ch = 0; ch < NCH; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(trow + ch * 32, v);
+      mask_chunk_bits(v, kCausal ? wrow[ch] : ~0u, ch * 32, rc);
       uint32_t pk[16];
 #pragma unroll
       for (int e2 = 0; e2 < 16; ++e2) {
-        const float p0 = fast_exp2(fmaf(__uint_as_float(v[ch][2 * e2]), rc.scale_log2, -ms));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(v[ch][2 * e2 + 1]), rc.scale_log2, -ms));
+        const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e2]), rc.scale_log2, -ms));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e2 + 1]), rc.scale_log2, -ms));
         acc[e2 & 3] += p0 + p1;
         pk[e2] = pack_bf16x2(p0, p1);
       }
@@ -476,6 +601,8 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kTempty + wg));
     if (row_valid) {
+      // Each thread writes its own row (with the gated sum's second pass
+      // adding the row already there, in fp32).
       __nv_bfloat16* op = P.out + orow * D;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -517,12 +644,16 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
   const uint32_t bars = sbase + P.off_bar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.off_bar + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 4);
-  volatile int* vote = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 8);
+  volatile int* votes = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 8);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
-      mbar_init(bars + 8 * (kFull + s), kProducers);
-      mbar_init(bars + 8 * (kEmpty + s), 1);
+      mbar_init(bars + 8 * (kFullQK + s), kProducers);
+      mbar_init(bars + 8 * (kQKdone + s), 1);
+    }
+    for (int s = 0; s < kVDepth; ++s) {
+      mbar_init(bars + 8 * (kFullV + s), kProducers);
+      mbar_init(bars + 8 * (kPVdone + s), 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bars + 8 * (kSready + w), 1);
@@ -535,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
     }
     mbar_init(bars + 8 * kDrain, 1);
     *abort_flag = 0;
-    *vote = 1;
+    votes[0] = 1;
+    votes[1] = 1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -563,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     if (warp < kMmaWarp) {
-      producer_role<D>(P, smem, sbase, bars, abort_flag, vote);
+      producer_role<D>(P, smem, sbase, bars, abort_flag, votes);
     } else {
       if ((threadIdx.x & 31) == 0) mma_role<D>(P, sbase, tmem_base, bars, abort_flag);
       __syncwarp();
@@ -582,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
 // ------------------------------------------------------------------ host
 struct Config {
   int Bt, log2g, left, right, span_pad, R, cols_stage, tmem_alloc;
-  uint32_t q_bytes, off_k, off_v, off_sig, off_bits, off_bar, smem_bytes;
+  uint32_t q_bytes, off_k, off_v, off_sig, off_vtok, off_bits, off_bar, smem_bytes;
 };
 
 static uint32_t round_up(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
@@ -617,8 +749,9 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
   c.off_k = kQStages * c.q_bytes;
   c.off_v = c.off_k + ring_bytes;
   c.off_sig = c.off_v + ring_bytes;
-  c.off_bits = round_up(c.off_sig + 2u * c.R * 4, 16);
-  c.off_bar = round_up(c.off_bits + 4u * kBM * (c.span_pad / 32) * 4, 64);
+  c.off_vtok = round_up(c.off_sig + 2u * c.R * 4, 16);
+  c.off_bits = round_up(c.off_vtok + 2u * c.span_pad * 4, 16);
+  c.off_bar = round_up(c.off_bits + 4u * c.Bt * (c.span_pad / 32) * 4, 64);
   c.smem_bytes = c.off_bar + 8 * kNumBars + 16 + 1024;  // + slot, flags, alignment slack
   return c.smem_bytes <= kMaxSmem;
 }
@@ -710,6 +843,7 @@ sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int acc
   P.off_k = c.off_k;
   P.off_v = c.off_v;
   P.off_sig = c.off_sig;
+  P.off_vtok = c.off_vtok;
   P.off_bits = c.off_bits;
   P.off_bar = c.off_bar;
   P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock

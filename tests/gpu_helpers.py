@@ -24,13 +24,20 @@ def span(path: str, g: int, w: int) -> int:
 
 
 def _ring_fits(sp: int, g: int, d: int) -> bool:
-    """The ring kernel's shared memory: 2 Q stages, K and V rings of
-    span + Bt rows, a bf16 P tile and the doubled sigma ring (227 KB max)."""
-    pad = -(-sp // 32) * 32
-    r = -(-(pad + 128 // g) // 16) * 16
-    smem = 2 * 128 * d * 2 + 2 * r * d * 2 + 128 * (-(-pad // 64) * 64) * 2
-    smem = -(-(smem + 8 * r) // 64) * 64 + 13 * 8 + 16 + 1024
-    return pad <= 160 and smem <= 232448
+    """The ring kernel's resources: 3 Q stages, K and V rings of span + 2 Bt
+    rows, the doubled sigma ring, two new-token lists, the mask words and 27
+    barriers in 227 KB of shared memory; two TMEM stages in 512 columns."""
+    rnd = lambda x, m: -(-x // m) * m
+    pad = rnd(sp, 32)
+    bt = 128 // g
+    r = rnd(pad + 2 * bt, 16)
+    off_sig = 3 * 128 * d * 2 + 2 * r * d * 2
+    off_vtok = rnd(off_sig + 2 * r * 4, 16)
+    off_bits = rnd(off_vtok + 2 * pad * 4, 16)
+    off_bar = rnd(off_bits + 4 * bt * (pad // 32) * 4, 64)
+    smem = off_bar + 8 * 27 + 16 + 1024
+    cols = rnd(max(pad, pad // 2 + d), 32)
+    return pad <= 160 and smem <= 232448 and 2 * cols <= 512
 
 
 def must_support(kernel: int, path: str, g: int, w: int, w_swa: int = 0, d: int = 128) -> bool:
