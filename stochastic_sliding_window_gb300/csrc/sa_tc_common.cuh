@@ -196,6 +196,54 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// Packed pairs of fp32 (sm_100 family f32x2 arithmetic): each lane of the
+// pair is rounded exactly as the scalar instruction would round it.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t x) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(x));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Columns c0 .. c0+31 that fall in the band [lo, hi], as bits (bit e:
+// column c0 + e).
+__device__ __forceinline__ uint32_t band_bits(int lo, int hi, int c0) {
+  const int a = lo - c0, b = hi - c0;  // first and last allowed offsets
+  if (b < 0 || a > 31 || a > b) return 0u;
+  const uint32_t upto_b = b >= 31 ? 0xffffffffu : ((2u << b) - 1u);
+  const uint32_t from_a = a <= 0 ? 0xffffffffu : ~((1u << a) - 1u);
+  return upto_b & from_a;
+}
+
+// Row sums of p are accumulated in one fixed order by every tcgen05 kernel
+// (so that they agree bit for bit): pair e2 of a 32-column chunk adds
+// p[2 e2] to acc[2 (e2 & 1)] and p[2 e2 + 1] to acc[2 (e2 & 1) + 1]; the row
+// sum is (acc[0] + acc[1]) + (acc[2] + acc[3]).
+
 // Per-row state of one tile, shared by the softmax variants.
 struct RowCtx {
   int lo, hi;      // attended column band of this row (sequence ends folded in)
@@ -266,7 +314,8 @@ __device__ __forceinline__ void exp_store_chunk(const uint32_t (&v)[32], float m
     for (int e2 = 0; e2 < 4; ++e2) {
       const float p0 = fast_exp2(fmaf(__uint_as_float(v[q4 * 8 + 2 * e2]), sl2, -ms));
       const float p1 = fast_exp2(fmaf(__uint_as_float(v[q4 * 8 + 2 * e2 + 1]), sl2, -ms));
-      acc[e2] += p0 + p1;
+      acc[2 * (e2 & 1)] += p0;
+      acc[2 * (e2 & 1) + 1] += p1;
       pk[e2] = pack_bf16x2(p0, p1);
     }
     const int col8 = c0 + q4 * 8;

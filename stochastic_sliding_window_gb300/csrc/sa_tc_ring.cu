@@ -496,54 +496,49 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     if (!wwait(bars + 8 * (kSready + wg), ph)) break;  // sigma of the tile is visible
     const int32_t* sig = sig2 + tw.slot_a;            // sigma of span column c is sig[c]
     bool row_valid = tw.p0 + t < P.n;
-    RowCtx rc;
-    rc.sig_p = sig[P.left + t];
-    if (row_valid && unsigned(rc.sig_p) >= unsigned(P.n)) {  // never expected: record, skip
+    int sig_p = sig[P.left + t];
+    if (row_valid && unsigned(sig_p) >= unsigned(P.n)) {  // never expected: record, skip
       atomicOr(P.err, SA_ERRBIT_INTERNAL);
       row_valid = false;
     }
-    rc.lo = max(t, P.left - tw.p0);
-    rc.hi = row_valid ? min(t + P.left + P.right, P.n - 1 - tw.p0 + P.left) : rc.lo - 1;
-    rc.wlo = rc.lo;
-    rc.whi = rc.hi;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      rc.wlo = max(rc.wlo, __shfl_xor_sync(0xffffffffu, rc.wlo, o));
-      rc.whi = min(rc.whi, __shfl_xor_sync(0xffffffffu, rc.whi, o));
-    }
-    rc.scale_log2 = P.scale_log2;
 
-    // Causal rule sigma[q] <= sigma[p]: the warpgroup first builds one 32-bit
-    // word per (token of the tile, 32-key chunk), each thread reading its
-    // chunk's sigma in one burst; every thread then fetches just its token's
-    // NCH words, so the per-element mask needs no memory access.
-    const uint32_t* wrow = nullptr;  // this row's token's NCH mask words
-    if constexpr (kCausal) {
-      uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem + P.off_bits) +
-                       (wg * 2 + ((it >> 1) & 1)) * (P.Bt * NCH);
+    // The warpgroup first builds one 32-bit word per (token of the tile,
+    // 32-key chunk): bit e set iff key column ch*32 + e is attended, i.e. it
+    // lies in the token's window (truncated at the sequence ends) and, when
+    // causal, sigma[q] <= sigma[p]; each thread reads its chunk's sigma in one
+    // burst.  The passes below then need only the row's own words.
+    uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem + P.off_bits) +
+                     (wg * 2 + ((it >> 1) & 1)) * (P.Bt * NCH);
+    {
       const int nwords = P.Bt * NCH;
       for (int w = r; w < nwords; w += kBM) {
         const int tt = w / NCH, ch = w - tt * NCH;
-        const int sp = sig[P.left + tt];
-        const int4* s4p = reinterpret_cast<const int4*>(sig + ch * 32);
-        int4 s4[8];
+        const int lo = max(tt, P.left - tw.p0);
+        const int hi = tw.p0 + tt < P.n ? min(tt + P.left + P.right, P.n - 1 - tw.p0 + P.left) : -1;
+        uint32_t word = band_bits(lo, hi, ch * 32);
+        if (kCausal && word != 0u) {
+          const int sp = sig[P.left + tt];
+          const int4* s4p = reinterpret_cast<const int4*>(sig + ch * 32);
+          int4 s4[8];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) s4[e4] = s4p[e4];
-        uint32_t word = 0;
+          for (int e4 = 0; e4 < 8; ++e4) s4[e4] = s4p[e4];
+          uint32_t cw = 0;
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          word |= (s4[e4].x <= sp ? 1u : 0u) << (4 * e4);
-          word |= (s4[e4].y <= sp ? 1u : 0u) << (4 * e4 + 1);
-          word |= (s4[e4].z <= sp ? 1u : 0u) << (4 * e4 + 2);
-          word |= (s4[e4].w <= sp ? 1u : 0u) << (4 * e4 + 3);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            cw |= (s4[e4].x <= sp ? 1u : 0u) << (4 * e4);
+            cw |= (s4[e4].y <= sp ? 1u : 0u) << (4 * e4 + 1);
+            cw |= (s4[e4].z <= sp ? 1u : 0u) << (4 * e4 + 2);
+            cw |= (s4[e4].w <= sp ? 1u : 0u) << (4 * e4 + 3);
+          }
+          word &= cw;
         }
         wbuf[w] = word;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kWsync + wg));
-      if (!wwait(bars + 8 * (kWsync + wg), ph)) break;
-      wrow = wbuf + t * NCH;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kWsync + wg));
+    if (!wwait(bars + 8 * (kWsync + wg), ph)) break;
+    const uint32_t* wrow = wbuf + t * NCH;
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kSfree + wg));  // sigma no longer read
 
@@ -551,34 +546,52 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     tc_fence_after();
     // Two passes over the row's 32-column chunks, loops kept rolled so the
     // code stays small (three roles share each SM's instruction cache):
-    // the masked row maximum, then p = 2^(s*scale*log2e - max) written back
-    // to TMEM as bf16 over the row's own S columns (P column pair c/2 holds
-    // keys c and c+1; chunk ch's P lands on S columns already consumed).
+    // the attended maximum, then p = 2^(s*scale*log2e - max) for attended
+    // columns (0 elsewhere) written back to TMEM as bf16 over the row's own S
+    // columns (P column pair c/2 holds keys c and c+1; chunk ch's P lands on
+    // S columns already consumed).
     float mx = -INFINITY;
 #pragma unroll 1
     for (int ch = 0; ch < NCH; ++ch) {
       uint32_t v[32];
       tmem_ld32(trow + ch * 32, v);
-      mx = fmaxf(mx, mask_chunk_bits(v, kCausal ? wrow[ch] : ~0u, ch * 32, rc));
+      const uint32_t bits = wrow[ch];
+      float m0 = mx, m1 = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float x0 = (bits >> e) & 1u ? __uint_as_float(v[e]) : -INFINITY;
+        const float x1 = (bits >> (e + 1)) & 1u ? __uint_as_float(v[e + 1]) : -INFINITY;
+        const float x2 = (bits >> (e + 2)) & 1u ? __uint_as_float(v[e + 2]) : -INFINITY;
+        const float x3 = (bits >> (e + 3)) & 1u ? __uint_as_float(v[e + 3]) : -INFINITY;
+        m0 = fmax3(m0, x0, x1);
+        m1 = fmax3(m1, x2, x3);
+      }
+      mx = fmaxf(m0, m1);
     }
-    const float ms = (mx == -INFINITY) ? 0.f : mx * rc.scale_log2;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float ms = (mx == -INFINITY) ? 0.f : mx * P.scale_log2;
+    const uint64_t sl2 = f2_pack(P.scale_log2, P.scale_log2);
+    const uint64_t nms = f2_pack(-ms, -ms);
+    uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll 1
     for (int ch = 0; ch < NCH; ++ch) {
       uint32_t v[32];
       tmem_ld32(trow + ch * 32, v);
-      mask_chunk_bits(v, kCausal ? wrow[ch] : ~0u, ch * 32, rc);
+      const uint32_t bits = wrow[ch];
       uint32_t pk[16];
 #pragma unroll
       for (int e2 = 0; e2 < 16; ++e2) {
-        const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e2]), rc.scale_log2, -ms));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e2 + 1]), rc.scale_log2, -ms));
-        acc[e2 & 3] += p0 + p1;
+        const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * e2]),
+                                                  __uint_as_float(v[2 * e2 + 1])),
+                                          sl2, nms));
+        const float p0 = (bits >> (2 * e2)) & 1u ? fast_exp2(x.x) : 0.f;
+        const float p1 = (bits >> (2 * e2 + 1)) & 1u ? fast_exp2(x.y) : 0.f;
+        acc2[e2 & 1] = f2_add(acc2[e2 & 1], f2_pack(p0, p1));
         pk[e2] = pack_bf16x2(p0, p1);
       }
       tmem_st16(trow + ch * 16, pk);
     }
-    const float l = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    const float2 a01 = f2_unpack(acc2[0]), a23 = f2_unpack(acc2[1]);
+    const float l = (a01.x + a01.y) + (a23.x + a23.y);
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -589,7 +602,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     tc_fence_after();
     float mul = l > 0.f ? 1.f / l : 0.f;
     const size_t orow =
-        row_valid ? (size_t(tw.b) * P.n + rc.sig_p) * P.Hq + size_t(tw.kvh) * P.g + j : 0;
+        row_valid ? (size_t(tw.b) * P.n + sig_p) * P.Hq + size_t(tw.kvh) * P.g + j : 0;
     if (P.gate != nullptr && row_valid) mul *= 1.f / (1.f + expf(-P.gate[orow]));
     uint32_t o[D / 32][32];
 #pragma unroll
@@ -600,6 +613,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kTempty + wg));
+    const uint64_t mul2 = f2_pack(mul, mul);
     if (row_valid) {
       // Each thread writes its own row (with the gated sum's second pass
       // adding the row already there, in fp32).
@@ -616,7 +630,13 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
         for (int q4 = 0; q4 < 4; ++q4) {
           float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[ch][q4 * 8 + e]) * mul;
+          for (int e = 0; e < 4; ++e) {
+            const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(o[ch][q4 * 8 + 2 * e]),
+                                                      __uint_as_float(o[ch][q4 * 8 + 2 * e + 1])),
+                                              mul2));
+            f[2 * e] = y.x;
+            f[2 * e + 1] = y.y;
+          }
           if (P.accumulate) {
             const __nv_bfloat162* pv2 = reinterpret_cast<const __nv_bfloat162*>(&prev[q4]);
 #pragma unroll
