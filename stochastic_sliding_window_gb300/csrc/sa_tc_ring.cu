@@ -184,6 +184,13 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 32-byte global store (sm_100 family): one whole sector per thread.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&r)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // A from TMEM (P), B from shared memory (V), D in TMEM (O).
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                              uint32_t idesc, uint32_t accumulate) {
@@ -614,9 +621,28 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kTempty + wg));
     const uint64_t mul2 = f2_pack(mul, mul);
-    if (row_valid) {
-      // Each thread writes its own row (with the gated sum's second pass
-      // adding the row already there, in fp32).
+    if (row_valid && !P.accumulate) {
+      // Each thread writes its own row, whole 32-byte sectors per store.
+      __nv_bfloat16* op = P.out + orow * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int k = half * 16 + 2 * e;
+            const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(o[ch][k]),
+                                                      __uint_as_float(o[ch][k + 1])),
+                                              mul2));
+            pk[e] = pack_bf16x2(y.x, y.y);
+          }
+          st_global_v8(op + ch * 32 + half * 16, pk);
+        }
+      }
+    } else if (row_valid) {
+      // Second pass of the gated sum: each thread reads its own row, adds in
+      // fp32 and writes it back.
       __nv_bfloat16* op = P.out + orow * D;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
