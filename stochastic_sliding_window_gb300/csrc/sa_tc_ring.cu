@@ -24,12 +24,14 @@
 // ring are kept twice (slots s and s + R) so that a tile's span is always a
 // plain contiguous array.
 //
-// Roles (three warpgroups, 384 threads):
-//   warps 0-2   producers: sigma of new positions, cp.async of Q / K / V rows
-//   warp 3      lane 0 issues the MMAs (in whichever order their operands
+// Roles (four warpgroups, 512 threads):
+//   warps 0-6   producers: sigma of new positions, cp.async of Q / K / V rows
+//               (seven warps, so that their copy streams hide each other's
+//               latency next to the softmax warps)
+//   warp 7      lane 0 issues the MMAs (in whichever order their operands
 //               become ready); the warp owns TMEM
-//   warps 4-7   softmax + epilogue of even tiles (TMEM stage 0)
-//   warps 8-11  softmax + epilogue of odd tiles  (TMEM stage 1)
+//   warps 8-11  softmax + epilogue of even tiles (TMEM stage 0)
+//   warps 12-15 softmax + epilogue of odd tiles  (TMEM stage 1)
 // Per tile: S = Q K^T (one or two MMAs when the span wraps the ring) into
 // TMEM; the warpgroup builds the causal mask words of the tile (one 32-bit
 // word per token and 32-key chunk) from sigma; each row's whole window is
@@ -50,14 +52,14 @@ namespace ring {
 
 using namespace tcc;
 
-constexpr int kThreads = 384;
-constexpr int kProducers = 96;  // warps 0-2
-constexpr int kMmaWarp = 3;
-constexpr int kFirstSoftmaxWarp = 4;
-constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 128;
-constexpr int kSoftmaxRegs = 184;
-static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
+constexpr int kThreads = 512;
+constexpr int kProducers = 224;  // warps 0-6
+constexpr int kMmaWarp = 7;
+constexpr int kFirstSoftmaxWarp = 8;
+constexpr int kLaunchRegs = 128;
+constexpr int kCtrlRegs = 96;
+constexpr int kSoftmaxRegs = 160;
+static_assert(256 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kMaxChunks = 5;  // spans up to 160 columns (whole row in registers)
 constexpr int kQStages = 3;  // Q buffers; a stage is free once its S MMA is done
@@ -206,7 +208,7 @@ template <int D>
 __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, uint32_t bars,
                               volatile int* abort_flag, volatile int* votes) {
   constexpr int CPR = D / 8;             // 16-byte chunks per row
-  constexpr int RPP = kProducers / CPR;  // rows per pass of the 96 threads
+  constexpr int RPP = kProducers / CPR;  // rows per pass of the producer threads
   constexpr int kBatch = 8;              // rows whose tokens are read before their copies
   const int tid = threadIdx.x;
   const int c = tid % CPR;
@@ -310,13 +312,6 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
       nx.step(P, 0);
       fetch(nx, pre);
     }
-    if (tid == 0) {
-      // Hand sigma to the softmax warpgroup of this tile once it has read
-      // what it needed from its previous tile (so this barrier is never two
-      // phases ahead of its waiter).
-      const int wg = it & 1;
-      if (wait(bars + 8 * (kSfree + wg), ((it >> 1) & 1) ^ 1)) mbar_arrive(bars + 8 * (kSready + wg));
-    }
     // Q: 128 rows (r = t*g + j), 2 K-blocks of [128 rows x 128 B], swizzled.
     const uint32_t sq = sbase + uint32_t(s) * P.q_bytes;
     const int32_t* sig_win = sig2 + w.slot_a;
@@ -358,6 +353,15 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
       }
     }
     cp_async_arrive_noinc(bars + 8 * (kFullQK + s));
+    if (tid == 0) {
+      // Hand sigma to the softmax warpgroup of this tile once it has read
+      // what it needed from its previous tile (so this barrier is never two
+      // phases ahead of its waiter).  Done after this thread's copies so
+      // that the wait never delays them; the next tile's sigma writes come
+      // after it.
+      const int wg = it & 1;
+      if (wait(bars + 8 * (kSfree + wg), ((it >> 1) & 1) ^ 1)) mbar_arrive(bars + 8 * (kSready + wg));
+    }
     return true;
   };
 
