@@ -62,7 +62,7 @@ constexpr int kSoftmaxRegs = 160;
 static_assert(256 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kMaxChunks = 5;  // spans up to 160 columns (whole row in registers)
-constexpr int kQStages = 3;  // Q buffers; a stage is free once its S MMA is done
+constexpr int kQStages = 2;  // Q buffers; a stage is free once its S MMA is done
 constexpr int kVDepth = 3;   // V (and K) rows of tile x overwrite those of tile x - 3
 constexpr uint32_t kMaxSmem = 232448;
 
@@ -251,11 +251,15 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
   };
 
   // V rows of tile x: they overwrite those of tile x - 3 (a new run: of
-  // every tile in flight).
-  auto load_v = [&](int x, const TileWalk& w) {
-    bool ok = true;
-    if (tid == 0) ok = retire(kPVdone, kVDepth, pv_seen, w.new_seg ? x - 1 : x - kVDepth);
-    if (!agree(votes + 1, ok)) return false;
+  // every tile in flight).  Unless `own_wait`, the caller's barrier has
+  // already covered that wait.
+  auto v_upto = [&](int x, const TileWalk& w) { return w.new_seg ? x - 1 : x - kVDepth; };
+  auto load_v = [&](int x, const TileWalk& w, bool own_wait) {
+    if (own_wait) {
+      bool ok = true;
+      if (tid == 0) ok = retire(kPVdone, kVDepth, pv_seen, v_upto(x, w));
+      if (!agree(votes + 1, ok)) return false;
+    }
     const int32_t* vt = vtok + (x & 1) * P.span_pad;
     const size_t rowbase = size_t(w.b) * P.n;
     for (int i0 = r_first; i0 < w.nld; i0 += RPP * kBatch) {
@@ -283,12 +287,14 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
   // the K rows it overwrites to tile it - 3 (a new run: to every tile in
   // flight, and it rewrites the whole sigma ring, which the warpgroups of
   // those tiles must have read: their O MMA being done implies it).
-  auto load_qk = [&](int it, const TileWalk& w, TileWalk& nx, int (&pre)[2], bool has_next) {
+  // pv_upto: the O MMAs the V load that follows in this iteration needs.
+  auto load_qk = [&](int it, const TileWalk& w, TileWalk& nx, int (&pre)[2], bool has_next,
+                     int pv_upto) {
     const int s = it % kQStages;
     bool ok = true;
     if (tid == 0) {
       ok = retire(kQKdone, kQStages, qk_seen, w.new_seg ? it - 1 : it - kQStages);
-      if (ok && w.new_seg) ok = retire(kPVdone, kVDepth, pv_seen, it - 1);
+      if (ok) ok = retire(kPVdone, kVDepth, pv_seen, w.new_seg ? it - 1 : pv_upto);
     }
     if (!agree(votes, ok)) return false;
     int32_t* vt = vtok + (it & 1) * P.span_pad;
@@ -374,17 +380,20 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
     nxt.step(P, begin);
     fetch(nxt, pre);
   }
-  // Iteration it loads sigma/Q/K of tile it and V of tile it - 1; before a
-  // new run the V of the previous tile goes first (the run's loads wait for
-  // every tile in flight, that tile's O MMA included).
+  // Iteration it loads sigma/Q/K of tile it and V of tile it - 1, whose wait
+  // is folded into the Q/K barrier; before a new run the V of the previous
+  // tile goes first (the run's loads wait for every tile in flight, that
+  // tile's O MMA included).
   for (int it = 0; it <= ntiles; ++it) {
     const TileWalk prev = cur;
     const bool has_cur = it < ntiles;
     if (has_cur) cur = nxt;
     const bool v_first = has_cur && cur.new_seg;
-    if (it >= 1 && v_first && !load_v(it - 1, prev)) break;
-    if (has_cur && !load_qk(it, cur, nxt, pre, it + 1 < ntiles)) break;
-    if (it >= 1 && !v_first && !load_v(it - 1, prev)) break;
+    if (it >= 1 && v_first && !load_v(it - 1, prev, true)) break;
+    if (has_cur && !load_qk(it, cur, nxt, pre, it + 1 < ntiles,
+                            (it >= 1 && !v_first) ? v_upto(it - 1, prev) : -1))
+      break;
+    if (it >= 1 && !v_first && !load_v(it - 1, prev, !has_cur)) break;
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // own copies land before exit
 }

@@ -24,14 +24,14 @@ def span(path: str, g: int, w: int) -> int:
 
 
 def _ring_fits(sp: int, g: int, d: int) -> bool:
-    """The ring kernel's resources: 3 Q stages, K and V rings of span + 2 Bt
+    """The ring kernel's resources: 2 Q stages, K and V rings of span + 2 Bt
     rows, the doubled sigma ring, two new-token lists, the mask words and 27
     barriers in 227 KB of shared memory; two TMEM stages in 512 columns."""
     rnd = lambda x, m: -(-x // m) * m
     pad = rnd(sp, 32)
     bt = 128 // g
     r = rnd(pad + 2 * bt, 16)
-    off_sig = 3 * 128 * d * 2 + 2 * r * d * 2
+    off_sig = 2 * 128 * d * 2 + 2 * r * d * 2
     off_vtok = rnd(off_sig + 2 * r * 4, 16)
     off_bits = rnd(off_vtok + 2 * pad * 4, 16)
     off_bar = rnd(off_bits + 4 * bt * (pad // 32) * 4, 64)
