@@ -414,16 +414,20 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
     const uint32_t qa = sbase + uint32_t(s) * P.q_bytes;
     const int n1 = min(P.span_pad, P.R - slot_a);
     const int n2 = P.span_pad - n1;
+    // Descriptors of the first K step; later steps add their byte offset / 16
+    // to the start-address field (every operand lies below 256 KB, so the
+    // field never carries).
+    const uint64_t a0 = sdesc_sw128(qa, 16, 1024);
+    const uint64_t b0 = sdesc_sw128(ka + slot_a * 128, 16, 1024);
+    const uint64_t w0 = sdesc_sw128(ka, 16, 1024);  // the part past the ring's end
+    const uint64_t ring_blk = uint64_t(P.R) * 8;   // next 64-column block of the ring
+    const uint32_t id1 = idesc_bf16(kBM, n1, 0), id2 = idesc_bf16(kBM, n2, 0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t koff = uint32_t(kk & 3) * 32u;
-      const uint64_t a = sdesc_sw128(qa + (kk >> 2) * (kBM * 128) + koff, 16, 1024);
-      const uint32_t kblk = ka + (kk >> 2) * (P.R * 128) + koff;
-      umma_bf16(d, a, sdesc_sw128(kblk + slot_a * 128, 16, 1024), idesc_bf16(kBM, n1, 0),
-                kk > 0 ? 1u : 0u);
-      if (n2 > 0)
-        umma_bf16(d + n1, a, sdesc_sw128(kblk, 16, 1024), idesc_bf16(kBM, n2, 0),
-                  kk > 0 ? 1u : 0u);
+      const uint64_t da = uint64_t((kk >> 2) * (kBM * 128 / 16) + (kk & 3) * 2);
+      const uint64_t db = uint64_t(kk >> 2) * ring_blk + uint64_t((kk & 3) * 2);
+      umma_bf16(d, a0 + da, b0 + db, id1, kk > 0 ? 1u : 0u);
+      if (n2 > 0) umma_bf16(d + n1, a0 + da, w0 + db, id2, kk > 0 ? 1u : 0u);
     }
     umma_commit(bars + 8 * (kSfull + ts));
     umma_commit(bars + 8 * (kQKdone + s));
@@ -435,11 +439,16 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
     const uint32_t stage = tmem_base + uint32_t(ts * P.cols_stage);
     const int ksteps = P.span_pad / 16;
     int vs = slot_a;
+    uint64_t bd = sdesc_sw128(va + vs * 128, P.R * 128, 1024);
+    const uint64_t wrap = uint64_t(P.R) * 8;  // R rows of 128 B, in 16-byte units
     for (int kk = 0; kk < ksteps; ++kk) {
-      const uint64_t bd = sdesc_sw128(va + vs * 128, P.R * 128, 1024);
       umma_bf16_ts(stage + o_col, stage + p_col + 8 * kk, bd, idesc_pv, kk > 0 ? 1u : 0u);
       vs += 16;
-      if (vs >= P.R) vs -= P.R;
+      bd += 128;  // 16 rows of 128 B
+      if (vs >= P.R) {
+        vs -= P.R;
+        bd -= wrap;
+      }
     }
     umma_commit(bars + 8 * (kOfull + ts));
     umma_commit(bars + 8 * (kPVdone + s));
