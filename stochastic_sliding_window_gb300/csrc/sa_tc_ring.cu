@@ -33,10 +33,11 @@
 //   warps 8-11  softmax + epilogue of even tiles (TMEM stage 0)
 //   warps 12-15 softmax + epilogue of odd tiles  (TMEM stage 1)
 // Per tile: S = Q K^T (one or two MMAs when the span wraps the ring) into
-// TMEM; the warpgroup builds the causal mask words of the tile (one 32-bit
-// word per token and 32-key chunk) from sigma; each row's whole window is
-// read once from TMEM into registers, masked, exponentiated, and written
-// back to TMEM as bf16 P over its own S columns; O = P V with P taken from
+// TMEM; each softmax warp builds the mask words of its tokens (one 32-bit
+// word per token and 32-key chunk) from sigma; each row's window is read
+// from TMEM in 32-column chunks in two passes (the attended maximum, then
+// exponentials) and P is written back to TMEM as bf16 over its own S
+// columns; O = P V with P taken from
 // TMEM and V used MN-major straight from the ring; the epilogue scales by
 // 1/rowsum, optionally applies the gate and the previous out row, and
 // scatters row sigma[p0+t].
@@ -97,9 +98,8 @@ enum : uint32_t {
   kPfull = 18,   // [2] P of tile it written to TMEM
   kOfull = 20,   // [2] O of tile it in TMEM
   kTempty = 22,  // [2] TMEM stage read out by the epilogue
-  kWsync = 24,   // [2] a warpgroup's mask words of the tile are written
-  kDrain = 26,   // final MMA completion
-  kNumBars = 27,
+  kDrain = 24,   // final MMA completion
+  kNumBars = 25,
 };
 static_assert(kFullQK + kQStages <= kQKdone && kQKdone + kQStages <= kFullV, "barrier slots");
 static_assert(32 * kMaxChunks <= 2 * kProducers, "a tile's new positions: two per producer thread");
@@ -454,14 +454,23 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
     umma_commit(bars + 8 * (kPVdone + s));
   };
   // Issue QK(qk_it) and PV(pv_it) in whichever order their operands become
-  // ready (pv_it <= qk_it): a PV whose P is written never waits behind the
-  // next tile's loads.
+  // ready (pv_it <= qk_it), PV first when both are: the softmax warpgroup
+  // waits on its O, and a PV whose P is written never waits behind the next
+  // tile's loads.
   const int ntiles = end - begin;
   TileWalk tq, tp;
   int qk_it = 0, pv_it = 0;
   long long last = clock64();
   while (pv_it < ntiles) {
     bool progress = false;
+    if (pv_it < qk_it &&
+        mbar_test_wait(bars + 8 * (kPfull + (pv_it & 1)), (pv_it >> 1) & 1) &&
+        mbar_test_wait(bars + 8 * (kFullV + pv_it % kVDepth), (pv_it / kVDepth) & 1)) {
+      tp.step(P, begin + pv_it);
+      pv(pv_it, tp.slot_a);
+      ++pv_it;
+      progress = true;
+    }
     if (qk_it < ntiles && qk_it < pv_it + 2) {
       if (mbar_test_wait(bars + 8 * (kFullQK + qk_it % kQStages), (qk_it / kQStages) & 1) &&
           mbar_test_wait(bars + 8 * (kTempty + (qk_it & 1)), ((qk_it >> 1) & 1) ^ 1)) {
@@ -470,14 +479,6 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
         ++qk_it;
         progress = true;
       }
-    }
-    if (pv_it < qk_it &&
-        mbar_test_wait(bars + 8 * (kPfull + (pv_it & 1)), (pv_it >> 1) & 1) &&
-        mbar_test_wait(bars + 8 * (kFullV + pv_it % kVDepth), (pv_it / kVDepth) & 1)) {
-      tp.step(P, begin + pv_it);
-      pv(pv_it, tp.slot_a);
-      ++pv_it;
-      progress = true;
     }
     if (progress) {
       last = clock64();
@@ -531,7 +532,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
       row_valid = false;
     }
 
-    // The warpgroup first builds one 32-bit word per (token of the tile,
+    // Each warp first builds one 32-bit word per (token of its rows,
     // 32-key chunk): bit e set iff key column ch*32 + e is attended, i.e. it
     // lies in the token's window (truncated at the sequence ends) and, when
     // causal, sigma[q] <= sigma[p]; each thread reads its chunk's sigma in one
@@ -539,9 +540,10 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem + P.off_bits) +
                      (wg * 2 + ((it >> 1) & 1)) * (P.Bt * NCH);
     {
-      const int nwords = P.Bt * NCH;
-      for (int w = r; w < nwords; w += kBM) {
-        const int tt = w / NCH, ch = w - tt * NCH;
+      // each warp builds the words of its own tokens (rows quad*32 .. +31)
+      const int tpw = 32 >> P.log2g;
+      for (int w = lane; w < tpw * NCH; w += 32) {
+        const int tt = quad * tpw + w / NCH, ch = w % NCH;
         const int lo = max(tt, P.left - tw.p0);
         const int hi = tw.p0 + tt < P.n ? min(tt + P.left + P.right, P.n - 1 - tw.p0 + P.left) : -1;
         uint32_t word = band_bits(lo, hi, ch * 32);
@@ -561,14 +563,11 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
           }
           word &= cw;
         }
-        wbuf[w] = word;
+        wbuf[tt * NCH + ch] = word;
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars + 8 * (kWsync + wg));
-    if (!wwait(bars + 8 * (kWsync + wg), ph)) break;
     const uint32_t* wrow = wbuf + t * NCH;
-    __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kSfree + wg));  // sigma no longer read
 
     if (!wwait(bars + 8 * (kSfull + wg), ph)) break;
@@ -730,7 +729,6 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
       mbar_init(bars + 8 * (kPfull + w), 4);
       mbar_init(bars + 8 * (kOfull + w), 1);
       mbar_init(bars + 8 * (kTempty + w), 4);
-      mbar_init(bars + 8 * (kWsync + w), 4);
     }
     mbar_init(bars + 8 * kDrain, 1);
     *abort_flag = 0;

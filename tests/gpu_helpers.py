@@ -25,7 +25,7 @@ def span(path: str, g: int, w: int) -> int:
 
 def _ring_fits(sp: int, g: int, d: int) -> bool:
     """The ring kernel's resources: 2 Q stages, K and V rings of span + 2 Bt
-    rows, the doubled sigma ring, two new-token lists, the mask words and 27
+    rows, the doubled sigma ring, two new-token lists, the mask words and 25
     barriers in 227 KB of shared memory; two TMEM stages in 512 columns."""
     rnd = lambda x, m: -(-x // m) * m
     pad = rnd(sp, 32)
@@ -35,7 +35,7 @@ def _ring_fits(sp: int, g: int, d: int) -> bool:
     off_vtok = rnd(off_sig + 2 * r * 4, 16)
     off_bits = rnd(off_vtok + 2 * pad * 4, 16)
     off_bar = rnd(off_bits + 4 * bt * (pad // 32) * 4, 64)
-    smem = off_bar + 8 * 27 + 16 + 1024
+    smem = off_bar + 8 * 25 + 16 + 1024
     cols = rnd(max(pad, pad // 2 + d), 32)
     return pad <= 160 and smem <= 232448 and 2 * cols <= 512
 
