@@ -12,17 +12,16 @@
 // sequence share all but Bt rows of their key span, so K and V live in a
 // ring of R = span + 2*Bt rows and each tile fetches only its Bt new rows
 // (plus its 128 Q rows); the first tile of a run fetches the whole span.
-// Three producer warps fetch rows with 16-byte cp.async copies (the widest
+// Producer warps fetch rows with 16-byte cp.async copies (the widest
 // random-row gather path measured on this part), computing the 128-byte
 // swizzle themselves.  Q and K of a tile are needed only by S = Q K^T, V only
 // by O = P V, so they land on separate barriers and are released separately:
-// a Q stage and the K rows a tile overwrites are free once the S MMA of the
-// tile three back has completed, V rows once its O MMA has.  V is fetched one tile behind Q and K (it is not needed
-// until the softmax is done), so the loads of Q and K run ahead of the
-// tensor cores without waiting for the softmax.  The sigma values of the next tile's new positions
-// are loaded into registers one tile ahead.  The key tokens sigma[q] of the
-// ring are kept twice (slots s and s + R) so that a tile's span is always a
-// plain contiguous array.
+// a Q stage is free once the S MMA of the tile two back has completed, the K
+// rows a tile overwrites once that of the tile three back has, V rows once
+// its O MMA has.  The sigma values of the next tile's new positions are
+// loaded into registers one tile ahead.  The key tokens sigma[q] of the ring
+// are kept twice (slots s and s + R) so that a tile's span is always a plain
+// contiguous array.
 //
 // Roles (four warpgroups, 512 threads):
 //   warps 0-6   producers: sigma of new positions, cp.async of Q / K / V rows
@@ -251,15 +250,9 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
   };
 
   // V rows of tile x: they overwrite those of tile x - 3 (a new run: of
-  // every tile in flight).  Unless `own_wait`, the caller's barrier has
-  // already covered that wait.
+  // every tile in flight); the Q/K barrier before them covers that wait.
   auto v_upto = [&](int x, const TileWalk& w) { return w.new_seg ? x - 1 : x - kVDepth; };
-  auto load_v = [&](int x, const TileWalk& w, bool own_wait) {
-    if (own_wait) {
-      bool ok = true;
-      if (tid == 0) ok = retire(kPVdone, kVDepth, pv_seen, v_upto(x, w));
-      if (!agree(votes + 1, ok)) return false;
-    }
+  auto load_v = [&](int x, const TileWalk& w) {
     const int32_t* vt = vtok + (x & 1) * P.span_pad;
     const size_t rowbase = size_t(w.b) * P.n;
     for (int i0 = r_first; i0 < w.nld; i0 += RPP * kBatch) {
@@ -380,20 +373,12 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
     nxt.step(P, begin);
     fetch(nxt, pre);
   }
-  // Iteration it loads sigma/Q/K of tile it and V of tile it - 1, whose wait
-  // is folded into the Q/K barrier; before a new run the V of the previous
-  // tile goes first (the run's loads wait for every tile in flight, that
-  // tile's O MMA included).
-  for (int it = 0; it <= ntiles; ++it) {
-    const TileWalk prev = cur;
-    const bool has_cur = it < ntiles;
-    if (has_cur) cur = nxt;
-    const bool v_first = has_cur && cur.new_seg;
-    if (it >= 1 && v_first && !load_v(it - 1, prev, true)) break;
-    if (has_cur && !load_qk(it, cur, nxt, pre, it + 1 < ntiles,
-                            (it >= 1 && !v_first) ? v_upto(it - 1, prev) : -1))
-      break;
-    if (it >= 1 && !v_first && !load_v(it - 1, prev, !has_cur)) break;
+  // Iteration it loads sigma, Q, K and V of tile it; the V rows' wait is
+  // folded into the Q/K barrier.
+  for (int it = 0; it < ntiles; ++it) {
+    cur = nxt;
+    if (!load_qk(it, cur, nxt, pre, it + 1 < ntiles, v_upto(it, cur))) break;
+    if (!load_v(it, cur)) break;
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // own copies land before exit
 }
