@@ -198,6 +198,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The slowest rank's value (replicas run independently; the job's time is
+    the longest one).  Identity when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own batch each step."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -309,11 +326,7 @@ def run_ours(args):
         torch.distributed.barrier()
     clocks = sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), dev)
     status = sa.check_error(err)
     if status != sa.SA_OK:
         raise RuntimeError(f"device error word reports status {status}")
@@ -355,7 +368,7 @@ def run_ours(args):
         return 0
     tokens = wl["batch"] * wl["seq_len"]
     ms_per_step = total_ms / args.steps
-    value = world * tokens / (ms_per_step * 1e-3)
+    value = job_tokens_per_s(world, tokens, ms_per_step)
     bytes_alg, flops_alg = algorithmic(wl)
     peaks = load_peaks()
     achieved = bytes_alg / (ms_per_step * 1e-3) / 1e9
@@ -376,7 +389,7 @@ def run_ours(args):
                       bytes_per_launch=bytes_alg, flops_per_launch=flops_alg,
                       tensor_frac=flops_alg / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"]),
         cpu_baseline=cpu,
-        e2e=dict(value=world * tokens / (e2e_ms * 1e-3), unit="tokens/s",
+        e2e=dict(value=job_tokens_per_s(world, tokens, e2e_ms), unit="tokens/s",
                  h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
         clocks=clocks,
         gpu_launches=args.steps * launches_per_step,
