@@ -15,6 +15,11 @@ sigma once) over its CUDA-event duration with the measured HBM copy peak.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference
 implementation of this method) on the host cores instead.
+
+``--workload`` times one of the other shapes instead of the headline (the
+pretraining layer, the very long context gated merge, the length sweep), with
+``--window`` / ``--seq-len`` overrides; their ``roofline`` uses whichever leg
+(HBM bytes or tensor FLOPs) bounds them.
 """
 
 from __future__ import annotations
@@ -33,8 +38,23 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = dict(workload="long_prefill_gqa", batch=1, seq_len=32768, num_q_heads=32,
-                num_kv_heads=8, head_dim=128, window=128, causal=True, path="sa", seed=0)
+                num_kv_heads=8, head_dim=128, window=128, causal=True, path="sa", seed=0,
+                std=None)
 METRIC = "SA fwd tokens/s and % roofline (bf16, n=32K, w=128, GQA 32q/8kv, d=128)"
+# The other workload shapes (--workload): causal SA or the causal gated SA+SWA
+# merge (gate logits ~ N(0, 1)); the default above is the headline.
+WORKLOADS = {
+    "long_prefill_gqa": WORKLOAD,
+    "pretrain_layer": dict(workload="pretrain_layer", batch=4, seq_len=2048, num_q_heads=16,
+                           num_kv_heads=16, head_dim=64, window=128, causal=True, path="gated",
+                           seed=0, std=1.0 / 8.0),
+    "very_long_context": dict(workload="very_long_context", batch=1, seq_len=131072,
+                              num_q_heads=32, num_kv_heads=4, head_dim=128, window=1024,
+                              causal=True, path="gated", seed=0, std=None),
+    "length_sweep": dict(workload="length_sweep", batch=1, seq_len=262144, num_q_heads=16,
+                         num_kv_heads=16, head_dim=128, window=128, causal=True, path="sa",
+                         seed=0, std=None),
+}
 PROFILE = os.path.join(ROOT, "profiles", "sa_ring_kernel_long_prefill_gqa_w128.md")
 # the ring kernel and the tcgen05 helpers it inlines: the profile's DRAM
 # counters hold only while these files are unchanged
@@ -52,11 +72,31 @@ def causal_sa_pairs(n: int, window: int) -> int:
     return n + sum(n - d for d in range(1, h + 1))
 
 
+def swa_pairs(n: int, window: int) -> int:
+    """Attended pairs of SWA: keys [i - w + 1, i] clipped at 0."""
+    w = min(window, n)
+    return n * w - w * (w - 1) // 2
+
+
 def algorithmic(wl) -> tuple[int, float]:
+    """Bytes the path must move (Q, K, V and Y once, sigma, gate logits when
+    gated) and FLOPs it must do (QK^T and PV, 2d each, per attended pair)."""
     b, n, hq, hkv, d = wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"], wl["head_dim"]
     bytes_alg = 2 * b * n * d * (hq + 2 * hkv + hq) + 4 * b * n
-    flops = 4.0 * d * hq * b * causal_sa_pairs(n, wl["window"])
+    pairs = causal_sa_pairs(n, wl["window"])
+    if wl["path"] == "gated":
+        bytes_alg += 2 * 4 * b * n * hq
+        pairs += swa_pairs(n, wl["window"])
+    flops = 4.0 * d * hq * b * pairs
     return bytes_alg, flops
+
+
+def metric_of(wl) -> str:
+    if wl is WORKLOAD:
+        return METRIC
+    what = "gated SA+SWA" if wl["path"] == "gated" else "SA"
+    return (f"{what} fwd tokens/s and % roofline (bf16, n={wl['seq_len']}, w={wl['window']}, "
+            f"{wl['num_q_heads']}q/{wl['num_kv_heads']}kv, d={wl['head_dim']})")
 
 
 def load_peaks() -> dict:
@@ -95,27 +135,35 @@ def profiled_traffic() -> int | None:
 
 # ------------------------------------------------------------------ oracle leg
 
-def _oracle_chunk(rows):
+def _oracle_rows(rows):
     import oracle
-    oracle.sa_rows(_G["q"], _G["k"], _G["v"], _G["perm"], _G["window"], _G["causal"], rows=rows)
+    if _G["path"] == "gated":
+        oracle.gated_rows(_G["q"], _G["k"], _G["v"], _G["perm"], _G["ga"], _G["gw"], _G["window"],
+                          None, _G["causal"], rows=rows)
+    else:
+        oracle.sa_rows(_G["q"], _G["k"], _G["v"], _G["perm"], _G["window"], _G["causal"], rows=rows)
+
+
+def _oracle_chunk(rows):
+    _oracle_rows(rows)
     return len(rows)
 
 
 def publish_oracle_inputs(case, perm, wl):
     """Make the inputs visible to oracle workers forked after this call."""
-    _G.update(q=case.q, k=case.k, v=case.v, perm=perm, window=wl["window"], causal=wl["causal"])
+    _G.update(q=case.q, k=case.k, v=case.v, perm=perm, window=wl["window"], causal=wl["causal"],
+              path=wl["path"], ga=case.gate_sa, gw=case.gate_swa)
 
 
 def oracle_throughput(case, perm, wl, seconds: float, pool=None, cores: int = 1) -> dict:
     """Time the oracle on a seeded sample of query tokens (all heads of each).
     Workers in ``pool`` must have been forked after publish_oracle_inputs."""
     import numpy as np
-    import oracle
     n = wl["seq_len"]
     rng = np.random.default_rng(1)
     calib = [(0, int(i)) for i in rng.integers(0, n, 16)]
     t0 = time.perf_counter()
-    oracle.sa_rows(case.q, case.k, case.v, perm, wl["window"], wl["causal"], rows=calib)
+    _oracle_rows(calib)
     per_row = max((time.perf_counter() - t0) / len(calib), 1e-6)
     count = int(max(cores * 4, min(n * wl["batch"], seconds * cores / per_row)))
     rows = [(0, int(i)) for i in rng.integers(0, n, count)]
@@ -215,16 +263,24 @@ def job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> fl
     return world * tokens_per_rank / (ms_per_step * 1e-3)
 
 
-def run_reference(args):
+def make_inputs(wl):
+    from sa_synth import make_case
+    return make_case(wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"],
+                     wl["head_dim"], wl["seed"], std=wl["std"], gates=wl["path"] == "gated")
+
+
+def config_of(wl) -> dict:
+    return {k: wl[k] for k in ("workload", "batch", "seq_len", "num_q_heads", "num_kv_heads",
+                               "head_dim", "window", "causal", "path")}
+
+
+def run_reference(args, wl=WORKLOAD):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     import numpy as np
-    from sa_synth import make_case
     import oracle
-    wl = WORKLOAD
-    case = make_case(wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"],
-                     wl["head_dim"], wl["seed"])
+    case = make_inputs(wl)
     perm = np.stack([oracle.make_perm(wl["seed"], 0, b, wl["seq_len"]) for b in range(wl["batch"])])
     cores = len(os.sched_getaffinity(0))
     publish_oracle_inputs(case, perm, wl)
@@ -237,12 +293,11 @@ def run_reference(args):
     tokens = sum(r["value"] * r["seconds"] for r in runs)
     secs = sum(r["seconds"] for r in runs)
     value = tokens / secs
-    line = dict(impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=world,
+    line = dict(impl="reference", metric=metric_of(wl), value=value, unit="tokens/s", n_gpus=world,
                 steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * secs / args.steps,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
                 data="synthetic",
-                config={k: wl[k] for k in ("workload", "batch", "seq_len", "num_q_heads",
-                                           "num_kv_heads", "head_dim", "window", "causal")},
+                config=config_of(wl),
                 cpu_baseline=dict(value=value, unit="tokens/s", cores=cores, kind="oracle",
                                   sample=runs[0]["sample"].split(",")[0] + " per step (seeded "
                                   "sample), fp64 NumPy oracle"),
@@ -252,13 +307,12 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+def run_ours(args, wl=WORKLOAD):
     import numpy as np
     rank, world, local = dist_env()
-    wl = WORKLOAD
-    from sa_synth import bf16_bits, make_case
-    case = make_case(wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"],
-                     wl["head_dim"], wl["seed"])
+    from sa_synth import bf16_bits
+    case = make_inputs(wl)
+    gated = wl["path"] == "gated"
 
     import stochastic_sliding_window_gb300 as sa
     sa.load()
@@ -286,13 +340,22 @@ def run_ours(args):
 
     q, k, v = to_dev(case.q), to_dev(case.k), to_dev(case.v)
     perm = torch.from_numpy(perm_np).to(dev)
+    ga = torch.from_numpy(case.gate_sa).to(dev) if gated else None
+    gw = torch.from_numpy(case.gate_swa).to(dev) if gated else None
     out = torch.empty_like(q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def forward(q_, k_, v_, p_, ga_, gw_, o_):
+        if gated:
+            sa.sa_swa_gated_forward(q_, k_, v_, p_, ga_, gw_, wl["window"], causal=wl["causal"],
+                                    out=o_, err=err, stream=stream)
+        else:
+            sa.sa_forward(q_, k_, v_, p_, wl["window"], causal=wl["causal"], out=o_, err=err,
+                          stream=stream)
+
     def step():
-        sa.sa_forward(q, k, v, perm, wl["window"], causal=wl["causal"], out=out, err=err,
-                      stream=stream)
+        forward(q, k, v, perm, ga, gw, out)
 
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
     for _ in range(args.warmup):
@@ -337,23 +400,26 @@ def run_ours(args):
     hv = torch.from_numpy(bf16_bits(case.v).view(np.int16)).view(torch.bfloat16).pin_memory()
     hp = torch.from_numpy(perm_np).pin_memory()
     hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hp))
+    hins = [hq, hk, hv, hp]
+    if gated:
+        hins += [torch.from_numpy(case.gate_sa).pin_memory(),
+                 torch.from_numpy(case.gate_swa).pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in hins)
     d2h = hout.numel() * hout.element_size()
-    q2, k2, v2, p2, o2 = (torch.empty_like(x) for x in (q, k, v, perm, out))
+    dins = [torch.empty_like(x, device=dev) for x in hins]
+    o2 = torch.empty_like(out)
 
     def e2e_step():
-        q2.copy_(hq, non_blocking=True)
-        k2.copy_(hk, non_blocking=True)
-        v2.copy_(hv, non_blocking=True)
-        p2.copy_(hp, non_blocking=True)
-        sa.sa_forward(q2, k2, v2, p2, wl["window"], causal=wl["causal"], out=o2, err=err,
-                      stream=stream)
+        for dst, src in zip(dins, hins):
+            dst.copy_(src, non_blocking=True)
+        forward(dins[0], dins[1], dins[2], dins[3], dins[4] if gated else None,
+                dins[5] if gated else None, o2)
         hout.copy_(o2, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize(dev)
-    e2e_steps = max(3, min(args.steps, 50))
+    e2e_steps = max(3, min(args.steps, 50 if wl is WORKLOAD else 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
@@ -371,23 +437,30 @@ def run_ours(args):
     value = job_tokens_per_s(world, tokens, ms_per_step)
     bytes_alg, flops_alg = algorithmic(wl)
     peaks = load_peaks()
-    achieved = bytes_alg / (ms_per_step * 1e-3) / 1e9
-    traffic = profiled_traffic()
+    secs = ms_per_step * 1e-3
+    tensor_bound = flops_alg / (peaks["bf16_tflops"] * 1e12) > bytes_alg / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:  # the slower of the two roofline legs bounds the path
+        roof = dict(bound="tensor", achieved=flops_alg / secs / 1e12, peak=peaks["bf16_tflops"],
+                    unit="TFLOP/s", peak_source=f"{peaks['source']} bf16_tflops (burst)")
+    else:
+        roof = dict(bound="hbm", achieved=bytes_alg / secs / 1e9, peak=peaks["hbm_gbs"],
+                    unit="GB/s", peak_source=f"{peaks['source']} hbm_gbs (copy, read+write)")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profiled_traffic() if wl is WORKLOAD else None
+    roof.update(bytes_per_launch=bytes_alg, flops_per_launch=flops_alg,
+                hbm_frac=bytes_alg / secs / 1e9 / peaks["hbm_gbs"],
+                tensor_frac=flops_alg / secs / 1e12 / peaks["bf16_tflops"])
+    in_mb = (bytes_alg - 2 * wl["batch"] * wl["seq_len"] * wl["num_q_heads"] * wl["head_dim"]) / 1e6
     line = dict(
-        metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
+        metric=metric_of(wl), value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
         warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True, scaling="weak",
         vs_baseline=None, dtype="bf16", data="synthetic",
-        config={k: wl[k] for k in ("workload", "batch", "seq_len", "num_q_heads", "num_kv_heads",
-                                   "head_dim", "window", "causal", "path")}
-        | dict(l2="flushed between steps (256 MB write); inputs 671 MB > L2",
+        config=config_of(wl)
+        | dict(l2=f"flushed between steps (256 MB write); inputs {in_mb:.0f} MB",
                kernel={sa.KERNEL_SIMT: "simt", sa.KERNEL_TCGEN05_GATHER: "tcgen05-gather",
                        sa.KERNEL_TCGEN05_RING: "tcgen05-ring"}.get(kernel, str(kernel)),
                parallelism="replicas" if world > 1 else "single-gpu"),
-        roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
-                      frac=achieved / peaks["hbm_gbs"], traffic=traffic,
-                      peak_source=f"{peaks['source']} hbm_gbs (copy, read+write)",
-                      bytes_per_launch=bytes_alg, flops_per_launch=flops_alg,
-                      tensor_frac=flops_alg / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"]),
+        roofline=roof,
         cpu_baseline=cpu,
         e2e=dict(value=job_tokens_per_s(world, tokens, e2e_ms), unit="tokens/s",
                  h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
@@ -408,12 +481,19 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--soak-seconds", type=float, default=1.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long_prefill_gqa",
+                    help="shape to time (default: the long-prefill GQA headline)")
+    ap.add_argument("--window", type=int, default=0, help="override the workload's window")
+    ap.add_argument("--seq-len", type=int, default=0, help="override the workload's length")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+    if args.window or args.seq_len:
+        wl = dict(wl, window=args.window or wl["window"], seq_len=args.seq_len or wl["seq_len"])
     if args.impl == "reference":
-        return run_reference(args)
-    return run_ours(args)
+        return run_reference(args, wl)
+    return run_ours(args, wl)
 
 
 if __name__ == "__main__":
