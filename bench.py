@@ -458,7 +458,8 @@ def run_ours(args, wl=WORKLOAD):
         config=config_of(wl)
         | dict(l2=f"flushed between steps (256 MB write); inputs {in_mb:.0f} MB",
                kernel={sa.KERNEL_SIMT: "simt", sa.KERNEL_TCGEN05_GATHER: "tcgen05-gather",
-                       sa.KERNEL_TCGEN05_RING: "tcgen05-ring"}.get(kernel, str(kernel)),
+                       sa.KERNEL_TCGEN05_RING: "tcgen05-ring",
+                       sa.KERNEL_TCGEN05_FLASH: "tcgen05-flash"}.get(kernel, str(kernel)),
                parallelism="replicas" if world > 1 else "single-gpu"),
         roofline=roof,
         cpu_baseline=cpu,

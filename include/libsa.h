@@ -70,7 +70,9 @@ enum {
   SA_KERNEL_SIMT = 1,    /* CUDA-core kernel: any window, the correctness baseline */
   SA_KERNEL_TCGEN05 = 2, /* the better-fitting tcgen05 kernel; SA_ERR_UNSUPPORTED if none fits */
   SA_KERNEL_TCGEN05_GATHER = 3, /* tcgen05 kernel that gathers every window with TMA */
-  SA_KERNEL_TCGEN05_RING = 4    /* tcgen05 kernel with a sliding K/V ring (spans <= 160 keys) */
+  SA_KERNEL_TCGEN05_RING = 4,   /* tcgen05 kernel with a sliding K/V ring (spans <= 160 keys) */
+  SA_KERNEL_TCGEN05_FLASH = 5   /* tcgen05 kernel streaming the span in 128-key chunks with an
+                                   online softmax (any window) */
 };
 
 /* Bits of the device error word. */
@@ -170,9 +172,9 @@ const char* sa_status_string(sa_status_t status);
 /* Detail of the last failing call on this thread ("" if none). */
 const char* sa_last_error_message(void);
 
-/* SA_KERNEL_SIMT, SA_KERNEL_TCGEN05_GATHER or SA_KERNEL_TCGEN05_RING: the
- * kernel the last successful forward call on this thread launched (0 before
- * any). */
+/* SA_KERNEL_SIMT, SA_KERNEL_TCGEN05_GATHER, SA_KERNEL_TCGEN05_RING or
+ * SA_KERNEL_TCGEN05_FLASH: the kernel the last successful forward call on
+ * this thread launched (0 before any; for the gated path, the SA pass's). */
 int32_t sa_last_kernel(void);
 
 /* Number of kernel launches the last successful forward call on this thread

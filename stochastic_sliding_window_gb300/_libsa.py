@@ -20,6 +20,7 @@ LIB_PATH = Path(__file__).resolve().with_name("libsa.so")
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_BAD_PERM, SA_ERR_TIMEOUT, \
     SA_ERR_INTERNAL = range(7)
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TCGEN05, KERNEL_TCGEN05_GATHER, KERNEL_TCGEN05_RING = 0, 1, 2, 3, 4
+KERNEL_TCGEN05_FLASH = 5
 ERRBIT_RANGE, ERRBIT_DUP, ERRBIT_TIMEOUT, ERRBIT_INTERNAL = 1, 2, 4, 8
 
 # Every function the header declares, with (restype, argtypes).

@@ -43,7 +43,7 @@ static sa_status_t check_params(const sa_params_t* prm, bool need_window) {
   if (prm->head_dim != 64 && prm->head_dim != 128)
     return fail(SA_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", prm->head_dim);
   if (need_window && prm->window < 1) return fail(SA_ERR_INVALID_ARG, "window must be >= 1");
-  if (prm->kernel < SA_KERNEL_AUTO || prm->kernel > SA_KERNEL_TCGEN05_RING)
+  if (prm->kernel < SA_KERNEL_AUTO || prm->kernel > SA_KERNEL_TCGEN05_FLASH)
     return fail(SA_ERR_INVALID_ARG, "unknown kernel selector %d", prm->kernel);
   const double rows = double(prm->batch) * prm->seqlen * prm->num_q_heads;
   if (rows * prm->head_dim >= 9.0e18 || double(prm->batch) * prm->seqlen >= 2147483647.0 ||
@@ -91,25 +91,32 @@ static sa_status_t finish(sa_status_t st, int32_t kernel, int32_t launches) {
   return st;
 }
 
-// The concrete kernel a request maps to for one path (SIMT, gather, ring),
-// or 0 when the requested tcgen05 variant cannot run this shape.
+// The concrete kernel a request maps to for one path (SIMT, gather, ring,
+// flash), or 0 when the requested tcgen05 variant cannot run this shape.
+// The tcgen05 preference: the ring kernel (narrow spans), else the flash
+// kernel (any span), else the gather kernel.
 static int32_t pick_kernel(const sa_params_t* prm, const Problem& pb, Path path) {
   const bool ring = ring_supported(pb, path);
+  const bool flash = flash_supported(pb, path);
   const bool gather = tc_supported(pb, path);
+  const int32_t best = ring ? SA_KERNEL_TCGEN05_RING
+                       : flash ? SA_KERNEL_TCGEN05_FLASH
+                       : gather ? SA_KERNEL_TCGEN05_GATHER
+                                : 0;
   switch (prm->kernel) {
     case SA_KERNEL_SIMT: return SA_KERNEL_SIMT;
     case SA_KERNEL_TCGEN05_RING: return ring ? SA_KERNEL_TCGEN05_RING : 0;
     case SA_KERNEL_TCGEN05_GATHER: return gather ? SA_KERNEL_TCGEN05_GATHER : 0;
-    case SA_KERNEL_TCGEN05:
-      return ring ? SA_KERNEL_TCGEN05_RING : gather ? SA_KERNEL_TCGEN05_GATHER : 0;
-    default:
-      return ring ? SA_KERNEL_TCGEN05_RING : gather ? SA_KERNEL_TCGEN05_GATHER : SA_KERNEL_SIMT;
+    case SA_KERNEL_TCGEN05_FLASH: return flash ? SA_KERNEL_TCGEN05_FLASH : 0;
+    case SA_KERNEL_TCGEN05: return best;
+    default: return best ? best : SA_KERNEL_SIMT;
   }
 }
 
 static sa_status_t launch_kernel(int32_t kernel, const Problem& pb, Path path, const float* gate,
                                  int accumulate, cudaStream_t s) {
   if (kernel == SA_KERNEL_TCGEN05_RING) return launch_ring(pb, path, gate, accumulate, s);
+  if (kernel == SA_KERNEL_TCGEN05_FLASH) return launch_flash(pb, path, gate, accumulate, s);
   return launch_tc(pb, path, gate, accumulate, s);
 }
 

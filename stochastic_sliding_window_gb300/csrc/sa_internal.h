@@ -1,5 +1,6 @@
 // Internal interface between the C-ABI entry points (sa_api.cu) and the
-// kernel launchers (sa_perm.cu, sa_simt.cu, sa_tc.cu).  Not installed.
+// kernel launchers (sa_perm.cu, sa_simt.cu, sa_tc.cu, sa_tc_ring.cu,
+// sa_tc_flash.cu).  Not installed.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -58,6 +59,13 @@ bool tc_supported(const Problem& pb, Path path);
 sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int accumulate,
                         cudaStream_t stream);
 bool ring_supported(const Problem& pb, Path path);
+
+// tcgen05 kernel streaming each tile's key span through shared memory in
+// 128-key chunks with an online softmax: any window.  Same contract as
+// launch_tc.
+sa_status_t launch_flash(const Problem& pb, Path path, const float* gate, int accumulate,
+                         cudaStream_t stream);
+bool flash_supported(const Problem& pb, Path path);
 
 // sigma^{-1} kernels.
 sa_status_t launch_inverse_perm(const int32_t* perm, int32_t* inv, int batch, int n,

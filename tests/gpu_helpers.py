@@ -13,8 +13,9 @@ from sa_synth import make_case
 MAX_ABS = 2e-2
 REL_L2 = 5e-3
 
-KERNELS = [sa.KERNEL_SIMT, sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING]
-KERNEL_IDS = ["simt", "gather", "ring"]
+KERNELS = [sa.KERNEL_SIMT, sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING,
+           sa.KERNEL_TCGEN05_FLASH]
+KERNEL_IDS = ["simt", "gather", "ring", "flash"]
 
 
 def span(path: str, g: int, w: int) -> int:
@@ -42,11 +43,14 @@ def _ring_fits(sp: int, g: int, d: int) -> bool:
 
 def must_support(kernel: int, path: str, g: int, w: int, w_swa: int = 0, d: int = 128) -> bool:
     """Shapes each tcgen05 variant is required to accept (the ring kernel
-    exactly; the gather kernel at least up to 256-key windows)."""
+    exactly; the flash kernel any window; the gather kernel at least up to
+    256-key windows)."""
     if kernel == sa.KERNEL_SIMT:
         return True
     if 128 % g:
         return False
+    if kernel == sa.KERNEL_TCGEN05_FLASH:
+        return d in (64, 128) and g <= 32
     paths = [("sa", w), ("swa", w_swa or w)] if path == "gated" else [(path, w)]
     if kernel == sa.KERNEL_TCGEN05_RING:
         return (128 // g) % 16 == 0 and all(_ring_fits(span(pp, g, ww), g, d) for pp, ww in paths)
@@ -56,7 +60,7 @@ def must_support(kernel: int, path: str, g: int, w: int, w_swa: int = 0, d: int 
 def kernel_ran(requested: int) -> bool:
     got = sa.last_kernel()
     if requested == sa.KERNEL_TCGEN05:
-        return got in (sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING)
+        return got in (sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING, sa.KERNEL_TCGEN05_FLASH)
     return got == requested
 
 

@@ -98,6 +98,12 @@ def test_tensor_core_and_simt_kernels_agree():
         b = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
                           kernel=sa.KERNEL_TCGEN05_GATHER)
         assert torch.equal(a, b)
+    for w in (32, 128):
+        # the flash kernel streams the same windows in chunks (online softmax)
+        a = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_TCGEN05_RING)
+        b = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
+                          kernel=sa.KERNEL_TCGEN05_FLASH)
+        assert (a.float() - b.float()).abs().max().item() <= 2e-2
     for w in (32, 128, 256):
         a = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_TCGEN05)
         b = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_SIMT)
@@ -116,10 +122,14 @@ def test_auto_kernel_choice():
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 128)
     assert sa.last_kernel() == sa.KERNEL_TCGEN05_RING and sa.last_launch_count() == 1
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 256)
-    assert sa.last_kernel() == sa.KERNEL_TCGEN05_GATHER
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_FLASH
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2048)
-    assert sa.last_kernel() == sa.KERNEL_SIMT
-    for k in (sa.KERNEL_TCGEN05, sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING):
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_FLASH
+    sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2048, kernel=sa.KERNEL_TCGEN05)
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_FLASH
+    sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 256, kernel=sa.KERNEL_TCGEN05_GATHER)
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_GATHER
+    for k in (sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING):
         with pytest.raises(sa.SaError) as ei:
             sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2048, kernel=k)
         assert ei.value.status == sa.SA_ERR_UNSUPPORTED

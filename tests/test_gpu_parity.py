@@ -136,9 +136,14 @@ def test_long_prefill_gqa_causal_sa(long_prefill, w):
     err = _err()
     y = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, err=err)
     assert sa.check_error(err) == sa.SA_OK
-    assert sa.last_kernel() == (sa.KERNEL_TCGEN05_RING if w <= 128 else sa.KERNEL_TCGEN05_GATHER)
+    assert sa.last_kernel() == (sa.KERNEL_TCGEN05_RING if w <= 128 else sa.KERNEL_TCGEN05_FLASH)
     want = oracle.sa_rows(inp.case.q, inp.case.k, inp.case.v, perm, w, True, rows=rows)
     compare(gather_rows(y, rows), want, f"c3 w={w}")
+    # the chunked online-softmax kernel on the same rows
+    yf = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
+                       kernel=sa.KERNEL_TCGEN05_FLASH, err=err)
+    assert sa.check_error(err) == sa.SA_OK
+    compare(gather_rows(yf, rows), want, f"c3 flash w={w}")
     # the gather kernel computes the same MMAs and softmax: identical bits
     yg = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
                        kernel=sa.KERNEL_TCGEN05_GATHER, err=err)
@@ -161,6 +166,7 @@ def test_very_long_context_gated(w):
     err = _err()
     y = sa.sa_swa_gated_forward(inp.q, inp.k, inp.v, perm_d, inp.ga, inp.gw, w, causal=True, err=err)
     assert sa.check_error(err) == sa.SA_OK
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_FLASH and sa.last_launch_count() == 2
     compare(gather_rows(y, rows), _want("gated", inp, perm, w, True, rows=rows), f"c4 w={w}")
 
 
