@@ -346,13 +346,16 @@ def run_ours(args, wl=WORKLOAD):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    kern = {"auto": sa.KERNEL_AUTO, "simt": sa.KERNEL_SIMT, "gather": sa.KERNEL_TCGEN05_GATHER,
+            "ring": sa.KERNEL_TCGEN05_RING, "flash": sa.KERNEL_TCGEN05_FLASH}[args.kernel]
+
     def forward(q_, k_, v_, p_, ga_, gw_, o_):
         if gated:
             sa.sa_swa_gated_forward(q_, k_, v_, p_, ga_, gw_, wl["window"], causal=wl["causal"],
-                                    out=o_, err=err, stream=stream)
+                                    out=o_, err=err, stream=stream, kernel=kern)
         else:
             sa.sa_forward(q_, k_, v_, p_, wl["window"], causal=wl["causal"], out=o_, err=err,
-                          stream=stream)
+                          stream=stream, kernel=kern)
 
     def step():
         forward(q, k, v, perm, ga, gw, out)
@@ -486,6 +489,8 @@ def main():
                     help="shape to time (default: the long-prefill GQA headline)")
     ap.add_argument("--window", type=int, default=0, help="override the workload's window")
     ap.add_argument("--seq-len", type=int, default=0, help="override the workload's length")
+    ap.add_argument("--kernel", choices=["auto", "simt", "gather", "ring", "flash"],
+                    default="auto", help="force one of the library's kernels (default: its choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
