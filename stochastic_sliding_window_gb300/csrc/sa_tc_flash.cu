@@ -4,24 +4,26 @@
 //
 // Same attention as the other tcgen05 kernels (Stochastic Attention summary,
 // "Core mechanism" steps 1-3; causal rule from "Theoretical properties"; SWA
-// from "Problem statement"): a tile is Bt = 128/g consecutive permuted
+// from "Problem statement"): a tile here is 2*Bt = 256/g consecutive permuted
 // positions of one (sequence, kv head) pair stacked with the g query heads of
-// that kv head (M = 128 rows, r = t*g + j), over its key span
-// [p0 - left, p0 + Bt - 1 + right].  The span is cut into chunks of 128 keys.
-// Per chunk, S = Q K^T lands in one of two TMEM buffers; the softmax
-// warpgroup masks it (window band and, when causal, sigma[q] <= sigma[p]),
-// keeps a running maximum and sum per row and writes bf16 P over S; O += P V
-// accumulates in TMEM.  A row's reference maximum is raised -- and O and the
+// that kv head (256 rows, r = t*g + j: two M = 128 halves), over its key span
+// [p0 - left, p0 + 2*Bt - 1 + right].  The span is cut into chunks of 128
+// keys, each loaded once for both halves.  Per chunk and half, S = Q K^T lands
+// in the half's TMEM buffer; the half's softmax warpgroup masks it (window
+// band and, when causal, sigma[q] <= sigma[p]), keeps a running maximum and
+// sum per row and writes bf16 P over S; O += P V accumulates in the half's
+// TMEM accumulator.  A row's reference maximum is raised -- and O and the
 // sum rescaled by 2^(old - new) -- only when a chunk's maximum exceeds it by
 // more than 2^8, so most chunks need no correction of O.  Shared memory does
 // not grow with the window: any window fits.
 //
-// Roles (three warpgroups, 384 threads):
-//   warps 0-6   producers: cp.async of the 128 Q rows of a tile and of the 128
+// Roles (four warpgroups, 512 threads):
+//   warps 0-6   producers: cp.async of the 256 Q rows of a tile and of the 128
 //               K and V rows of each chunk (with the chunk's key tokens)
 //   warp 7      lane 0 issues the MMAs in whichever order their operands
 //               become ready; the warp owns TMEM
-//   warps 8-11  softmax, O correction and epilogue (scatter to sigma[p])
+//   warps 8-11  softmax, O correction and epilogue of rows 0-127
+//   warps 12-15 the same for rows 128-255
 // Every wait is bounded (SA_ERRBIT_TIMEOUT); producer copies are drained
 // before exit.
 #include "sa_internal.h"
@@ -34,18 +36,20 @@ namespace flash {
 
 using namespace tcc;
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kProducers = 224;  // warps 0-6
 constexpr int kMmaWarp = 7;
 constexpr int kFirstSoftmaxWarp = 8;
-constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 104;
-constexpr int kSoftmaxRegs = 248;
-static_assert(256 * kCtrlRegs + 128 * kSoftmaxRegs <= kThreads * kLaunchRegs,
+constexpr int kLaunchRegs = 128;
+constexpr int kCtrlRegs = 96;
+constexpr int kSoftmaxRegs = 160;
+static_assert(256 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
+constexpr int kRows = 2 * kBM;      // rows of a tile: two halves of M = 128
 constexpr int kKC = 128;            // keys per chunk
 constexpr int kSub = kKC / 32;      // 32-column pieces of a chunk
-constexpr int kMaxRows = 10;        // rows per producer thread per tile or chunk
+constexpr int kMaxRows = 10;        // rows per producer thread per chunk
+constexpr int kBatch = 8;           // Q rows whose tokens are loaded before their copies
 constexpr float kRescaleLog2 = 8.f; // raise a row's reference maximum past 2^8
 constexpr uint32_t kMaxSmem = 232448;
 
@@ -62,25 +66,25 @@ struct Params {
   int causal, accumulate;
   float scale_log2;
   int tiles_per_seq, num_tiles;
-  uint32_t q_bytes, kv_bytes;  // one Q stage; one K (or V) chunk
+  uint32_t q_bytes, kv_bytes;  // one half (128 rows) of the Q tile; one K (or V) chunk
   uint32_t off_k, off_v, off_csig, off_qtok, off_bits, off_bar;
   int tmem_alloc;
   long long timeout_cycles;
 };
 
-// Barrier slots (8 bytes each) after off_bar.  [2] families: tile families
-// are indexed by the CTA-local tile x & 1, chunk families by the CTA-local
-// chunk number c_all & 1 (c_all = x * nchunks + chunk).
+// Barrier slots (8 bytes each) after off_bar.  Chunk stages are indexed by
+// the CTA-local chunk number c_all & 1 (c_all = x * nchunks + chunk); [2]
+// half families by the half (softmax warpgroup) h.
 enum : uint32_t {
-  kQfull = 0,    // [2] Q rows and tokens of tile x landed (cp.async)
-  kQfree = 2,    // [2] last S MMA of tile x done: its Q stage is free
-  kCfull = 4,    // [2] K, V rows and key tokens of chunk c_all landed
-  kCfree = 6,    // [2] O MMA of chunk c_all done: its stage is free
-  kSfull = 8,    // [2] S of chunk c_all in TMEM buffer c_all & 1
-  kPfull = 10,   // [2] P of chunk c_all written (4 softmax warps)
-  kPVdone = 12,  // [2] O MMA of chunk c_all done: S buffer free, O current
-  kOfull = 14,   // last O MMA of tile x done
-  kOfree = 15,   // the epilogue has read O of tile x (4 softmax warps)
+  kQfull = 0,    // Q rows and tokens of tile x landed (cp.async)
+  kQfree = 1,    // both halves' last S MMA of tile x done: the Q stage is free
+  kCfull = 2,    // [2] K, V rows and key tokens of chunk c_all landed
+  kCfree = 4,    // [2] both halves' O MMA of chunk c_all done: its stage is free
+  kSfull = 6,    // [h] S of the half's current chunk in its TMEM buffer
+  kPfull = 8,    // [h] P of the half's current chunk written (4 softmax warps)
+  kPVdone = 10,  // [h] the half's O MMA of its current chunk done
+  kOfull = 12,   // [h] the half's last O MMA of tile x done
+  kOfree = 14,   // [h] the half's epilogue has read O of tile x (4 warps)
   kDrain = 16,
   kNumBars = 17,
 };
@@ -187,39 +191,43 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
   if (ntiles > 0) fetch_chunk(0);
   for (int x = 0; x < ntiles; ++x) {
     const Tile t = tile_of(P, begin + x);
-    const int qs = x & 1;
-    // Q stage of tile x - 2 is free once that tile's last S MMA is done.
+    // The Q stage is free once both halves' last S MMA of tile x - 1 is done.
     bool ok = true;
-    if (tid == 0 && x >= 2) ok = wait(bars + 8 * (kQfree + qs), uint32_t((x >> 1) - 1) & 1u);
+    if (tid == 0 && x >= 1) ok = wait(bars + 8 * kQfree, uint32_t(x - 1) & 1u);
     if (!agree(ok)) break;
     {
-      const uint32_t sq = sbase + uint32_t(qs) * P.q_bytes + kb * (kBM * 128);
+      // 256 rows (r = t*g + j) in two halves of [128 rows x D], each two
+      // K-blocks of [128 rows x 128 B], swizzled.
       const __nv_bfloat16* qbase =
           P.q + (size_t(t.b) * P.n * P.Hq + size_t(t.kvh) * P.g) * D + cc * 8;
-      int tq[kMaxRows];
+      for (int r0 = r_first; r0 < kRows; r0 += RPP * kBatch) {
+        int tq[kBatch];
 #pragma unroll
-      for (int k = 0; k < kMaxRows; ++k) {
-        const int r = r_first + RPP * k;
-        if (r < kBM) tq[k] = token(t, t.p0 + (r >> P.log2g));
-      }
+        for (int k = 0; k < kBatch; ++k) {
+          const int r = r0 + RPP * k;
+          if (r < kRows) tq[k] = token(t, t.p0 + (r >> P.log2g));
+        }
 #pragma unroll
-      for (int k = 0; k < kMaxRows; ++k) {
-        const int r = r_first + RPP * k;
-        if (r < kBM)
-          cp_async16(sq + r * 128 + ((c8 ^ (r & 7)) << 4),
-                     qbase + tq[k] * tokstride + (r & (P.g - 1)) * D);
+        for (int k = 0; k < kBatch; ++k) {
+          const int r = r0 + RPP * k;
+          if (r < kRows)
+            cp_async16(sbase + uint32_t(r >> 7) * P.q_bytes + kb * (kBM * 128) + (r & 127) * 128 +
+                           ((c8 ^ (r & 7)) << 4),
+                       qbase + tq[k] * tokstride + (r & (P.g - 1)) * D);
+        }
       }
-      if (P.perm && tid < P.Bt) {  // the tile's tokens, for the softmax warps
-        const int qc = min(t.p0 + tid, P.n - 1);
-        cp_async4(sbase + P.off_qtok + uint32_t(qs * kBM + tid) * 4,
-                  P.perm + size_t(t.b) * P.n + qc);
+      if (P.perm) {  // the tile's tokens, for the softmax warps
+        for (int i = tid; i < P.Bt; i += kProducers) {
+          const int qc = min(t.p0 + i, P.n - 1);
+          cp_async4(sbase + P.off_qtok + uint32_t(i) * 4, P.perm + size_t(t.b) * P.n + qc);
+        }
       }
-      cp_async_arrive_noinc(bars + 8 * (kQfull + qs));
+      cp_async_arrive_noinc(bars + 8 * kQfull);
     }
     for (int c = 0; c < nch; ++c) {
       const int call = x * nch + c;
       const int s = call & 1;
-      // The stage's previous chunk (call - 2) must have had its O MMA.
+      // The stage's previous chunk (call - 2) must have had both halves' O MMAs.
       ok = true;
       if (tid == 0 && call >= 2) ok = wait(bars + 8 * (kCfree + s), uint32_t((call >> 1) - 1) & 1u);
       if (!agree(ok)) {
@@ -259,69 +267,73 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   cta_range(P, begin, end);
   const int nch = P.nchunks;
   const int total = (end - begin) * nch;
-  const uint32_t o_col = 2 * kKC;
   const uint32_t idesc_qk = idesc_bf16(kBM, kKC, 0);
   const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
-  auto qk = [&](int call) {
-    const int x = call / nch, c = call - x * nch;
-    const int b = call & 1;
+  // S of half h in TMEM columns [h*128, h*128 + 128); O of half h at 256 + h*D.
+  auto qk = [&](int h, int call) {
+    const int c = call % nch;
     fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
     tc_fence_after();
-    const uint32_t d = tmem_base + uint32_t(b * kKC);
-    const uint64_t a0 = sdesc_sw128(sbase + uint32_t(x & 1) * P.q_bytes, 16, 1024);
-    const uint64_t b0 = sdesc_sw128(sbase + P.off_k + uint32_t(b) * P.kv_bytes, 16, 1024);
+    const uint32_t d = tmem_base + uint32_t(h * kKC);
+    const uint64_t a0 = sdesc_sw128(sbase + uint32_t(h) * P.q_bytes, 16, 1024);
+    const uint64_t b0 = sdesc_sw128(sbase + P.off_k + uint32_t(call & 1) * P.kv_bytes, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint64_t da = uint64_t((kk >> 2) * (kBM * 128 / 16) + (kk & 3) * 2);
       const uint64_t db = uint64_t((kk >> 2) * (kKC * 128 / 16) + (kk & 3) * 2);
       umma_bf16(d, a0 + da, b0 + db, idesc_qk, kk > 0 ? 1u : 0u);
     }
-    umma_commit(bars + 8 * (kSfull + b));
-    if (c == nch - 1) umma_commit(bars + 8 * (kQfree + (x & 1)));
+    umma_commit(bars + 8 * (kSfull + h));
+    if (c == nch - 1) umma_commit(bars + 8 * kQfree);
   };
-  auto pv = [&](int call) {
-    const int x = call / nch, c = call - x * nch;
-    const int b = call & 1;
+  auto pv = [&](int h, int call) {
+    const int c = call % nch;
     tc_fence_after();
-    const uint32_t sbuf = tmem_base + uint32_t(b * kKC);
-    uint64_t bd = sdesc_sw128(sbase + P.off_v + uint32_t(b) * P.kv_bytes, kKC * 128, 1024);
+    const uint32_t sbuf = tmem_base + uint32_t(h * kKC);
+    const uint32_t o = tmem_base + uint32_t(2 * kKC + h * D);
+    uint64_t bd = sdesc_sw128(sbase + P.off_v + uint32_t(call & 1) * P.kv_bytes, kKC * 128, 1024);
 #pragma unroll
     for (int kk = 0; kk < kKC / 16; ++kk) {
-      umma_bf16_ts(tmem_base + o_col, sbuf + 8 * kk, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
+      umma_bf16_ts(o, sbuf + 8 * kk, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
       bd += 128;  // 16 keys of 128 B
     }
-    umma_commit(bars + 8 * (kPVdone + b));
-    umma_commit(bars + 8 * (kCfree + b));
-    if (c == nch - 1) umma_commit(bars + 8 * kOfull);
-    (void)x;
+    umma_commit(bars + 8 * (kPVdone + h));
+    umma_commit(bars + 8 * (kCfree + (call & 1)));
+    if (c == nch - 1) umma_commit(bars + 8 * (kOfull + h));
   };
-  // Issue QK(gq) and PV(gp) (gp <= gq) as their operands become ready, PV
-  // first when both are: the softmax warpgroup waits on it.
-  int gq = 0, gp = 0;
+  // Per half: QK(qn) after the half's previous O MMA has read its P (one S
+  // buffer per half), PV(pn) once P is written; PV first when both are ready.
+  int qn[2] = {0, 0}, pn[2] = {0, 0};
   long long last = clock64();
-  while (gp < total) {
+  while (pn[0] < total || pn[1] < total) {
     bool progress = false;
-    if (gp < gq) {
-      const int xp = gp / nch, cp = gp - xp * nch;
-      bool ready = mbar_test_wait(bars + 8 * (kPfull + (gp & 1)), (gp >> 1) & 1);
-      // a tile's first O MMA overwrites O: the epilogue of the previous tile
-      // must have read it
-      if (ready && cp == 0) ready = mbar_test_wait(bars + 8 * kOfree, (xp & 1) ^ 1);
-      if (ready) {
-        pv(gp);
-        ++gp;
-        progress = true;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (pn[h] < qn[h]) {
+        const int call = pn[h], x = call / nch;
+        bool ready = mbar_test_wait(bars + 8 * (kPfull + h), call & 1);
+        // a tile's first O MMA overwrites O: the half's epilogue of the
+        // previous tile must have read it
+        if (ready && call - x * nch == 0) ready = mbar_test_wait(bars + 8 * (kOfree + h), (x & 1) ^ 1);
+        if (ready) {
+          pv(h, call);
+          ++pn[h];
+          progress = true;
+        }
       }
     }
-    if (gq < total && gq < gp + 2) {
-      const int xq = gq / nch, cq = gq - xq * nch;
-      bool ready = mbar_test_wait(bars + 8 * (kCfull + (gq & 1)), (gq >> 1) & 1) &&
-                   mbar_test_wait(bars + 8 * (kPVdone + (gq & 1)), ((gq >> 1) & 1) ^ 1);
-      if (ready && cq == 0) ready = mbar_test_wait(bars + 8 * (kQfull + (xq & 1)), (xq >> 1) & 1);
-      if (ready) {
-        qk(gq);
-        ++gq;
-        progress = true;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (qn[h] < total && qn[h] == pn[h]) {
+        const int call = qn[h], x = call / nch;
+        bool ready = mbar_test_wait(bars + 8 * (kCfull + (call & 1)), (call >> 1) & 1) &&
+                     mbar_test_wait(bars + 8 * (kPVdone + h), (call & 1) ^ 1);
+        if (ready && call - x * nch == 0) ready = mbar_test_wait(bars + 8 * kQfull, x & 1);
+        if (ready) {
+          qk(h, call);
+          ++qn[h];
+          progress = true;
+        }
       }
     }
     if (progress) {
@@ -348,18 +360,21 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
                              volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int h = (warp - kFirstSoftmaxWarp) >> 2;  // the half of the tile (rows h*128 ..)
   const int quad = warp & 3;
-  const int r = quad * 32 + lane;
+  const int wi = h * 4 + quad;  // this warp among the eight softmax warps
+  const int r = h * kBM + quad * 32 + lane;
   const int t = r >> P.log2g;
   const int j = r & (P.g - 1);
-  const int tpw = 32 >> P.log2g;  // tokens of this warp's rows: quad*tpw .. +tpw-1
+  const int tpw = 32 >> P.log2g;                   // tokens of this warp's rows:
+  const int tw0 = (h * kBM + quad * 32) >> P.log2g;  // tw0 .. tw0 + tpw - 1
   const uint32_t lanes = uint32_t(quad * 32) << 16;
-  const uint32_t o_taddr = tmem_base + lanes + 2 * kKC;
+  const uint32_t o_taddr = tmem_base + lanes + uint32_t(2 * kKC + h * D);
   const int32_t* qtok = reinterpret_cast<const int32_t*>(smem + P.off_qtok);
   const int32_t* csig = reinterpret_cast<const int32_t*>(smem + P.off_csig);
-  uint32_t* wall = reinterpret_cast<uint32_t*>(smem + P.off_bits) + quad * (32 * kSub);
+  uint32_t* wall = reinterpret_cast<uint32_t*>(smem + P.off_bits) + wi * (2 * 32 * kSub);
   // this warp's tokens (sigma of its rows' positions) for the causal masks
-  int32_t* wsig = reinterpret_cast<int32_t*>(smem + P.off_bits + 2 * 4 * 32 * kSub * 4) + quad * 32;
+  int32_t* wsig = reinterpret_cast<int32_t*>(smem + P.off_bits + 8 * 2 * 32 * kSub * 4) + wi * 32;
   auto wwait = [&](uint32_t bar, uint32_t par) {
     const bool ok = bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
     return __all_sync(0xffffffffu, ok);
@@ -372,15 +387,15 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
   bool alive = true;
   for (int x = 0; x < ntiles && alive; ++x) {
     const Tile tl = tile_of(P, begin + x);
-    if (!wwait(bars + 8 * (kQfull + (x & 1)), uint32_t(x >> 1) & 1u)) break;
+    if (!wwait(bars + 8 * kQfull, uint32_t(x) & 1u)) break;
     // Tokens of this warp's rows, kept in registers: the Q stage (and its
-    // token list) is refilled as soon as the tile's last S MMA is done.
+    // token list) is refilled as soon as the tile's last S MMAs are done.
     int wtok = 0;
     if (lane < tpw) {
-      const int tt = quad * tpw + lane;
-      wtok = P.perm ? qtok[(x & 1) * kBM + tt] : min(tl.p0 + tt, P.n - 1);
+      const int tt = tw0 + lane;
+      wtok = P.perm ? qtok[tt] : min(tl.p0 + tt, P.n - 1);
     }
-    const int sig_p = __shfl_sync(0xffffffffu, wtok, t - quad * tpw);
+    const int sig_p = __shfl_sync(0xffffffffu, wtok, t - tw0);
     __syncwarp();  // the previous tile's reads of wsig are done
     if (lane < tpw) wsig[lane] = wtok;
     __syncwarp();
@@ -393,18 +408,17 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     float l = 0.f;
     for (int c = 0; c < nch; ++c) {
       const int call = x * nch + c;
-      const int b = call & 1;
-      const uint32_t ph = uint32_t(call >> 1) & 1u;
-      if (!wwait(bars + 8 * (kCfull + b), ph)) {  // the chunk's key tokens
+      const int b = call & 1;  // chunk stage
+      if (!wwait(bars + 8 * (kCfull + b), uint32_t(call >> 1) & 1u)) {  // the chunk's key tokens
         alive = false;
         break;
       }
       // Mask words of the chunk for this warp's tokens: bit e of word
       // (token, q) set iff key column c*128 + 32q + e is attended.
-      uint32_t* wb = wall + b * (4 * 32 * kSub);
+      uint32_t* wb = wall + b * (32 * kSub);
       for (int w = lane; w < tpw * kSub; w += 32) {
         const int ti = w / kSub, q = w - ti * kSub;
-        const int tt = quad * tpw + ti;
+        const int tt = tw0 + ti;
         const int lo = max(tt, P.left - tl.p0) - c * kKC - 32 * q;
         const int hi = (tl.p0 + tt < P.n ? min(tt + P.left + P.right, P.n - 1 - tl.p0 + P.left)
                                          : -1 - kKC * nch) -
@@ -427,13 +441,13 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
         wb[ti * kSub + q] = word;
       }
       __syncwarp();
-      const uint32_t* wrow = wb + (t - quad * tpw) * kSub;
-      if (!wwait(bars + 8 * (kSfull + b), ph)) {
+      const uint32_t* wrow = wb + (t - tw0) * kSub;
+      if (!wwait(bars + 8 * (kSfull + h), uint32_t(call) & 1u)) {
         alive = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sb = tmem_base + lanes + uint32_t(b * kKC);
+      const uint32_t sb = tmem_base + lanes + uint32_t(h * kKC);
       // pass 1: the chunk's attended maximum
       float mx = -INFINITY;
 #pragma unroll 1
@@ -469,8 +483,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O must hold the O MMAs of every earlier chunk of the tile.
-        if (c > 0 && !wwait(bars + 8 * (kPVdone + ((call - 1) & 1)),
-                            uint32_t((call - 1) >> 1) & 1u)) {
+        if (c > 0 && !wwait(bars + 8 * (kPVdone + h), uint32_t(call - 1) & 1u)) {
           alive = false;
           break;
         }
@@ -517,12 +530,12 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kPfull + b));
+      if (lane == 0) mbar_arrive(bars + 8 * (kPfull + h));
     }
     if (!alive) break;
 
     // epilogue: O / l (x sigmoid(gate)), scattered to row sigma[p0 + t]
-    if (!wwait(bars + 8 * kOfull, uint32_t(x & 1))) break;
+    if (!wwait(bars + 8 * (kOfull + h), uint32_t(x & 1))) break;
     tc_fence_after();
     float mul = l > 0.f ? 1.f / l : 0.f;
     const size_t orow =
@@ -536,7 +549,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bars + 8 * kOfree);
+    if (lane == 0) mbar_arrive(bars + 8 * (kOfree + h));
     const uint64_t mul2 = f2_pack(mul, mul);
     if (row_valid) {
       __nv_bfloat16* op = P.out + orow * D;
@@ -591,17 +604,17 @@ __global__ void __launch_bounds__(kThreads, 1) sa_flash_kernel(const __grid_cons
   volatile int* vote = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 8);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
+    mbar_init(bars + 8 * kQfull, kProducers);
+    mbar_init(bars + 8 * kQfree, 2);  // one commit per half
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bars + 8 * (kQfull + s), kProducers);
-      mbar_init(bars + 8 * (kQfree + s), 1);
       mbar_init(bars + 8 * (kCfull + s), kProducers);
-      mbar_init(bars + 8 * (kCfree + s), 1);
+      mbar_init(bars + 8 * (kCfree + s), 2);  // one commit per half
       mbar_init(bars + 8 * (kSfull + s), 1);
       mbar_init(bars + 8 * (kPfull + s), 4);
       mbar_init(bars + 8 * (kPVdone + s), 1);
+      mbar_init(bars + 8 * (kOfull + s), 1);
+      mbar_init(bars + 8 * (kOfree + s), 4);
     }
-    mbar_init(bars + 8 * kOfull, 1);
-    mbar_init(bars + 8 * kOfree, 4);
     mbar_init(bars + 8 * kDrain, 1);
     *abort_flag = 0;
     *vote = 1;
@@ -659,7 +672,7 @@ static uint32_t round_up(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
 static bool make_config(const Problem& pb, Path path, Config& c) {
   if (pb.d != 64 && pb.d != 128) return false;
   if (pb.g < 1 || pb.g > 32 || kBM % pb.g != 0) return false;
-  c.Bt = kBM / pb.g;
+  c.Bt = kRows / pb.g;  // tokens of a (256-row) tile
   c.log2g = 0;
   while ((1 << c.log2g) < pb.g) ++c.log2g;
   if (path == kPathSA) {
@@ -672,14 +685,15 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
   const long long nch = (span + kKC - 1) / kKC;
   if (nch > (1 << 20)) return false;
   c.nchunks = int(nch);
-  c.q_bytes = kBM * pb.d * 2;
+  c.q_bytes = kBM * pb.d * 2;  // one half of the Q tile
   c.kv_bytes = kKC * pb.d * 2;
   c.off_k = 2 * c.q_bytes;
   c.off_v = c.off_k + 2 * c.kv_bytes;
   c.off_csig = c.off_v + 2 * c.kv_bytes;
   c.off_qtok = c.off_csig + 2u * kKC * 4;
-  c.off_bits = c.off_qtok + 2u * kBM * 4;
-  c.off_bar = round_up(c.off_bits + 2u * 4 * 32 * kSub * 4 + 4 * 32 * 4, 64);
+  c.off_bits = c.off_qtok + uint32_t(kRows) * 4;
+  // mask words (8 warps x 2 stages x 32 tokens x 4) and the warps' tokens
+  c.off_bar = round_up(c.off_bits + 8u * 2 * 32 * kSub * 4 + 8 * 32 * 4, 64);
   c.smem_bytes = c.off_bar + 8 * kNumBars + 16 + 1024;  // + slot, flags, alignment slack
   return c.smem_bytes <= kMaxSmem;
 }
@@ -758,7 +772,7 @@ sa_status_t launch_flash(const Problem& pb, Path path, const float* gate, int ac
   P.off_qtok = c.off_qtok;
   P.off_bits = c.off_bits;
   P.off_bar = c.off_bar;
-  P.tmem_alloc = 512;  // two S buffers of 128 columns, then O
+  P.tmem_alloc = 512;  // S of the two halves (128 columns each), then their O
   P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock
   const int grid = P.num_tiles < sms ? P.num_tiles : sms;
   const cudaError_t ce = (pb.d == 128) ? launch_one<128>(grid, c.smem_bytes, stream, P)
