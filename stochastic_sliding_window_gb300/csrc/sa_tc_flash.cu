@@ -63,6 +63,7 @@ struct Params {
   int32_t* err;
   int B, n, Hq, Hkv, g, log2g, Bt;
   int left, right, nchunks;
+  int qstages;  // Q tile stages: 2 when shared memory allows (d = 64), else 1
   int causal, accumulate;
   float scale_log2;
   int tiles_per_seq, num_tiles;
@@ -76,17 +77,17 @@ struct Params {
 // the CTA-local chunk number c_all & 1 (c_all = x * nchunks + chunk); [2]
 // half families by the half (softmax warpgroup) h.
 enum : uint32_t {
-  kQfull = 0,    // Q rows and tokens of tile x landed (cp.async)
-  kQfree = 1,    // both halves' last S MMA of tile x done: the Q stage is free
-  kCfull = 2,    // [2] K, V rows and key tokens of chunk c_all landed
-  kCfree = 4,    // [2] both halves' O MMA of chunk c_all done: its stage is free
-  kSfull = 6,    // [h] S of the half's current chunk in its TMEM buffer
-  kPfull = 8,    // [h] P of the half's current chunk written (4 softmax warps)
-  kPVdone = 10,  // [h] the half's O MMA of its current chunk done
-  kOfull = 12,   // [h] the half's last O MMA of tile x done
-  kOfree = 14,   // [h] the half's epilogue has read O of tile x (4 warps)
-  kDrain = 16,
-  kNumBars = 17,
+  kQfull = 0,    // [stage] Q rows and tokens of tile x landed (cp.async)
+  kQfree = 2,    // [stage] both halves' last S MMA of tile x done: the stage is free
+  kCfull = 4,    // [2] K, V rows and key tokens of chunk c_all landed
+  kCfree = 6,    // [2] both halves' O MMA of chunk c_all done: its stage is free
+  kSfull = 8,    // [h] S of the half's current chunk in its TMEM buffer
+  kPfull = 10,   // [h] P of the half's current chunk written (4 softmax warps)
+  kPVdone = 12,  // [h] the half's O MMA of its current chunk done
+  kOfull = 14,   // [h] the half's last O MMA of tile x done
+  kOfree = 16,   // [h] the half's epilogue has read O of tile x (4 warps)
+  kDrain = 18,
+  kNumBars = 19,
 };
 
 struct Tile {
@@ -191,10 +192,14 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
   if (ntiles > 0) fetch_chunk(0);
   for (int x = 0; x < ntiles; ++x) {
     const Tile t = tile_of(P, begin + x);
-    // The Q stage is free once both halves' last S MMA of tile x - 1 is done.
+    const int qs = x % P.qstages;
+    // The Q stage is free once both halves' last S MMA of its previous tile
+    // (x - qstages) is done.
     bool ok = true;
-    if (tid == 0 && x >= 1) ok = wait(bars + 8 * kQfree, uint32_t(x - 1) & 1u);
+    if (tid == 0 && x >= P.qstages)
+      ok = wait(bars + 8 * (kQfree + qs), uint32_t(x / P.qstages - 1) & 1u);
     if (!agree(ok)) break;
+    const uint32_t qstage = sbase + uint32_t(qs) * 2 * P.q_bytes;
     {
       // 256 rows (r = t*g + j) in two halves of [128 rows x D], each two
       // K-blocks of [128 rows x 128 B], swizzled.
@@ -211,7 +216,7 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
         for (int k = 0; k < kBatch; ++k) {
           const int r = r0 + RPP * k;
           if (r < kRows)
-            cp_async16(sbase + uint32_t(r >> 7) * P.q_bytes + kb * (kBM * 128) + (r & 127) * 128 +
+            cp_async16(qstage + uint32_t(r >> 7) * P.q_bytes + kb * (kBM * 128) + (r & 127) * 128 +
                            ((c8 ^ (r & 7)) << 4),
                        qbase + tq[k] * tokstride + (r & (P.g - 1)) * D);
         }
@@ -219,10 +224,10 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
       if (P.perm) {  // the tile's tokens, for the softmax warps
         for (int i = tid; i < P.Bt; i += kProducers) {
           const int qc = min(t.p0 + i, P.n - 1);
-          cp_async4(sbase + P.off_qtok + uint32_t(i) * 4, P.perm + size_t(t.b) * P.n + qc);
+          cp_async4(sbase + P.off_qtok + uint32_t(qs * kRows + i) * 4, P.perm + size_t(t.b) * P.n + qc);
         }
       }
-      cp_async_arrive_noinc(bars + 8 * kQfull);
+      cp_async_arrive_noinc(bars + 8 * (kQfull + qs));
     }
     for (int c = 0; c < nch; ++c) {
       const int call = x * nch + c;
@@ -271,11 +276,12 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
   // S of half h in TMEM columns [h*128, h*128 + 128); O of half h at 256 + h*D.
   auto qk = [&](int h, int call) {
-    const int c = call % nch;
+    const int x = call / nch, c = call - x * nch;
+    const int qs = x % P.qstages;
     fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
     tc_fence_after();
     const uint32_t d = tmem_base + uint32_t(h * kKC);
-    const uint64_t a0 = sdesc_sw128(sbase + uint32_t(h) * P.q_bytes, 16, 1024);
+    const uint64_t a0 = sdesc_sw128(sbase + uint32_t(qs * 2 + h) * P.q_bytes, 16, 1024);
     const uint64_t b0 = sdesc_sw128(sbase + P.off_k + uint32_t(call & 1) * P.kv_bytes, 16, 1024);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
@@ -284,7 +290,7 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
       umma_bf16(d, a0 + da, b0 + db, idesc_qk, kk > 0 ? 1u : 0u);
     }
     umma_commit(bars + 8 * (kSfull + h));
-    if (c == nch - 1) umma_commit(bars + 8 * kQfree);
+    if (c == nch - 1) umma_commit(bars + 8 * (kQfree + qs));
   };
   auto pv = [&](int h, int call) {
     const int c = call % nch;
@@ -328,7 +334,8 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
         const int call = qn[h], x = call / nch;
         bool ready = mbar_test_wait(bars + 8 * (kCfull + (call & 1)), (call >> 1) & 1) &&
                      mbar_test_wait(bars + 8 * (kPVdone + h), (call & 1) ^ 1);
-        if (ready && call - x * nch == 0) ready = mbar_test_wait(bars + 8 * kQfull, x & 1);
+        if (ready && call - x * nch == 0)
+          ready = mbar_test_wait(bars + 8 * (kQfull + x % P.qstages), (x / P.qstages) & 1);
         if (ready) {
           qk(h, call);
           ++qn[h];
@@ -387,13 +394,14 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
   bool alive = true;
   for (int x = 0; x < ntiles && alive; ++x) {
     const Tile tl = tile_of(P, begin + x);
-    if (!wwait(bars + 8 * kQfull, uint32_t(x) & 1u)) break;
+    const int qs = x % P.qstages;
+    if (!wwait(bars + 8 * (kQfull + qs), uint32_t(x / P.qstages) & 1u)) break;
     // Tokens of this warp's rows, kept in registers: the Q stage (and its
     // token list) is refilled as soon as the tile's last S MMAs are done.
     int wtok = 0;
     if (lane < tpw) {
       const int tt = tw0 + lane;
-      wtok = P.perm ? qtok[tt] : min(tl.p0 + tt, P.n - 1);
+      wtok = P.perm ? qtok[qs * kRows + tt] : min(tl.p0 + tt, P.n - 1);
     }
     const int sig_p = __shfl_sync(0xffffffffu, wtok, t - tw0);
     __syncwarp();  // the previous tile's reads of wsig are done
@@ -604,9 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1) sa_flash_kernel(const __grid_cons
   volatile int* vote = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 8);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    mbar_init(bars + 8 * kQfull, kProducers);
-    mbar_init(bars + 8 * kQfree, 2);  // one commit per half
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bars + 8 * (kQfull + s), kProducers);
+      mbar_init(bars + 8 * (kQfree + s), 2);  // one commit per half
       mbar_init(bars + 8 * (kCfull + s), kProducers);
       mbar_init(bars + 8 * (kCfree + s), 2);  // one commit per half
       mbar_init(bars + 8 * (kSfull + s), 1);
@@ -663,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_flash_kernel(const __grid_cons
 
 // ------------------------------------------------------------------ host
 struct Config {
-  int Bt, log2g, left, right, nchunks;
+  int Bt, log2g, left, right, nchunks, qstages;
   uint32_t q_bytes, kv_bytes, off_k, off_v, off_csig, off_qtok, off_bits, off_bar, smem_bytes;
 };
 
@@ -687,15 +695,18 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
   c.nchunks = int(nch);
   c.q_bytes = kBM * pb.d * 2;  // one half of the Q tile
   c.kv_bytes = kKC * pb.d * 2;
-  c.off_k = 2 * c.q_bytes;
-  c.off_v = c.off_k + 2 * c.kv_bytes;
-  c.off_csig = c.off_v + 2 * c.kv_bytes;
-  c.off_qtok = c.off_csig + 2u * kKC * 4;
-  c.off_bits = c.off_qtok + uint32_t(kRows) * 4;
-  // mask words (8 warps x 2 stages x 32 tokens x 4) and the warps' tokens
-  c.off_bar = round_up(c.off_bits + 8u * 2 * 32 * kSub * 4 + 8 * 32 * 4, 64);
-  c.smem_bytes = c.off_bar + 8 * kNumBars + 16 + 1024;  // + slot, flags, alignment slack
-  return c.smem_bytes <= kMaxSmem;
+  for (c.qstages = 2; c.qstages >= 1; --c.qstages) {  // two Q stages when they fit
+    c.off_k = uint32_t(c.qstages) * 2 * c.q_bytes;
+    c.off_v = c.off_k + 2 * c.kv_bytes;
+    c.off_csig = c.off_v + 2 * c.kv_bytes;
+    c.off_qtok = c.off_csig + 2u * kKC * 4;
+    c.off_bits = c.off_qtok + uint32_t(c.qstages * kRows) * 4;
+    // mask words (8 warps x 2 stages x 32 tokens x 4) and the warps' tokens
+    c.off_bar = round_up(c.off_bits + 8u * 2 * 32 * kSub * 4 + 8 * 32 * 4, 64);
+    c.smem_bytes = c.off_bar + 8 * kNumBars + 16 + 1024;  // + slot, flags, alignment slack
+    if (c.smem_bytes <= kMaxSmem) return true;
+  }
+  return false;
 }
 
 static bool device_sm103(int* sms) {
@@ -759,6 +770,7 @@ sa_status_t launch_flash(const Problem& pb, Path path, const float* gate, int ac
   P.left = c.left;
   P.right = c.right;
   P.nchunks = c.nchunks;
+  P.qstages = c.qstages;
   P.causal = (path == kPathSA) ? pb.causal : 0;
   P.accumulate = accumulate;
   P.scale_log2 = pb.scale * 1.4426950408889634f;
