@@ -184,3 +184,38 @@ def test_length_sweep_causal_sa(n):
         assert sa.check_error(err) == sa.SA_OK
         compare(gather_rows(y, rows), oracle.sa_rows(inp.case.q, inp.case.k, inp.case.v, perm, 128,
                                                      True, rows=rows), f"c5 n={n} layer={layer}")
+
+
+# ------------------------------------------------------------ online-softmax corrections
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_flash_kernel_rescales_when_scores_grow_across_chunks(causal):
+    """With sigma = identity and key scores rising along the sequence (by 256
+    per 128 keys, i.e. ~33 in the kernel's base-2 units), every later 128-key
+    chunk's maximum exceeds the running reference by far more than 2^8, so the
+    chunked kernel must rescale O and the row sum again and again; the result
+    must still be the exact softmax (fp64 oracle)."""
+    b, n, hq, hkv, d, w = 1, 1536, 8, 2, 128, 1024
+    rng = np.random.default_rng(7)
+    q = np.zeros((b, n, hq, d), np.float32)
+    q[..., 0] = 16.0
+    k = np.zeros((b, n, hkv, d), np.float32)
+    k[0, :, :, 0] = (np.arange(n, dtype=np.float32) % 512)[:, None] * 0.125
+    k[..., 1:] = rng.standard_normal((b, n, hkv, d - 1)).astype(np.float32) * 0.05
+    v = rng.standard_normal((b, n, hkv, d)).astype(np.float32)
+    from sa_synth import round_bf16
+    q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)  # both sides see these values
+    ident = np.arange(n, dtype=np.int64)[None]
+    perm_d = torch.from_numpy(ident.astype(np.int32)).cuda()
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+    err = _err()
+    y = sa.sa_forward(dev(q), dev(k), dev(v), perm_d, w, causal=causal,
+                      kernel=sa.KERNEL_TCGEN05_FLASH, err=err)
+    assert sa.check_error(err) == sa.SA_OK
+    rows = sample_rows(b, n, 200, seed=5)
+    want = oracle.sa_rows(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64),
+                          ident, w, causal, rows=rows)
+    compare(gather_rows(y, rows), want, f"flash rescale causal={causal}")
+    ys = sa.sa_forward(dev(q), dev(k), dev(v), perm_d, w, causal=causal, kernel=sa.KERNEL_SIMT,
+                       err=err)
+    assert (y.float() - ys.float()).abs().max().item() <= 2e-2
