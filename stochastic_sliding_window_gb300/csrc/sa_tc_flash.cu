@@ -275,14 +275,23 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   const uint32_t idesc_qk = idesc_bf16(kBM, kKC, 0);
   const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
   // S of half h in TMEM columns [h*128, h*128 + 128); O of half h at 256 + h*D.
-  auto qk = [&](int h, int call) {
-    const int x = call / nch, c = call - x * nch;
-    const int qs = x % P.qstages;
+  // Shared-memory descriptors of every stage, built once (kept in registers:
+  // chosen by selects, not indexed).
+  const uint64_t q00 = sdesc_sw128(sbase, 16, 1024);
+  const uint64_t q01 = sdesc_sw128(sbase + P.q_bytes, 16, 1024);
+  const uint64_t q10 = sdesc_sw128(sbase + 2 * P.q_bytes, 16, 1024);
+  const uint64_t q11 = sdesc_sw128(sbase + 3 * P.q_bytes, 16, 1024);
+  const uint64_t k0 = sdesc_sw128(sbase + P.off_k, 16, 1024);
+  const uint64_t k1 = sdesc_sw128(sbase + P.off_k + P.kv_bytes, 16, 1024);
+  const uint64_t v0 = sdesc_sw128(sbase + P.off_v, kKC * 128, 1024);
+  const uint64_t v1 = sdesc_sw128(sbase + P.off_v + P.kv_bytes, kKC * 128, 1024);
+  // c: the chunk within its tile; qs: the tile's Q stage.
+  auto qk = [&](int h, int call, int c, int qs) {
     fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
     tc_fence_after();
     const uint32_t d = tmem_base + uint32_t(h * kKC);
-    const uint64_t a0 = sdesc_sw128(sbase + uint32_t(qs * 2 + h) * P.q_bytes, 16, 1024);
-    const uint64_t b0 = sdesc_sw128(sbase + P.off_k + uint32_t(call & 1) * P.kv_bytes, 16, 1024);
+    const uint64_t a0 = qs == 0 ? (h == 0 ? q00 : q01) : (h == 0 ? q10 : q11);
+    const uint64_t b0 = (call & 1) ? k1 : k0;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint64_t da = uint64_t((kk >> 2) * (kBM * 128 / 16) + (kk & 3) * 2);
@@ -292,12 +301,11 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
     umma_commit(bars + 8 * (kSfull + h));
     if (c == nch - 1) umma_commit(bars + 8 * (kQfree + qs));
   };
-  auto pv = [&](int h, int call) {
-    const int c = call % nch;
+  auto pv = [&](int h, int call, int c) {
     tc_fence_after();
     const uint32_t sbuf = tmem_base + uint32_t(h * kKC);
     const uint32_t o = tmem_base + uint32_t(2 * kKC + h * D);
-    uint64_t bd = sdesc_sw128(sbase + P.off_v + uint32_t(call & 1) * P.kv_bytes, kKC * 128, 1024);
+    uint64_t bd = (call & 1) ? v1 : v0;
 #pragma unroll
     for (int kk = 0; kk < kKC / 16; ++kk) {
       umma_bf16_ts(o, sbuf + 8 * kk, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
@@ -309,21 +317,31 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   };
   // Per half: QK(qn) after the half's previous O MMA has read its P (one S
   // buffer per half), PV(pn) once P is written; PV first when both are ready.
+  // Tile, chunk and Q stage of each half's next QK and PV are kept as
+  // counters: this single thread's loop stays free of divisions, which would
+  // delay every reaction to a barrier.
   int qn[2] = {0, 0}, pn[2] = {0, 0};
+  int pc[2] = {0, 0}, px[2] = {0, 0};                // PV: chunk, tile
+  int qc[2] = {0, 0};                                // QK: chunk
+  int qst[2] = {0, 0}, qph[2] = {0, 0};              // QK: Q stage and its parity
   long long last = clock64();
   while (pn[0] < total || pn[1] < total) {
     bool progress = false;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (pn[h] < qn[h]) {
-        const int call = pn[h], x = call / nch;
+        const int call = pn[h];
         bool ready = mbar_test_wait(bars + 8 * (kPfull + h), call & 1);
         // a tile's first O MMA overwrites O: the half's epilogue of the
         // previous tile must have read it
-        if (ready && call - x * nch == 0) ready = mbar_test_wait(bars + 8 * (kOfree + h), (x & 1) ^ 1);
+        if (ready && pc[h] == 0) ready = mbar_test_wait(bars + 8 * (kOfree + h), (px[h] & 1) ^ 1);
         if (ready) {
-          pv(h, call);
+          pv(h, call, pc[h]);
           ++pn[h];
+          if (++pc[h] == nch) {
+            pc[h] = 0;
+            ++px[h];
+          }
           progress = true;
         }
       }
@@ -331,14 +349,20 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (qn[h] < total && qn[h] == pn[h]) {
-        const int call = qn[h], x = call / nch;
+        const int call = qn[h];
         bool ready = mbar_test_wait(bars + 8 * (kCfull + (call & 1)), (call >> 1) & 1) &&
                      mbar_test_wait(bars + 8 * (kPVdone + h), (call & 1) ^ 1);
-        if (ready && call - x * nch == 0)
-          ready = mbar_test_wait(bars + 8 * (kQfull + x % P.qstages), (x / P.qstages) & 1);
+        if (ready && qc[h] == 0) ready = mbar_test_wait(bars + 8 * (kQfull + qst[h]), qph[h]);
         if (ready) {
-          qk(h, call);
+          qk(h, call, qc[h], qst[h]);
           ++qn[h];
+          if (++qc[h] == nch) {
+            qc[h] = 0;
+            if (++qst[h] == P.qstages) {
+              qst[h] = 0;
+              qph[h] ^= 1;
+            }
+          }
           progress = true;
         }
       }
