@@ -104,9 +104,10 @@ def test_inverse_perm():
 
 # ---------------------------------------------------------------- neighbour sets
 
-def test_hand_worked_neighbour_sets():
+@pytest.mark.parametrize("golden", ["sa_hand_n6.txt", "sa_hand_n6_w5.txt"])
+def test_hand_worked_neighbour_sets(golden):
     rec = {}
-    for line in _golden_lines("sa_hand_n6.txt"):
+    for line in _golden_lines(golden):
         key, rest = line.split(None, 1)
         rec[key] = rest
     sigma = np.array([int(x) for x in rec["sigma"].split()])
@@ -181,6 +182,23 @@ def test_receptive_field_swa_is_linear():
     sizes = graph.receptive_field_sizes([graph.adjacency_swa(n, w)] * layers)
     for l in range(1, layers + 1):
         assert sizes[l - 1].tolist() == [min(i + 1, l * (w - 1) + 1) for i in range(n)]
+
+
+def test_receptive_field_matches_set_unions_over_layers():
+    """R_l(i) by explicit set unions over each layer's neighbour sets, layer 1
+    first ("Theoretical properties", receptive-field bullet), on tiny inputs
+    with a different sigma per layer so that the layer order matters."""
+    n, w = 9, 2
+    sigmas = [prng.make_perm(11, l, 0, n) for l in range(3)]
+    for causal in (False, True):
+        reach = [{i} for i in range(n)]
+        want = []
+        for sigma in sigmas:
+            nb = [set(graph.neighbours_sa(sigma, w, causal, i).tolist()) for i in range(n)]
+            reach = [set().union(*(reach[j] for j in nb[i])) for i in range(n)]
+            want.append([len(r) for r in reach])
+        adj = [graph.adjacency_sa(s, w, causal) for s in sigmas]
+        assert graph.receptive_field_sizes(adj).tolist() == want
 
 
 def test_receptive_field_sa_grows_far_faster_than_swa():
@@ -320,6 +338,18 @@ def test_gate_limits_reduce_to_single_paths():
     got = attention.gated_forward(c.q, c.k, c.v, perm, zero, zero, w)
     np.testing.assert_allclose(got, 0.5 * (y_sa + y_swa), atol=1e-15)
     assert attention.sigmoid(np.array([-1000.0]))[0] == 0.0
+
+
+def test_gated_swa_window_is_its_own():
+    """With window_swa set, the SWA branch of the gated sum uses it, not w."""
+    c = _case(n=20)
+    perm = np.stack([prng.make_perm(0, 1, b, 20) for b in range(2)])
+    big = np.full(c.gate_sa.shape, 40.0)
+    got = attention.gated_forward(c.q, c.k, c.v, perm, -big, big, 8, 3)
+    np.testing.assert_allclose(got, attention.swa_forward(c.q, c.k, c.v, 3), atol=1e-15)
+    assert np.abs(got - attention.swa_forward(c.q, c.k, c.v, 8)).max() > 1e-3
+    got = attention.gated_forward(c.q, c.k, c.v, perm, big, -big, 8, 3)
+    np.testing.assert_allclose(got, attention.sa_forward(c.q, c.k, c.v, perm, 8, True), atol=1e-15)
 
 
 def test_gqa_head_map_and_scale_pinned_by_sdpa():
