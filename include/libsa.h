@@ -57,7 +57,7 @@ extern "C" {
 typedef enum sa_status {
   SA_OK = 0,
   SA_ERR_INVALID_ARG = 1, /* NULL pointer, size <= 0, Hq % Hkv != 0, ... */
-  SA_ERR_UNSUPPORTED = 2, /* valid request this build cannot run (head_dim, alignment, kernel) */
+  SA_ERR_UNSUPPORTED = 2, /* valid request this library cannot run (head_dim, alignment, kernel) */
   SA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
   SA_ERR_BAD_PERM = 4,    /* device check found perm entries out of range or repeated */
   SA_ERR_TIMEOUT = 5,     /* a device pipeline wait ran past its bound; results are invalid */

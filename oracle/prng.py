@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY -- see the package docstring.
 
 The pages say only that each layer draws sigma ~ Uniform(S_n) independently
 ("Stochastic Attention" summary, section "Core mechanism", step 1).  They fix
-no generator, so this build fixes one that both the oracle and the library
+no generator, so one is fixed here that both the oracle and the library
 implement separately from its published definition:
 
 * splitmix64 (S. Vigna's public-domain generator): state += 0x9E3779B97F4A7C15,

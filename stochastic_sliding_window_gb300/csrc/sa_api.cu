@@ -261,7 +261,7 @@ extern "C" const char* sa_status_string(sa_status_t status) {
   switch (status) {
     case SA_OK: return "SA_OK";
     case SA_ERR_INVALID_ARG: return "SA_ERR_INVALID_ARG: invalid argument";
-    case SA_ERR_UNSUPPORTED: return "SA_ERR_UNSUPPORTED: not supported by this build";
+    case SA_ERR_UNSUPPORTED: return "SA_ERR_UNSUPPORTED: not supported by this library";
     case SA_ERR_CUDA: return "SA_ERR_CUDA: CUDA runtime error";
     case SA_ERR_BAD_PERM: return "SA_ERR_BAD_PERM: perm is not a permutation";
     case SA_ERR_TIMEOUT: return "SA_ERR_TIMEOUT: device wait ran past its bound";
