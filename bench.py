@@ -9,7 +9,9 @@ windowed attention, sigma^-1 scatter) through the libsa C ABI.
 Prints ONE JSON line (rank 0).  ``value`` is device-timed tokens/s with
 inputs resident in HBM (L2 flushed between steps); ``e2e`` times the same
 call with the host->device copies of Q/K/V/sigma from pinned memory and the
-device->host copy of the output inside the timed region.  ``roofline``
+device->host copy of the output inside the timed region, two streams taking
+alternate steps so that one step's output copy overlaps the next step's
+input copy.  ``roofline``
 compares the kernel's algorithmic bytes per launch (Q, K, V and Y once,
 sigma once) over its CUDA-event duration with the measured HBM copy peak.
 
@@ -349,13 +351,13 @@ def run_ours(args, wl=WORKLOAD):
     kern = {"auto": sa.KERNEL_AUTO, "simt": sa.KERNEL_SIMT, "gather": sa.KERNEL_TCGEN05_GATHER,
             "ring": sa.KERNEL_TCGEN05_RING, "flash": sa.KERNEL_TCGEN05_FLASH}[args.kernel]
 
-    def forward(q_, k_, v_, p_, ga_, gw_, o_):
+    def forward(q_, k_, v_, p_, ga_, gw_, o_, st=stream):
         if gated:
             sa.sa_swa_gated_forward(q_, k_, v_, p_, ga_, gw_, wl["window"], causal=wl["causal"],
-                                    out=o_, err=err, stream=stream, kernel=kern)
+                                    out=o_, err=err, stream=st, kernel=kern)
         else:
             sa.sa_forward(q_, k_, v_, p_, wl["window"], causal=wl["causal"], out=o_, err=err,
-                          stream=stream, kernel=kern)
+                          stream=st, kernel=kern)
 
     def step():
         forward(q, k, v, perm, ga, gw, out)
@@ -397,41 +399,56 @@ def run_ours(args, wl=WORKLOAD):
     if status != sa.SA_OK:
         raise RuntimeError(f"device error word reports status {status}")
 
-    # end to end: pinned host buffers in, result out, copies inside the timing
+    # end to end: pinned host buffers in, result out, copies inside the timing.
+    # Two streams take alternate steps, each with its own device buffers and
+    # host result buffer, so one step's result copy overlaps the next step's
+    # input copy (the host link is full duplex).  Every step still copies all
+    # of its inputs in and its whole result out.
     hq = torch.from_numpy(bf16_bits(case.q).view(np.int16)).view(torch.bfloat16).pin_memory()
     hk = torch.from_numpy(bf16_bits(case.k).view(np.int16)).view(torch.bfloat16).pin_memory()
     hv = torch.from_numpy(bf16_bits(case.v).view(np.int16)).view(torch.bfloat16).pin_memory()
     hp = torch.from_numpy(perm_np).pin_memory()
-    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     hins = [hq, hk, hv, hp]
     if gated:
         hins += [torch.from_numpy(case.gate_sa).pin_memory(),
                  torch.from_numpy(case.gate_swa).pin_memory()]
     h2d = sum(t.numel() * t.element_size() for t in hins)
-    d2h = hout.numel() * hout.element_size()
-    dins = [torch.empty_like(x, device=dev) for x in hins]
-    o2 = torch.empty_like(out)
+    d2h = out.numel() * out.element_size()
+    slots = [dict(stream=torch.cuda.Stream(dev),
+                  dins=[torch.empty_like(x, device=dev) for x in hins],
+                  out=torch.empty_like(out),
+                  hout=torch.empty(out.shape, dtype=torch.bfloat16).pin_memory())
+             for _ in range(2)]
 
-    def e2e_step():
-        for dst, src in zip(dins, hins):
-            dst.copy_(src, non_blocking=True)
-        forward(dins[0], dins[1], dins[2], dins[3], dins[4] if gated else None,
-                dins[5] if gated else None, o2)
-        hout.copy_(o2, non_blocking=True)
+    def e2e_step(i):
+        sl = slots[i & 1]
+        with torch.cuda.stream(sl["stream"]):
+            for dst, src in zip(sl["dins"], hins):
+                dst.copy_(src, non_blocking=True)
+            d = sl["dins"]
+            forward(d[0], d[1], d[2], d[3], d[4] if gated else None, d[5] if gated else None,
+                    sl["out"], st=sl["stream"])
+            sl["hout"].copy_(sl["out"], non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
-    e2e_steps = max(3, min(args.steps, 50 if wl is WORKLOAD else 10))
+    e2e_steps = max(4, min(args.steps, 50 if wl is WORKLOAD else 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    for sl in slots:
+        sl["stream"].wait_stream(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    for sl in slots:
+        stream.wait_stream(sl["stream"])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
-        raise RuntimeError("end-to-end output differs from the device-resident run")
+    ref_out = out.cpu().view(torch.int16)
+    for sl in slots:
+        if not torch.equal(sl["hout"].view(torch.int16), ref_out):
+            raise RuntimeError("end-to-end output differs from the device-resident run")
 
     if rank != 0:
         return 0
