@@ -69,6 +69,38 @@ def test_algorithmic_counts_of_the_headline_workload():
     assert f == 4.0 * d * hq * (n * (1 + h) - h * (h + 1) // 2)
 
 
+@pytest.mark.parametrize("n,w", [(1, 1), (5, 2), (64, 9), (256, 32), (100, 300), (2048, 128),
+                                 (32768, 128)])
+def test_pair_counts_agree_with_the_oracle_closed_forms(n, w):
+    """The bench's pair counts are the oracle's closed forms, which the oracle
+    pins check against brute-force adjacency counts."""
+    from oracle import graph
+    assert bench.causal_sa_pairs(n, w) == graph.attended_pairs_closed_form(n, w, "sa", True)
+    assert bench.swa_pairs(n, w) == graph.attended_pairs_closed_form(n, w, "swa")
+
+
+@pytest.mark.parametrize("name,window,seq_len,mb,gflop", [
+    # algorithmic bytes (MB) and FLOPs (GF) per step, as tabulated for each shape
+    ("pretrain_layer", 0, 0, 68.2, 6.31),
+    ("long_prefill_gqa", 32, 0, 671.2, 9.12),
+    ("long_prefill_gqa", 64, 0, 671.2, 17.71),
+    ("long_prefill_gqa", 256, 0, 671.2, 69.12),
+    ("very_long_context", 0, 0, 2450.0, 3290.0),
+    ("very_long_context", 2048, 0, 2450.0, 6556.0),
+    ("length_sweep", 0, 0, 4300.0, 139.6),
+    ("length_sweep", 0, 2048, 33.6, 1.07),
+])
+def test_algorithmic_counts_of_every_workload(name, window, seq_len, mb, gflop):
+    wl = dict(bench.WORKLOADS[name])
+    if window:
+        wl["window"] = window
+    if seq_len:
+        wl["seq_len"] = seq_len
+    b, f = bench.algorithmic(wl)
+    assert b / 1e6 == pytest.approx(mb, rel=5e-3)
+    assert f / 1e9 == pytest.approx(gflop, rel=5e-3)
+
+
 def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
