@@ -5,6 +5,8 @@ behaviour on ranks other than 0."""
 
 from __future__ import annotations
 
+import json
+
 import os
 import socket
 import sys
@@ -109,3 +111,31 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
         steps, warmup = 1, 3
 
     assert bench.run_reference(Args()) == 0
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """Rank 0 of the reference arm times the oracle and prints one JSON line
+    with the keys the bench contract names (checked on a tiny workload)."""
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(bench.os, "sched_getaffinity", lambda pid: {0, 1})
+    wl = dict(workload="tiny", batch=1, seq_len=256, num_q_heads=2, num_kv_heads=2, head_dim=64,
+              window=32, causal=True, path="sa", seed=0, std=None)
+
+    class Args:
+        steps, warmup = 1, 0
+
+    assert bench.run_reference(Args(), wl) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e", "gpu_launches"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["n_gpus"] == 1 and line["steps"] == 1 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "tiny" and line["vs_baseline"] is None
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] == line["value"]
+    assert cb["unit"] == "tokens/s" and cb["sample"]
+    assert line["e2e"] == dict(value=line["value"], unit="tokens/s", h2d_bytes_per_step=0,
+                               d2h_bytes_per_step=0)
