@@ -71,6 +71,8 @@ MUTANTS = [
      "w_swa = window"),
     ("sigmoid-sign", "attention", "return 1.0 / (1.0 + np.exp(-x))",
      "return 1.0 / (1.0 + np.exp(x))"),
+    ("sigmoid-slope", "attention", "return 1.0 / (1.0 + np.exp(-x))",
+     "return 1.0 / (1.0 + np.exp(-2.0 * x))"),
     ("mask-fills-zero", "attention", "s = np.where(mask, s, -np.inf)",
      "s = np.where(mask, s, 0.0)"),
     ("causal-full-upper", "attention",
@@ -103,6 +105,7 @@ PINS = [
     ("relabelling", pins.test_relabelling_equivariance_noncausal, ()),
     ("gate limits", pins.test_gate_limits_reduce_to_single_paths, ()),
     ("gated SWA window", pins.test_gated_swa_window_is_its_own, ()),
+    ("gated logistic", pins.test_gated_merge_with_arbitrary_logits_uses_the_logistic_function, ()),
     ("GQA and scale", pins.test_gqa_head_map_and_scale_pinned_by_sdpa, ()),
 ]
 

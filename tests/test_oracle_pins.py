@@ -340,6 +340,22 @@ def test_gate_limits_reduce_to_single_paths():
     assert attention.sigmoid(np.array([-1000.0]))[0] == 0.0
 
 
+def test_gated_merge_with_arbitrary_logits_uses_the_logistic_function():
+    """Y = sigmoid(a_sa) Y_sa + sigmoid(a_swa) Y_swa ("Gated SA and SWA"
+    equation) at ordinary logit values, with the logistic function taken from
+    scipy rather than the oracle."""
+    special = pytest.importorskip("scipy.special")
+    c = _case(n=20)
+    perm = np.stack([prng.make_perm(0, 2, b, 20) for b in range(2)])
+    w = 6
+    a_sa = 1.5 * np.asarray(c.gate_sa, dtype=np.float64)
+    a_swa = 1.5 * np.asarray(c.gate_swa, dtype=np.float64)
+    got = attention.gated_forward(c.q, c.k, c.v, perm, a_sa, a_swa, w)
+    want = (special.expit(a_sa)[..., None] * attention.sa_forward(c.q, c.k, c.v, perm, w, True)
+            + special.expit(a_swa)[..., None] * attention.swa_forward(c.q, c.k, c.v, w))
+    np.testing.assert_allclose(got, want, atol=1e-14)
+
+
 def test_gated_swa_window_is_its_own():
     """With window_swa set, the SWA branch of the gated sum uses it, not w."""
     c = _case(n=20)
