@@ -66,6 +66,9 @@ MUTANTS = [
      "p = e / e.sum(axis=0, keepdims=True)"),
     ("gates-swapped", "attention", "return g1 * y_sa + g2 * y_swa",
      "return g2 * y_sa + g1 * y_swa"),
+    ("swa-window-zero-taken-literally", "attention",
+     "w_swa = window if (window_swa is None or window_swa <= 0) else window_swa",
+     "w_swa = window if (window_swa is None or window_swa < 0) else window_swa"),
     ("swa-window-ignored", "attention",
      "w_swa = window if (window_swa is None or window_swa <= 0) else window_swa",
      "w_swa = window"),

@@ -366,6 +366,9 @@ def test_gated_swa_window_is_its_own():
     assert np.abs(got - attention.swa_forward(c.q, c.k, c.v, 8)).max() > 1e-3
     got = attention.gated_forward(c.q, c.k, c.v, perm, big, -big, 8, 3)
     np.testing.assert_allclose(got, attention.sa_forward(c.q, c.k, c.v, perm, 8, True), atol=1e-15)
+    # window_swa <= 0 means "the same window as SA"
+    got = attention.gated_forward(c.q, c.k, c.v, perm, -big, big, 8, 0)
+    np.testing.assert_allclose(got, attention.swa_forward(c.q, c.k, c.v, 8), atol=1e-15)
 
 
 def test_gqa_head_map_and_scale_pinned_by_sdpa():
