@@ -32,6 +32,12 @@ MUTANTS = [
      "state = (state + GOLDEN_GAMMA + 2) & MASK64"),
     ("stream-ignores-layer", "prng", "start = (seed + (layer << 32) + batch_index) & MASK64",
      "start = (seed + batch_index) & MASK64"),
+    ("stream-layer-shift", "prng", "start = (seed + (layer << 32) + batch_index) & MASK64",
+     "start = (seed + (layer << 31) + batch_index) & MASK64"),
+    ("stream-without-mixing-step", "prng", "    _, out = splitmix64_step(start)\n",
+     "    out = start\n"),
+    ("draws-state-not-output", "prng", "        return out\n\n    return fisher_yates(n, draw)",
+     "        return state\n\n    return fisher_yates(n, draw)"),
     ("sattolo-draw", "prng", "j = (x * (i + 1)) >> 64", "j = (x * i) >> 64"),
     ("shuffle-skips-last", "prng", "for i in range(n - 1, 0, -1):",
      "for i in range(n - 2, 0, -1):"),
@@ -89,6 +95,8 @@ PINS = [
     ("Fisher-Yates stub draws", pins.test_fisher_yates_index_mapping_with_stub_draws, ()),
     ("uniform over S4", pins.test_perm_draw_is_uniform_over_s4, ()),
     ("streams differ", pins.test_streams_differ_by_layer_and_batch, ()),
+    ("stream state", pins.test_stream_state_is_one_published_step_from_the_start, ()),
+    ("make_perm wiring", pins.test_make_perm_consumes_successive_stream_outputs, ()),
     ("inverse", pins.test_inverse_perm, ()),
     ("hand sets w=2", pins.test_hand_worked_neighbour_sets, ("sa_hand_n6.txt",)),
     ("hand sets w=5", pins.test_hand_worked_neighbour_sets, ("sa_hand_n6_w5.txt",)),

@@ -50,6 +50,37 @@ def test_splitmix64_published_vectors():
             assert got == want
 
 
+def test_stream_state_is_one_published_step_from_the_start():
+    """The stream of (seed, layer, b) starts from the splitmix64 output for the
+    initial state seed + (layer << 32) + b; seeds are chosen so that this
+    initial state is one whose first output is published."""
+    first = {}
+    for line in _golden_lines("splitmix64.txt"):
+        vals = [int(x) for x in line.split()]
+        first[vals[0]] = vals[1]
+    mask = (1 << 64) - 1
+    assert prng.stream_state(0, 0, 0) == first[0]
+    assert prng.stream_state(1234567, 0, 0) == first[1234567]
+    assert prng.stream_state(1234567 - 5, 0, 5) == first[1234567]
+    assert prng.stream_state((1234567 - (1 << 32)) & mask, 1, 0) == first[1234567]
+    assert prng.stream_state((1234567 - (3 << 32) - 9) & mask, 3, 9) == first[1234567]
+
+
+def test_make_perm_consumes_successive_stream_outputs():
+    """make_perm wires the pinned pieces together: Fisher-Yates (pinned by stub
+    draws) fed with successive splitmix64 outputs (pinned by the published
+    vectors) from the stream state (pinned above)."""
+    for seed, layer, b, n in ((0, 0, 0, 8), (7, 2, 1, 33), (2**63 + 5, 1, 3, 100)):
+        state = prng.stream_state(seed, layer, b)
+        draws = []
+        for _ in range(max(n - 1, 0)):
+            state, out = prng.splitmix64_step(state)
+            draws.append(out)
+        it = iter(draws)
+        assert prng.make_perm(seed, layer, b, n).tolist() == \
+            prng.fisher_yates(n, lambda: next(it)).tolist()
+
+
 def test_fisher_yates_index_mapping_with_stub_draws():
     # x = 0 maps every draw to j = 0; Durstenfeld's loop then rotates the
     # identity left by one: sigma[p] = (p + 1) mod n.
