@@ -185,6 +185,24 @@ def test_expected_degree_closed_form():
         assert abs(a.sum(axis=1).mean() - want) < 1e-12
 
 
+def test_closed_forms_at_full_windows():
+    """With w >= 2n - 2 every token reaches every other: pair probability 1,
+    expected degree n, n^2 non-causal and n(n+1)/2 causal pairs; the brute
+    force agrees."""
+    for n in (2, 5, 16, 40):
+        for w in (2 * n - 2, 2 * n, 5 * n + 1):
+            if w < 1:
+                continue
+            assert graph.pair_probability_closed_form(n, w) == 1.0
+            assert graph.expected_degree_closed_form(n, w) == n
+            assert graph.attended_pairs_closed_form(n, w, "sa", False) == n * n
+            assert graph.attended_pairs_closed_form(n, w, "sa", True) == n * (n + 1) // 2
+            perm = prng.make_perm(n, w, 0, n)
+            assert graph.adjacency_sa(perm, w, False).all()
+            assert np.array_equal(graph.adjacency_sa(perm, w, True),
+                                  np.tril(np.ones((n, n), dtype=bool)))
+
+
 def test_pair_probability_matches_closed_form_and_w_over_n():
     n, w, seeds = 16, 4, 1500
     p_exact = graph.pair_probability_closed_form(n, w)
@@ -276,6 +294,43 @@ def test_full_attention_matches_sdpa(causal):
     c = _case()
     got = attention.full_attention(c.q, c.k, c.v, causal)
     np.testing.assert_allclose(got, _sdpa(c.q, c.k, c.v, causal=causal), atol=1e-12)
+
+
+def test_softmax_is_stable_at_large_scores():
+    """Scores of several hundred (exp overflows fp64 past ~709) must still give
+    the softmax: SA with a full window against torch SDPA in fp64."""
+    c = _case(b=1, n=24, hq=2, hkv=2, d=16)
+    q = np.asarray(c.q) * 40.0
+    k = np.asarray(c.k) * 40.0
+    s_max = np.abs(np.einsum("bihd,bjhd->bhij", q, k)).max() / 4.0
+    assert s_max > 800.0
+    perm = prng.make_perm(6, 0, 0, 24)[None]
+    for causal in (False, True):
+        want = _sdpa(q, k, c.v, causal=causal)
+        got = attention.sa_forward(q, k, c.v, perm, 48, causal)
+        assert np.isfinite(got).all()
+        np.testing.assert_allclose(got, want, atol=1e-10)
+        got = attention.full_attention(q, k, c.v, causal)
+        assert np.isfinite(got).all()
+        np.testing.assert_allclose(got, want, atol=1e-10)
+
+
+def test_argument_checks():
+    """Empty and impossible inputs: an empty shuffle is empty; a window below 1,
+    a negative length or a query with no key is rejected."""
+    assert prng.fisher_yates(0, lambda: 0).tolist() == []
+    with pytest.raises(ValueError):
+        prng.fisher_yates(-1, lambda: 0)
+    with pytest.raises(ValueError):
+        graph.half_width(0)
+    with pytest.raises(ValueError):
+        graph.neighbours_swa(5, 0, 2)
+    c = _case(b=1, n=4, hq=1, hkv=1, d=8)
+    mask = np.ones((4, 4), dtype=bool)
+    attention.masked_attention(c.q, c.k, c.v, mask)
+    mask[2] = False
+    with pytest.raises(ValueError):
+        attention.masked_attention(c.q, c.k, c.v, mask)
 
 
 def test_identity_perm_is_banded_attention():
