@@ -79,6 +79,9 @@ def _params(**kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(batch=0), 1), (dict(seqlen=0), 1), (dict(num_q_heads=3), 1), (dict(head_dim=96), 2),
     (dict(window=0), 1), (dict(kernel=7), 1), (dict(kernel=-1), 1),
+    # sizes whose token or row index would not fit 32 bits
+    (dict(batch=65536, seqlen=65536), 2),
+    (dict(batch=1, seqlen=1 << 27, num_q_heads=16, num_kv_heads=2), 2),
 ])
 def test_forward_argument_validation_without_gpu(kw, status):
     lib = sa.load()
