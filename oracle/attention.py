@@ -30,6 +30,8 @@ def _as_f64(x) -> np.ndarray:
 
 
 def _head_map(hq: int, hkv: int) -> np.ndarray:
+    """Query head hq reads kv head hq // g: the pages do not discuss GQA, and
+    the standard grouping is used."""
     if hq % hkv != 0:
         raise ValueError("num_q_heads must be a multiple of num_kv_heads")
     return np.arange(hq) // (hq // hkv)
@@ -37,7 +39,9 @@ def _head_map(hq: int, hkv: int) -> np.ndarray:
 
 def _attend(qrow: np.ndarray, kb: np.ndarray, vb: np.ndarray, keys: np.ndarray,
             head_map: np.ndarray, scale: float) -> np.ndarray:
-    """Softmax attention of one token's query heads over ``keys``.
+    """Softmax attention of one token's query heads over ``keys``: the
+    standard attention that "Core mechanism", step 2 runs inside the window,
+    with the maximum subtracted before exponentiating.
 
     qrow [Hq, d]; kb, vb [n, Hkv, d] (one sequence); returns [Hq, d].
     """
@@ -88,7 +92,8 @@ def sa_rows(q, k, v, perm, window: int, causal: bool, scale: float | None = None
 
 
 def swa_rows(q, k, v, window: int, scale: float | None = None, rows=None) -> np.ndarray:
-    """SWA output rows over keys [max(0, i-w+1), i] -> [R, Hq, d]."""
+    """SWA output rows over keys [max(0, i-w+1), i] -> [R, Hq, d]
+    ("Problem statement": a local window of size w)."""
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     _check(q, k, v)
     bsz, n, hq, d = q.shape
@@ -102,7 +107,8 @@ def swa_rows(q, k, v, window: int, scale: float | None = None, rows=None) -> np.
 
 
 def sigmoid(x) -> np.ndarray:
-    """1 / (1 + e^{-x}) in fp64 (overflow of e^{-x} correctly gives 0)."""
+    """The gates' sigmoid of the "Gated SA and SWA" equation, in fp64
+    (overflow of e^{-x} correctly gives 0)."""
     x = _as_f64(x)
     with np.errstate(over="ignore"):
         return 1.0 / (1.0 + np.exp(-x))
@@ -133,18 +139,18 @@ def _full(rows_fn, q):
 
 
 def sa_forward(q, k, v, perm, window: int, causal: bool, scale: float | None = None) -> np.ndarray:
-    """Full SA output [B, n, Hq, d] (all rows)."""
+    """Full SA output [B, n, Hq, d] (all rows; "Core mechanism", steps 1-3)."""
     return _full(lambda: sa_rows(q, k, v, perm, window, causal, scale), q)
 
 
 def swa_forward(q, k, v, window: int, scale: float | None = None) -> np.ndarray:
-    """Full SWA output [B, n, Hq, d]."""
+    """Full SWA output [B, n, Hq, d] ("Problem statement")."""
     return _full(lambda: swa_rows(q, k, v, window, scale), q)
 
 
 def gated_forward(q, k, v, perm, gate_sa, gate_swa, window: int, window_swa: int | None = None,
                   causal: bool = True, scale: float | None = None) -> np.ndarray:
-    """Full gated SA+SWA output [B, n, Hq, d]."""
+    """Full gated SA+SWA output [B, n, Hq, d] ("Gated SA and SWA" equation)."""
     return _full(lambda: gated_rows(q, k, v, perm, gate_sa, gate_swa, window, window_swa,
                                     causal, scale), q)
 
@@ -173,7 +179,9 @@ def masked_attention(q, k, v, mask: np.ndarray, scale: float | None = None) -> n
 
 
 def full_attention(q, k, v, causal: bool, scale: float | None = None) -> np.ndarray:
-    """Full softmax attention (all keys, or keys j <= i when causal)."""
+    """Full softmax attention (all keys, or keys j <= i when causal): what SA
+    reduces to once the window spans the whole sequence, the reference the
+    wide-window pins compare against."""
     n = np.shape(q)[1]
     mask = np.tril(np.ones((n, n), dtype=bool)) if causal else np.ones((n, n), dtype=bool)
     return masked_attention(q, k, v, mask, scale)

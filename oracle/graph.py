@@ -23,7 +23,8 @@ from .prng import inverse_perm
 
 
 def half_width(window: int) -> int:
-    """SA half-width h = floor(w / 2)."""
+    """SA half-width h = floor(w / 2): the window |p - q| <= w/2 of "Core
+    mechanism", step 2; the pages leave odd w open and floor is taken."""
     if window < 1:
         raise ValueError("window must be >= 1")
     return window // 2
@@ -31,7 +32,13 @@ def half_width(window: int) -> int:
 
 def neighbours_sa(perm: np.ndarray, window: int, causal: bool, i: int,
                   inv: np.ndarray | None = None) -> np.ndarray:
-    """Sorted original-token indices that token i attends to under SA."""
+    """Sorted original-token indices that token i attends to under SA.
+
+    "Core mechanism", steps 1-3: token i sits at permuted position
+    p = sigma^-1(i) and attends to the tokens at permuted positions within
+    distance h of p, truncated at the sequence ends.  Causal ("Theoretical
+    properties", causal-constraint bullet): only keys whose original index
+    does not exceed i."""
     perm = np.asarray(perm)
     n = perm.shape[0]
     if inv is None:
@@ -46,14 +53,16 @@ def neighbours_sa(perm: np.ndarray, window: int, causal: bool, i: int,
 
 
 def neighbours_swa(n: int, window: int, i: int) -> np.ndarray:
-    """Original-token indices that token i attends to under SWA."""
+    """Original-token indices that token i attends to under SWA: the local
+    window of size w ending at i ("Problem statement"), clipped at 0."""
     if window < 1:
         raise ValueError("window must be >= 1")
     return np.arange(max(0, i - window + 1), i + 1, dtype=np.int64)
 
 
 def adjacency_sa(perm: np.ndarray, window: int, causal: bool) -> np.ndarray:
-    """Boolean A[i, j] = (j in N(i)) for one sequence, built token by token."""
+    """Boolean A[i, j] = (j in N(i)) for one sequence, built token by token:
+    the random neighbourhood graph of "Core mechanism", closing paragraph."""
     perm = np.asarray(perm)
     n = perm.shape[0]
     inv = inverse_perm(perm)
@@ -64,6 +73,8 @@ def adjacency_sa(perm: np.ndarray, window: int, causal: bool) -> np.ndarray:
 
 
 def adjacency_swa(n: int, window: int) -> np.ndarray:
+    """Boolean A[i, j] = (j in N_swa(i)): SWA's banded graph ("Problem
+    statement")."""
     a = np.zeros((n, n), dtype=bool)
     for i in range(n):
         a[i, neighbours_swa(n, window, i)] = True
@@ -71,7 +82,8 @@ def adjacency_swa(n: int, window: int) -> np.ndarray:
 
 
 def attended_pairs_closed_form(n: int, window: int, path: str, causal: bool = True) -> int:
-    """Exact number of (query, key) pairs attended in one sequence.
+    """Exact number of (query, key) pairs attended in one sequence: the
+    linear O(n w) work of "Theoretical properties" and "Results / Efficiency".
 
     Independent of sigma: the window covers the same set of permuted position
     pairs for every sigma.  Non-causal SA counts every ordered pair at
@@ -102,13 +114,16 @@ def pair_probability_closed_form(n: int, window: int) -> float:
 
 
 def expected_degree_closed_form(n: int, window: int) -> float:
-    """E|N(i)| for non-causal SA averaged over tokens: 1 + (2hn - h(h+1))/n."""
+    """E|N(i)| for non-causal SA averaged over tokens: 1 + (2hn - h(h+1))/n.
+    The pages give the neighbourhood's expected size as about w ("Core
+    mechanism", closing paragraph)."""
     h = min(half_width(window), n - 1)
     return 1.0 + (2 * h * n - h * (h + 1)) / n
 
 
 def receptive_field_sizes(adjacencies: list[np.ndarray]) -> np.ndarray:
-    """|R_l(i)| for l = 1..L, where R_0(i) = {i} and
+    """Receptive fields over stacked layers ("Theoretical properties",
+    receptive-field bullet): |R_l(i)| for l = 1..L, where R_0(i) = {i} and
     R_l(i) = union over j in N_l(i) of R_{l-1}(j)  (layer 1 acts first).
 
     ``adjacencies[l-1]`` is layer l's boolean A[i, j] = (j in N_l(i)).

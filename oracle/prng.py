@@ -34,7 +34,11 @@ MIX2 = 0x94D049BB133111EB
 
 
 def splitmix64_step(state: int) -> tuple[int, int]:
-    """One splitmix64 step: returns (new_state, output)."""
+    """One splitmix64 step: returns (new_state, output).
+
+    S. Vigna's public-domain generator.  The pages ask only for
+    sigma ~ Uniform(S_n) ("Core mechanism", step 1) and name no generator; this
+    one is the convention fixed for both the oracle and the library."""
     state = (state + GOLDEN_GAMMA) & MASK64
     z = state
     z = ((z ^ (z >> 30)) * MIX1) & MASK64
@@ -44,7 +48,10 @@ def splitmix64_step(state: int) -> tuple[int, int]:
 
 
 def stream_state(seed: int, layer: int, batch_index: int) -> int:
-    """Initial splitmix64 state of the sigma stream for (seed, layer, batch)."""
+    """Initial splitmix64 state of the sigma stream for (seed, layer, batch).
+
+    One stream per layer and sequence: "Core mechanism", step 1 draws an
+    independent permutation for every layer."""
     if layer < 0 or batch_index < 0:
         raise ValueError("layer and batch_index must be non-negative")
     start = (seed + (layer << 32) + batch_index) & MASK64
@@ -54,6 +61,9 @@ def stream_state(seed: int, layer: int, batch_index: int) -> int:
 
 def fisher_yates(n: int, draw) -> np.ndarray:
     """Durstenfeld shuffle of [0, n) driven by ``draw()`` -> uint64 Python int.
+
+    With uniform draws it yields sigma ~ Uniform(S_n) ("Core mechanism",
+    step 1); index j for position i is the high word of x * (i + 1).
 
     ``draw`` is a parameter so that tests can drive the index mapping with
     stub generators.
@@ -69,7 +79,8 @@ def fisher_yates(n: int, draw) -> np.ndarray:
 
 
 def make_perm(seed: int, layer: int, batch_index: int, n: int) -> np.ndarray:
-    """sigma for (seed, layer, batch_index) over n tokens, as int64[n]."""
+    """sigma for (seed, layer, batch_index) over n tokens, as int64[n]
+    ("Core mechanism", step 1: X'[p] = X[sigma[p]])."""
     state = stream_state(seed, layer, batch_index)
 
     def draw():
