@@ -1,6 +1,8 @@
 // C-ABI entry points of libsa: argument validation, kernel choice, the host
-// sigma generator and error reporting.  Every step of the attention itself
-// runs in the CUDA kernels of sa_simt.cu / sa_tc.cu / sa_perm.cu.
+// sigma generator (sigma ~ Uniform(S_n), one per layer: Stochastic Attention
+// summary, "Core mechanism" step 1) and error reporting.  Every step of the
+// attention itself runs in the CUDA kernels of sa_tc_ring.cu, sa_tc_flash.cu,
+// sa_tc.cu and sa_simt.cu; sigma^-1 in sa_perm.cu.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
