@@ -186,3 +186,30 @@ def test_forward_reports_out_of_range_perm_without_fault(kernel):
     err2 = _err()
     sa.sa_forward(inp.q, inp.k, inp.v, good, 16, kernel=kernel, err=err2)
     assert sa.check_error(err2) == sa.SA_OK
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
+@pytest.mark.parametrize("path", ["sa", "swa", "gated"])
+def test_writes_stay_inside_out(kernel, path):
+    """Canary-padded output: the out tensor sits inside a NaN-filled buffer
+    with 8 KB on each side.  Every row of out must be written (finite) and
+    the padding must keep its NaNs (no scatter row outside out)."""
+    b, n, hq, hkv, d, w = 2, 333, 8, 2, 128, 64
+    if not must_support(kernel, path, hq // hkv, w, d=d):
+        pytest.skip("shape outside this kernel's required range")
+    inp = Inputs(b, n, hq, hkv, d, seed=11)
+    _, perm_d = perms(3, 0, b, n)
+    numel, pad = b * n * hq * d, 4096  # pad: bf16 elements, a multiple of 16 bytes
+    buf = torch.full((pad + numel + pad,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[pad:pad + numel].view(b, n, hq, d)
+    err = _err()
+    if path == "sa":
+        sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, out=out, kernel=kernel, err=err)
+    elif path == "swa":
+        sa.swa_forward(inp.q, inp.k, inp.v, w, out=out, kernel=kernel, err=err)
+    else:
+        sa.sa_swa_gated_forward(inp.q, inp.k, inp.v, perm_d, inp.ga, inp.gw, w, causal=True,
+                                out=out, kernel=kernel, err=err)
+    assert sa.check_error(err) == sa.SA_OK
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + numel:]).all()
+    assert torch.isfinite(out.float()).all()
