@@ -119,3 +119,19 @@ def test_params_struct_layout_matches_header():
     assert ctypes.sizeof(sa.SaParams) == 48
     assert sa.SaParams.err.offset == 40
     assert sa.SaParams.softmax_scale.offset == 32
+
+
+def test_binding_constants_match_the_header():
+    """Status codes, kernel selectors and error bits of the Python binding are
+    the values include/libsa.h declares."""
+    text = (Path(__file__).resolve().parents[1] / "include" / "libsa.h").read_text()
+    enum = dict((m.group(1), int(m.group(2)))
+                for m in re.finditer(r"\b(SA_(?:OK|ERR_\w+|KERNEL_\w+))\s*=\s*(\d+)", text))
+    defines = dict((m.group(1), int(m.group(2)))
+                   for m in re.finditer(r"#define\s+(SA_ERRBIT_\w+)\s+(\d+)", text))
+    assert len(enum) == 13 and len(defines) == 4
+    for name, value in enum.items():
+        py = name if name.startswith("SA_OK") or name.startswith("SA_ERR_") else name[3:]
+        assert getattr(sa, py) == value, name
+    for name, value in defines.items():
+        assert getattr(sa, name[3:]) == value, name
