@@ -16,6 +16,10 @@ gist.science/ja/paper/2604.00754 and gist.science/ko/paper/2604.00754):
                   written per ORIGINAL token i over its neighbour set
                   (sections "Core mechanism" steps 1-3, "Theoretical
                   properties" causal bullet, "Gated SA and SWA" equation).
+* ``backward``  -- gradients of SA, SWA and the gated merge with respect to
+                  Q, K, V and the gate logits, and each row's log-sum-exp
+                  (the chain rule through the forward definition; the pages
+                  use SA to pretrain a model: "Main contributions", item 3).
 * ``graph``     -- neighbour sets, the pairwise connection probability and the
                   receptive-field growth over stacked layers
                   (section "Core mechanism", last paragraph; "Theoretical
@@ -36,6 +40,13 @@ from .attention import (
     gated_forward,
     full_attention,
     masked_attention,
+)
+from .backward import (
+    sa_backward,
+    swa_backward,
+    gated_backward,
+    sa_lse,
+    swa_lse,
 )
 from .graph import (
     neighbours_sa,
@@ -62,6 +73,11 @@ __all__ = [
     "gated_forward",
     "full_attention",
     "masked_attention",
+    "sa_backward",
+    "swa_backward",
+    "gated_backward",
+    "sa_lse",
+    "swa_lse",
     "neighbours_sa",
     "neighbours_swa",
     "adjacency_sa",
