@@ -30,7 +30,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -57,7 +56,10 @@ WORKLOADS = {
                          num_kv_heads=16, head_dim=128, window=128, causal=True, path="sa",
                          seed=0, std=None),
 }
-PROFILE = os.path.join(ROOT, "profiles", "sa_ring_kernel_long_prefill_gqa_w128.md")
+# DRAM bytes per launch of the headline kernel from its ncu capture, with the
+# sha256 of the kernel sources the capture was taken on (written beside the
+# ncu summary, profiles/sa_ring_kernel_long_prefill_gqa_w128.md)
+PROFILE = os.path.join(ROOT, "profiles", "sa_ring_kernel_long_prefill_gqa_w128.json")
 # the ring kernel and the tcgen05 helpers it inlines: the profile's DRAM
 # counters hold only while these files are unchanged
 KERNEL_SOURCES = [os.path.join(ROOT, "stochastic_sliding_window_gb300", "csrc", f)
@@ -121,18 +123,17 @@ def kernel_source_sha256() -> str:
 
 
 def profiled_traffic() -> int | None:
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (its sha256 is recorded in the summary)."""
+    """DRAM bytes per launch from the committed ncu capture, if it was taken
+    on the current kernel source (null once the kernel has changed)."""
     try:
-        text = open(PROFILE).read()
+        with open(PROFILE) as f:
+            rec = json.load(f)
         src = kernel_source_sha256()
-    except OSError:
+    except (OSError, ValueError):
         return None
-    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != src:
+    if rec.get("kernel_source_sha256") != src:
         return None
-    return int(m_tr.group(1))
+    return int(rec["traffic_bytes_per_launch"])
 
 
 # ------------------------------------------------------------------ oracle leg
@@ -272,8 +273,15 @@ def make_inputs(wl):
 
 
 def config_of(wl) -> dict:
-    return {k: wl[k] for k in ("workload", "batch", "seq_len", "num_q_heads", "num_kv_heads",
-                               "head_dim", "window", "causal", "path")}
+    """The workload keys both arms report (so that their configs compare
+    equal), with how the GPU arm keeps L2 from serving a step's inputs."""
+    b, n, hq, hkv, d = (wl[k] for k in ("batch", "seq_len", "num_q_heads", "num_kv_heads",
+                                        "head_dim"))
+    in_mb = 2 * b * n * d * (hq + 2 * hkv) / 1e6
+    cfg = {k: wl[k] for k in ("workload", "batch", "seq_len", "num_q_heads", "num_kv_heads",
+                              "head_dim", "window", "causal", "path")}
+    cfg["l2"] = f"flushed between steps (256 MB write); inputs {in_mb:.0f} MB"
+    return cfg
 
 
 def run_reference(args, wl=WORKLOAD):
@@ -349,7 +357,7 @@ def run_ours(args, wl=WORKLOAD):
     stream = torch.cuda.current_stream(dev)
 
     kern = {"auto": sa.KERNEL_AUTO, "simt": sa.KERNEL_SIMT, "gather": sa.KERNEL_TCGEN05_GATHER,
-            "ring": sa.KERNEL_TCGEN05_RING, "flash": sa.KERNEL_TCGEN05_FLASH}[args.kernel]
+            "ring": sa.KERNEL_TCGEN05_RING, "chunk": sa.KERNEL_TCGEN05_CHUNK}[args.kernel]
 
     def forward(q_, k_, v_, p_, ga_, gw_, o_, st=stream):
         if gated:
@@ -470,17 +478,15 @@ def run_ours(args, wl=WORKLOAD):
     roof.update(bytes_per_launch=bytes_alg, flops_per_launch=flops_alg,
                 hbm_frac=bytes_alg / secs / 1e9 / peaks["hbm_gbs"],
                 tensor_frac=flops_alg / secs / 1e12 / peaks["bf16_tflops"])
-    in_mb = (bytes_alg - 2 * wl["batch"] * wl["seq_len"] * wl["num_q_heads"] * wl["head_dim"]) / 1e6
     line = dict(
         metric=metric_of(wl), value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
         warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True, scaling="weak",
         vs_baseline=None, dtype="bf16", data="synthetic",
-        config=config_of(wl)
-        | dict(l2=f"flushed between steps (256 MB write); inputs {in_mb:.0f} MB",
-               kernel={sa.KERNEL_SIMT: "simt", sa.KERNEL_TCGEN05_GATHER: "tcgen05-gather",
-                       sa.KERNEL_TCGEN05_RING: "tcgen05-ring",
-                       sa.KERNEL_TCGEN05_FLASH: "tcgen05-flash"}.get(kernel, str(kernel)),
-               parallelism="replicas" if world > 1 else "single-gpu"),
+        config=config_of(wl),
+        run=dict(kernel={sa.KERNEL_SIMT: "simt", sa.KERNEL_TCGEN05_GATHER: "tcgen05-gather",
+                         sa.KERNEL_TCGEN05_RING: "tcgen05-ring",
+                         sa.KERNEL_TCGEN05_CHUNK: "tcgen05-chunk"}.get(kernel, str(kernel)),
+                 parallelism="replicas" if world > 1 else "single-gpu"),
         roofline=roof,
         cpu_baseline=cpu,
         e2e=dict(value=job_tokens_per_s(world, tokens, e2e_ms), unit="tokens/s",
@@ -506,7 +512,7 @@ def main():
                     help="shape to time (default: the long-prefill GQA headline)")
     ap.add_argument("--window", type=int, default=0, help="override the workload's window")
     ap.add_argument("--seq-len", type=int, default=0, help="override the workload's length")
-    ap.add_argument("--kernel", choices=["auto", "simt", "gather", "ring", "flash"],
+    ap.add_argument("--kernel", choices=["auto", "simt", "gather", "ring", "chunk"],
                     default="auto", help="force one of the library's kernels (default: its choice)")
     args = ap.parse_args()
     if args.warmup < 3:

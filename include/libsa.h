@@ -71,7 +71,7 @@ enum {
   SA_KERNEL_TCGEN05 = 2, /* the better-fitting tcgen05 kernel; SA_ERR_UNSUPPORTED if none fits */
   SA_KERNEL_TCGEN05_GATHER = 3, /* tcgen05 kernel that gathers every window with TMA */
   SA_KERNEL_TCGEN05_RING = 4,   /* tcgen05 kernel with a sliding K/V ring (spans <= 160 keys) */
-  SA_KERNEL_TCGEN05_FLASH = 5   /* tcgen05 kernel streaming the span in 128-key chunks with an
+  SA_KERNEL_TCGEN05_CHUNK = 5   /* tcgen05 kernel streaming the span in 128-key chunks with an
                                    online softmax (any window) */
 };
 
@@ -166,6 +166,24 @@ sa_status_t sa_check_error(const int32_t* d_err, cudaStream_t stream);
 /* Enqueue a reset of the device error word (NULL: the library's own) to 0. */
 sa_status_t sa_clear_error(int32_t* d_err, cudaStream_t stream);
 
+/*
+ * Failure detection: every pipeline wait inside the tcgen05 kernels is
+ * bounded by a number of SM cycles; a wait that runs past it sets
+ * SA_ERRBIT_TIMEOUT in the device error word, the kernel stops its pipeline,
+ * lets its own copies and MMAs finish, frees its tensor memory and returns
+ * (sa_check_error then reports SA_ERR_TIMEOUT; the CUDA context stays usable).
+ * sa_set_wait_limit sets that bound for every launch made from now on, by any
+ * thread; cycles <= 0 restores the default (4e9 cycles, ~2 s at the maximum
+ * SM clock).  A bound far below a kernel's normal waits (a few hundred cycles)
+ * makes a call give up on purpose, which is how the timeout path is tested.
+ * The final wait for a kernel's own MMAs before tensor memory is freed has a
+ * fixed bound of its own and is not affected.  Host only; never fails.
+ */
+sa_status_t sa_set_wait_limit(int64_t cycles);
+
+/* The current wait bound in SM cycles (see sa_set_wait_limit). */
+int64_t sa_get_wait_limit(void);
+
 /* Static text for a status code. */
 const char* sa_status_string(sa_status_t status);
 
@@ -173,7 +191,7 @@ const char* sa_status_string(sa_status_t status);
 const char* sa_last_error_message(void);
 
 /* SA_KERNEL_SIMT, SA_KERNEL_TCGEN05_GATHER, SA_KERNEL_TCGEN05_RING or
- * SA_KERNEL_TCGEN05_FLASH: the kernel the last successful forward call on
+ * SA_KERNEL_TCGEN05_CHUNK: the kernel the last successful forward call on
  * this thread launched (0 before any; for the gated path, the SA pass's). */
 int32_t sa_last_kernel(void);
 

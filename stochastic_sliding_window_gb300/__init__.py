@@ -16,7 +16,7 @@ from ._libsa import (
     KERNEL_TCGEN05,
     KERNEL_TCGEN05_GATHER,
     KERNEL_TCGEN05_RING,
-    KERNEL_TCGEN05_FLASH,
+    KERNEL_TCGEN05_CHUNK,
     SA_ERR_BAD_PERM,
     SA_ERR_CUDA,
     SA_ERR_INTERNAL,
@@ -29,6 +29,7 @@ from ._libsa import (
     SaParams,
     check_error,
     clear_error,
+    get_wait_limit,
     last_kernel,
     last_launch_count,
     load,
@@ -37,13 +38,14 @@ from ._libsa import (
     sa_forward,
     sa_inverse_perm,
     sa_swa_gated_forward,
+    set_wait_limit,
     swa_forward,
 )
 
 __all__ = [
-    "ERRBIT_DUP", "ERRBIT_INTERNAL", "ERRBIT_RANGE", "ERRBIT_TIMEOUT", "KERNEL_AUTO", "KERNEL_SIMT", "KERNEL_TCGEN05", "KERNEL_TCGEN05_GATHER", "KERNEL_TCGEN05_RING", "KERNEL_TCGEN05_FLASH",
+    "ERRBIT_DUP", "ERRBIT_INTERNAL", "ERRBIT_RANGE", "ERRBIT_TIMEOUT", "KERNEL_AUTO", "KERNEL_SIMT", "KERNEL_TCGEN05", "KERNEL_TCGEN05_GATHER", "KERNEL_TCGEN05_RING", "KERNEL_TCGEN05_CHUNK",
     "SA_ERR_BAD_PERM", "SA_ERR_CUDA", "SA_ERR_INTERNAL", "SA_ERR_INVALID_ARG", "SA_ERR_TIMEOUT", "SA_ERR_UNSUPPORTED",
     "SA_OK", "SIGNATURES", "SaError", "SaParams", "check_error", "clear_error", "last_kernel",
     "last_launch_count", "load", "make_perm", "make_perms", "sa_forward", "sa_inverse_perm",
-    "sa_swa_gated_forward", "swa_forward",
+    "sa_swa_gated_forward", "set_wait_limit", "get_wait_limit", "swa_forward",
 ]

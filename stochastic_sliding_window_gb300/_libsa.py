@@ -10,7 +10,7 @@ fallback implementation.
 from __future__ import annotations
 
 import ctypes
-from ctypes import POINTER, byref, c_char_p, c_float, c_int32, c_size_t, c_uint64, c_void_p
+from ctypes import POINTER, byref, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
 from pathlib import Path
 
 import numpy as np
@@ -20,7 +20,7 @@ LIB_PATH = Path(__file__).resolve().with_name("libsa.so")
 SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CUDA, SA_ERR_BAD_PERM, SA_ERR_TIMEOUT, \
     SA_ERR_INTERNAL = range(7)
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TCGEN05, KERNEL_TCGEN05_GATHER, KERNEL_TCGEN05_RING = 0, 1, 2, 3, 4
-KERNEL_TCGEN05_FLASH = 5
+KERNEL_TCGEN05_CHUNK = 5
 ERRBIT_RANGE, ERRBIT_DUP, ERRBIT_TIMEOUT, ERRBIT_INTERNAL = 1, 2, 4, 8
 
 # Every function the header declares, with (restype, argtypes).
@@ -34,6 +34,8 @@ SIGNATURES = {
     "sa_make_perm": (c_int32, [c_uint64, c_int32, c_int32, c_int32, POINTER(c_int32)]),
     "sa_check_error": (c_int32, [c_void_p, c_void_p]),
     "sa_clear_error": (c_int32, [c_void_p, c_void_p]),
+    "sa_set_wait_limit": (c_int32, [c_int64]),
+    "sa_get_wait_limit": (c_int64, []),
     "sa_status_string": (c_char_p, [c_int32]),
     "sa_last_error_message": (c_char_p, []),
     "sa_last_kernel": (c_int32, []),
@@ -105,44 +107,78 @@ def _stream(t, stream):
 
 
 def _need(t, name, dtype, ndim):
+    """Type, dtype, rank and contiguity of one tensor argument."""
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
 
 
+def _shape(t, name, want):
+    if tuple(t.shape) != tuple(want):
+        raise ValueError(f"{name} must have shape {tuple(want)}, got {tuple(t.shape)}")
+
+
+def _on_device(first, name0, named):
+    """Every tensor on the first one's CUDA device (the library works on the
+    current device, which each call sets to that one)."""
+    if not first.is_cuda:
+        raise ValueError(f"{name0} must be a CUDA tensor")
+    for name, t in named:
+        if t is not None and t.device != first.device:
+            raise ValueError(f"{name} must be on {first.device}, got {t.device}")
+
+
+def _check_err(err):
+    import torch
+    if err is None:
+        return
+    if not isinstance(err, torch.Tensor) or err.dtype != torch.int32 or err.numel() < 1:
+        raise TypeError("err must be an int32 tensor with at least one element")
+
+
 def _params(q, k, window, window_swa, causal, softmax_scale, kernel, err) -> SaParams:
     b, n, hq, d = q.shape
-    if k.shape[0] != b or k.shape[1] != n or k.shape[3] != d:
-        raise ValueError("q and k/v shapes disagree")
     return SaParams(b, n, hq, k.shape[2], d, int(window), int(window_swa), int(bool(causal)),
                     float(softmax_scale), int(kernel), c_void_p(err.data_ptr() if err is not None else None))
 
 
-def _qkv(q, k, v):
+def _validate(q, k, v, out, perm=None, gates=(), err=None):
+    """Every check the C ABI cannot make, since it trusts the sizes it is
+    given: dtypes, ranks, contiguity, shapes against q's, one device.  Raises
+    before anything is launched."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
         _need(t, name, torch.bfloat16, 4)
-    if k.shape != v.shape:
-        raise ValueError("k and v shapes differ")
+    b, n, hq, d = q.shape
+    if k.shape[0] != b or k.shape[1] != n or k.shape[3] != d:
+        raise ValueError(f"k must be [B={b}, n={n}, Hkv, d={d}], got {tuple(k.shape)}")
+    _shape(v, "v", k.shape)
+    _shape(out, "out", q.shape)
+    if perm is not None:
+        _need(perm, "perm", torch.int32, 2)
+        _shape(perm, "perm", (b, n))
+    for name, g in gates:
+        _need(g, name, torch.float32, 3)
+        _shape(g, name, (b, n, hq))
+    _check_err(err)
+    _on_device(q, "q", [("k", k), ("v", v), ("out", out), ("perm", perm), ("err", err)]
+               + list(gates))
 
 
 def sa_forward(q, k, v, perm, window: int, causal: bool = True, softmax_scale: float = 0.0,
                out=None, kernel: int = KERNEL_AUTO, err=None, stream=None):
     """Stochastic Attention forward; returns out (bf16 [B, n, Hq, d])."""
     import torch
-    _qkv(q, k, v)
-    _need(perm, "perm", torch.int32, 2)
     out = torch.empty_like(q) if out is None else out
-    _need(out, "out", torch.bfloat16, 4)
+    _validate(q, k, v, out, perm=perm, err=err)
     prm = _params(q, k, window, 0, causal, softmax_scale, kernel, err)
-    _check(load().sa_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(), perm.data_ptr(),
-                             out.data_ptr(), _stream(q, stream)))
+    with torch.cuda.device(q.device):
+        _check(load().sa_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                 perm.data_ptr(), out.data_ptr(), _stream(q, stream)))
     return out
 
 
@@ -150,12 +186,12 @@ def swa_forward(q, k, v, window: int, softmax_scale: float = 0.0, out=None,
                 kernel: int = KERNEL_AUTO, err=None, stream=None):
     """Sliding-window attention over the original order."""
     import torch
-    _qkv(q, k, v)
     out = torch.empty_like(q) if out is None else out
-    _need(out, "out", torch.bfloat16, 4)
+    _validate(q, k, v, out, err=err)
     prm = _params(q, k, window, 0, True, softmax_scale, kernel, err)
-    _check(load().swa_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                              _stream(q, stream)))
+    with torch.cuda.device(q.device):
+        _check(load().swa_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                  out.data_ptr(), _stream(q, stream)))
     return out
 
 
@@ -164,20 +200,19 @@ def sa_swa_gated_forward(q, k, v, perm, gate_sa, gate_swa, window: int, window_s
                          kernel: int = KERNEL_AUTO, err=None, stream=None):
     """sigmoid(gate_sa) * SA + sigmoid(gate_swa) * SWA."""
     import torch
-    _qkv(q, k, v)
-    _need(perm, "perm", torch.int32, 2)
-    _need(gate_sa, "gate_sa", torch.float32, 3)
-    _need(gate_swa, "gate_swa", torch.float32, 3)
     out = torch.empty_like(q) if out is None else out
-    _need(out, "out", torch.bfloat16, 4)
+    _validate(q, k, v, out, perm=perm, gates=(("gate_sa", gate_sa), ("gate_swa", gate_swa)),
+              err=err)
     prm = _params(q, k, window, window_swa, causal, softmax_scale, kernel, err)
     lib = load()
-    ws = lib.sa_gated_workspace_size(byref(prm))
-    work = torch.empty(ws, dtype=torch.uint8, device=q.device) if ws else None
-    _check(lib.sa_swa_gated_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                    perm.data_ptr(), gate_sa.data_ptr(), gate_swa.data_ptr(),
-                                    out.data_ptr(), work.data_ptr() if work is not None else None,
-                                    ws, _stream(q, stream)))
+    with torch.cuda.device(q.device):
+        ws = lib.sa_gated_workspace_size(byref(prm))
+        work = torch.empty(ws, dtype=torch.uint8, device=q.device) if ws else None
+        _check(lib.sa_swa_gated_forward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                        perm.data_ptr(), gate_sa.data_ptr(), gate_swa.data_ptr(),
+                                        out.data_ptr(),
+                                        work.data_ptr() if work is not None else None, ws,
+                                        _stream(q, stream)))
     return out
 
 
@@ -187,25 +222,45 @@ def sa_inverse_perm(perm, inv=None, err=None, stream=None):
     _need(perm, "perm", torch.int32, 2)
     inv = torch.empty_like(perm) if inv is None else inv
     _need(inv, "inv", torch.int32, 2)
+    _shape(inv, "inv", perm.shape)
+    _check_err(err)
+    _on_device(perm, "perm", [("inv", inv), ("err", err)])
     b, n = perm.shape
-    _check(load().sa_inverse_perm(perm.data_ptr(), inv.data_ptr(), b, n,
-                                  err.data_ptr() if err is not None else None, _stream(perm, stream)))
+    with torch.cuda.device(perm.device):
+        _check(load().sa_inverse_perm(perm.data_ptr(), inv.data_ptr(), b, n,
+                                      err.data_ptr() if err is not None else None,
+                                      _stream(perm, stream)))
     return inv
 
 
 def check_error(err=None, stream=None) -> int:
     """Synchronise and map the device error word to a status (0 = fine)."""
     import torch
+    _check_err(err)
     dev = err.device if err is not None else torch.device("cuda", torch.cuda.current_device())
-    s = _stream(torch.empty(0, device=dev), stream)
-    return int(load().sa_check_error(err.data_ptr() if err is not None else None, s))
+    with torch.cuda.device(dev):
+        s = _stream(torch.empty(0, device=dev), stream)
+        return int(load().sa_check_error(err.data_ptr() if err is not None else None, s))
 
 
 def clear_error(err=None, stream=None):
     import torch
+    _check_err(err)
     dev = err.device if err is not None else torch.device("cuda", torch.cuda.current_device())
-    _check(load().sa_clear_error(err.data_ptr() if err is not None else None,
-                                 _stream(torch.empty(0, device=dev), stream)))
+    with torch.cuda.device(dev):
+        _check(load().sa_clear_error(err.data_ptr() if err is not None else None,
+                                     _stream(torch.empty(0, device=dev), stream)))
+
+
+def set_wait_limit(cycles: int) -> None:
+    """Bound every pipeline wait of later tcgen05 launches to `cycles` SM
+    cycles (<= 0: the default).  A tiny bound makes a call give up on
+    purpose: the timeout path's test."""
+    _check(load().sa_set_wait_limit(int(cycles)))
+
+
+def get_wait_limit() -> int:
+    return int(load().sa_get_wait_limit())
 
 
 def make_perm(seed: int, layer: int, batch_index: int, n: int) -> np.ndarray:

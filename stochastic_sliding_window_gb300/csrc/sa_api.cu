@@ -1,8 +1,9 @@
 // C-ABI entry points of libsa: argument validation, kernel choice, the host
 // sigma generator (sigma ~ Uniform(S_n), one per layer: Stochastic Attention
 // summary, "Core mechanism" step 1) and error reporting.  Every step of the
-// attention itself runs in the CUDA kernels of sa_tc_ring.cu, sa_tc_flash.cu,
+// attention itself runs in the CUDA kernels of sa_tc_ring.cu, sa_tc_chunk.cu,
 // sa_tc.cu and sa_simt.cu; sigma^-1 in sa_perm.cu.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -17,6 +18,11 @@ static thread_local int32_t g_last_kernel = 0;
 static thread_local int32_t g_last_launches = 0;
 
 __device__ int32_t g_error_word = 0;
+
+constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s at the maximum SM clock
+static std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+
+long long wait_limit_cycles() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 sa_status_t fail(sa_status_t st, const char* fmt, ...) {
   va_list ap;
@@ -45,7 +51,7 @@ static sa_status_t check_params(const sa_params_t* prm, bool need_window) {
   if (prm->head_dim != 64 && prm->head_dim != 128)
     return fail(SA_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", prm->head_dim);
   if (need_window && prm->window < 1) return fail(SA_ERR_INVALID_ARG, "window must be >= 1");
-  if (prm->kernel < SA_KERNEL_AUTO || prm->kernel > SA_KERNEL_TCGEN05_FLASH)
+  if (prm->kernel < SA_KERNEL_AUTO || prm->kernel > SA_KERNEL_TCGEN05_CHUNK)
     return fail(SA_ERR_INVALID_ARG, "unknown kernel selector %d", prm->kernel);
   const double rows = double(prm->batch) * prm->seqlen * prm->num_q_heads;
   if (rows * prm->head_dim >= 9.0e18 || double(prm->batch) * prm->seqlen >= 2147483647.0 ||
@@ -94,22 +100,22 @@ static sa_status_t finish(sa_status_t st, int32_t kernel, int32_t launches) {
 }
 
 // The concrete kernel a request maps to for one path (SIMT, gather, ring,
-// flash), or 0 when the requested tcgen05 variant cannot run this shape.
-// The tcgen05 preference: the ring kernel (narrow spans), else the flash
+// chunk), or 0 when the requested tcgen05 variant cannot run this shape.
+// The tcgen05 preference: the ring kernel (narrow spans), else the chunk
 // kernel (any span), else the gather kernel.
 static int32_t pick_kernel(const sa_params_t* prm, const Problem& pb, Path path) {
   const bool ring = ring_supported(pb, path);
-  const bool flash = flash_supported(pb, path);
+  const bool chunk = chunk_supported(pb, path);
   const bool gather = tc_supported(pb, path);
   const int32_t best = ring ? SA_KERNEL_TCGEN05_RING
-                       : flash ? SA_KERNEL_TCGEN05_FLASH
+                       : chunk ? SA_KERNEL_TCGEN05_CHUNK
                        : gather ? SA_KERNEL_TCGEN05_GATHER
                                 : 0;
   switch (prm->kernel) {
     case SA_KERNEL_SIMT: return SA_KERNEL_SIMT;
     case SA_KERNEL_TCGEN05_RING: return ring ? SA_KERNEL_TCGEN05_RING : 0;
     case SA_KERNEL_TCGEN05_GATHER: return gather ? SA_KERNEL_TCGEN05_GATHER : 0;
-    case SA_KERNEL_TCGEN05_FLASH: return flash ? SA_KERNEL_TCGEN05_FLASH : 0;
+    case SA_KERNEL_TCGEN05_CHUNK: return chunk ? SA_KERNEL_TCGEN05_CHUNK : 0;
     case SA_KERNEL_TCGEN05: return best;
     default: return best ? best : SA_KERNEL_SIMT;
   }
@@ -118,7 +124,7 @@ static int32_t pick_kernel(const sa_params_t* prm, const Problem& pb, Path path)
 static sa_status_t launch_kernel(int32_t kernel, const Problem& pb, Path path, const float* gate,
                                  int accumulate, cudaStream_t s) {
   if (kernel == SA_KERNEL_TCGEN05_RING) return launch_ring(pb, path, gate, accumulate, s);
-  if (kernel == SA_KERNEL_TCGEN05_FLASH) return launch_flash(pb, path, gate, accumulate, s);
+  if (kernel == SA_KERNEL_TCGEN05_CHUNK) return launch_chunk(pb, path, gate, accumulate, s);
   return launch_tc(pb, path, gate, accumulate, s);
 }
 
@@ -258,6 +264,14 @@ extern "C" sa_status_t sa_clear_error(int32_t* d_err, cudaStream_t stream) {
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(ce));
   return SA_OK;
 }
+
+extern "C" sa_status_t sa_set_wait_limit(int64_t cycles) {
+  g_wait_limit.store(cycles > 0 ? (long long)cycles : kDefaultWaitLimit, std::memory_order_relaxed);
+  g_msg[0] = '\0';
+  return SA_OK;
+}
+
+extern "C" int64_t sa_get_wait_limit(void) { return wait_limit_cycles(); }
 
 extern "C" const char* sa_status_string(sa_status_t status) {
   switch (status) {

@@ -1,8 +1,9 @@
 // Internal interface between the C-ABI entry points (sa_api.cu) and the
 // kernel launchers (sa_perm.cu, sa_simt.cu, sa_tc.cu, sa_tc_ring.cu,
-// sa_tc_flash.cu).  Not installed.
+// sa_tc_chunk.cu).  Not installed.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,6 +41,10 @@ sa_status_t fail(sa_status_t st, const char* fmt, ...);
 // Device error word owned by the library (used when the caller passes NULL).
 int32_t* default_error_word();
 
+// Bound, in SM cycles, on every pipeline wait of the tcgen05 kernels
+// launched from now on (default ~2 s at the maximum clock; sa_set_wait_limit).
+long long wait_limit_cycles();
+
 // SIMT (CUDA-core) kernel: any window.  `path` selects SA, SWA or gated.
 sa_status_t launch_simt(const Problem& pb, Path path, cudaStream_t stream);
 
@@ -63,9 +68,14 @@ bool ring_supported(const Problem& pb, Path path);
 // tcgen05 kernel streaming each tile's key span through shared memory in
 // 128-key chunks with an online softmax: any window.  Same contract as
 // launch_tc.
-sa_status_t launch_flash(const Problem& pb, Path path, const float* gate, int accumulate,
+sa_status_t launch_chunk(const Problem& pb, Path path, const float* gate, int accumulate,
                          cudaStream_t stream);
-bool flash_supported(const Problem& pb, Path path);
+bool chunk_supported(const Problem& pb, Path path);
+
+// Tensor map of a row-major bf16 [rows, d] tensor for TMA copies of
+// 64-column x box_rows boxes with the 128-byte swizzle (false if the driver
+// entry point or the encoding fails).
+bool encode_row_map(CUtensorMap* m, const void* base, uint64_t rows, int d, int box_rows);
 
 // sigma^{-1} kernels.
 sa_status_t launch_inverse_perm(const int32_t* perm, int32_t* inv, int batch, int n,

@@ -191,7 +191,7 @@ __device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUte
     for (int s = 0; s < P.s_stages; ++s)
       if (issued[s]) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(bars.full(s), issued_par[s]) && clock64() - t0 < P.timeout_cycles) {
+        while (!mbar_try_wait(bars.full(s), issued_par[s]) && clock64() - t0 < kDrainCycles) {
         }
       }
   }
@@ -254,7 +254,7 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, co
   // All MMAs this thread issued complete before TMEM can be released.
   umma_commit(bars.drain());
   const long long t0 = clock64();
-  while (!mbar_try_wait(bars.drain(), 0) && clock64() - t0 < P.timeout_cycles) {
+  while (!mbar_try_wait(bars.drain(), 0) && clock64() - t0 < kDrainCycles) {
   }
 }
 
@@ -531,37 +531,10 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
   return false;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 // Row-gather view of a BSHD bf16 tensor: [rows, d] with 64-element boxes of
 // one row, 128-byte swizzle.
 static bool make_row_map(CUtensorMap* m, const void* base, uint64_t rows, int d) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(d) * 2};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_row_map(m, base, rows, d, 1);
 }
 
 template <int D, int NCH>
@@ -600,6 +573,37 @@ static cudaError_t launch_variant(int nch, int grid, uint32_t smem, cudaStream_t
 }
 
 }  // namespace tc
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_row_map(CUtensorMap* m, const void* base, uint64_t rows, int d, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(d) * 2};
+  const cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool tc_supported(const Problem& pb, Path path) {
   if (path != kPathSA && path != kPathSWA) return false;
@@ -652,7 +656,7 @@ sa_status_t launch_tc(const Problem& pb, Path path, const float* gate, int accum
   P.stage_bytes = c.stage_bytes;
   P.sig_off = c.sig_off;
   P.bar_off = c.bar_off;
-  P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock
+  P.timeout_cycles = wait_limit_cycles();
   const int grid = P.num_tiles < sms ? P.num_tiles : sms;
   const int nch = c.span_pad / 32 <= kMaxRegChunks ? c.span_pad / 32 : 0;
   cudaError_t ce;

@@ -32,7 +32,7 @@
 #include <cstring>
 
 namespace sa {
-namespace flash {
+namespace chunk {
 
 using namespace tcc;
 
@@ -381,7 +381,7 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   }
   umma_commit(bars + 8 * kDrain);
   const long long t0 = clock64();
-  while (!mbar_try_wait(bars + 8 * kDrain, 0) && clock64() - t0 < P.timeout_cycles) {
+  while (!mbar_try_wait(bars + 8 * kDrain, 0) && clock64() - t0 < kDrainCycles) {
   }
 }
 
@@ -624,7 +624,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) sa_flash_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kThreads, 1) sa_chunk_kernel(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
   // Align by pointer arithmetic on the shared array (not through an integer)
   // so the compiler keeps the shared address space.
@@ -744,37 +744,37 @@ static bool device_sm103(int* sms) {
 
 template <int D>
 static cudaError_t launch_one(int grid, uint32_t smem, cudaStream_t stream, const Params& P) {
-  cudaError_t ce = cudaFuncSetAttribute(sa_flash_kernel<D>,
+  cudaError_t ce = cudaFuncSetAttribute(sa_chunk_kernel<D>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (ce != cudaSuccess) return ce;
   cudaFuncAttributes fa;
-  ce = cudaFuncGetAttributes(&fa, sa_flash_kernel<D>);
+  ce = cudaFuncGetAttributes(&fa, sa_chunk_kernel<D>);
   if (ce != cudaSuccess) return ce;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;  // register split
   int resident = 0;
-  ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, sa_flash_kernel<D>, kThreads, smem);
+  ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, sa_chunk_kernel<D>, kThreads, smem);
   if (ce != cudaSuccess) return ce;
   if (resident < 1) return cudaErrorInvalidConfiguration;
-  sa_flash_kernel<D><<<grid, kThreads, smem, stream>>>(P);
+  sa_chunk_kernel<D><<<grid, kThreads, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
-}  // namespace flash
+}  // namespace chunk
 
-bool flash_supported(const Problem& pb, Path path) {
+bool chunk_supported(const Problem& pb, Path path) {
   if (path != kPathSA && path != kPathSWA) return false;
-  if (!flash::device_sm103(nullptr)) return false;
-  flash::Config c;
-  return flash::make_config(pb, path, c);
+  if (!chunk::device_sm103(nullptr)) return false;
+  chunk::Config c;
+  return chunk::make_config(pb, path, c);
 }
 
-sa_status_t launch_flash(const Problem& pb, Path path, const float* gate, int accumulate,
+sa_status_t launch_chunk(const Problem& pb, Path path, const float* gate, int accumulate,
                          cudaStream_t stream) {
-  using namespace flash;
+  using namespace chunk;
   int sms = 0;
   if (!device_sm103(&sms)) return fail(SA_ERR_UNSUPPORTED, "device is not sm_103");
   Config c;
-  if (!make_config(pb, path, c)) return fail(SA_ERR_UNSUPPORTED, "shape does not fit the flash kernel");
+  if (!make_config(pb, path, c)) return fail(SA_ERR_UNSUPPORTED, "shape does not fit the chunk kernel");
   Params P;
   std::memset(&P, 0, sizeof(P));
   P.q = static_cast<const __nv_bfloat16*>(pb.q);
@@ -809,11 +809,11 @@ sa_status_t launch_flash(const Problem& pb, Path path, const float* gate, int ac
   P.off_bits = c.off_bits;
   P.off_bar = c.off_bar;
   P.tmem_alloc = 512;  // S of the two halves (128 columns each), then their O
-  P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock
+  P.timeout_cycles = wait_limit_cycles();
   const int grid = P.num_tiles < sms ? P.num_tiles : sms;
   const cudaError_t ce = (pb.d == 128) ? launch_one<128>(grid, c.smem_bytes, stream, P)
                                        : launch_one<64>(grid, c.smem_bytes, stream, P);
-  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "flash kernel launch: %s", cudaGetErrorString(ce));
+  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "chunk kernel launch: %s", cudaGetErrorString(ce));
   return SA_OK;
 }
 

@@ -13,6 +13,10 @@ namespace sa {
 namespace tcc {
 
 constexpr int kBM = 128;  // MMA M: query rows per tile
+// Bound on the final wait for a CTA's own MMAs before TMEM is freed (~2 s at
+// the maximum SM clock).  Kept apart from the pipeline wait limit so that a
+// short limit never frees TMEM under MMAs still in flight.
+constexpr long long kDrainCycles = 4000000000LL;
 
 // ------------------------------------------------------------------ PTX
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -24,17 +28,22 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 
 // try_wait with a suspend-time hint: the thread sleeps in the instruction
-// until the phase completes or ~1 ms passes, instead of spinning.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// until the phase completes or about `hint_ns` nanoseconds pass, instead of
+// spinning.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  return mbar_try_wait_hint(bar, parity, 1000000u);
 }
 
 // Non-blocking test of the phase with the given parity.
@@ -150,13 +159,16 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 
 // Wait on `bar` for the phase of the given parity, for at most `limit`
 // SM cycles.  On expiry sets SA_ERRBIT_TIMEOUT in *err and the CTA's abort
-// flag; returns false then, or when another role has already aborted.
+// flag; returns false then, or when another role has already aborted.  Each
+// sleep in try_wait lasts at most ~limit/4 ns (1 ms at most), so a short
+// limit is honoured even while the phase never completes.
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, long long limit,
                                              int32_t* err, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint = limit >= 4000000LL ? 1000000u : uint32_t(limit > 4 ? limit >> 2 : 1);
+  if (mbar_try_wait_hint(bar, parity, hint)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;

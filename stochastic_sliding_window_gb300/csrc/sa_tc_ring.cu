@@ -479,7 +479,7 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   }
   umma_commit(bars + 8 * kDrain);
   const long long t0 = clock64();
-  while (!mbar_try_wait(bars + 8 * kDrain, 0) && clock64() - t0 < P.timeout_cycles) {
+  while (!mbar_try_wait(bars + 8 * kDrain, 0) && clock64() - t0 < kDrainCycles) {
   }
 }
 
@@ -897,7 +897,7 @@ sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int acc
   P.off_vtok = c.off_vtok;
   P.off_bits = c.off_bits;
   P.off_bar = c.off_bar;
-  P.timeout_cycles = 4000000000LL;  // ~2 s at the maximum SM clock
+  P.timeout_cycles = wait_limit_cycles();
   const int grid = P.num_tiles < sms ? P.num_tiles : sms;
   const int nch = c.span_pad / 32;
   const cudaError_t ce = (pb.d == 128) ? launch_variant<128>(nch, grid, c.smem_bytes, stream, P)

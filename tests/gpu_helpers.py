@@ -14,8 +14,8 @@ MAX_ABS = 2e-2
 REL_L2 = 5e-3
 
 KERNELS = [sa.KERNEL_SIMT, sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING,
-           sa.KERNEL_TCGEN05_FLASH]
-KERNEL_IDS = ["simt", "gather", "ring", "flash"]
+           sa.KERNEL_TCGEN05_CHUNK]
+KERNEL_IDS = ["simt", "gather", "ring", "chunk"]
 
 
 def span(path: str, g: int, w: int) -> int:
@@ -43,13 +43,13 @@ def _ring_fits(sp: int, g: int, d: int) -> bool:
 
 def must_support(kernel: int, path: str, g: int, w: int, w_swa: int = 0, d: int = 128) -> bool:
     """Shapes each tcgen05 variant is required to accept (the ring kernel
-    exactly; the flash kernel any window; the gather kernel at least up to
+    exactly; the chunk kernel any window; the gather kernel at least up to
     256-key windows)."""
     if kernel == sa.KERNEL_SIMT:
         return True
     if 128 % g:
         return False
-    if kernel == sa.KERNEL_TCGEN05_FLASH:
+    if kernel == sa.KERNEL_TCGEN05_CHUNK:
         return d in (64, 128) and g <= 32
     paths = [("sa", w), ("swa", w_swa or w)] if path == "gated" else [(path, w)]
     if kernel == sa.KERNEL_TCGEN05_RING:
@@ -60,7 +60,7 @@ def must_support(kernel: int, path: str, g: int, w: int, w_swa: int = 0, d: int 
 def kernel_ran(requested: int) -> bool:
     got = sa.last_kernel()
     if requested == sa.KERNEL_TCGEN05:
-        return got in (sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING, sa.KERNEL_TCGEN05_FLASH)
+        return got in (sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING, sa.KERNEL_TCGEN05_CHUNK)
     return got == requested
 
 

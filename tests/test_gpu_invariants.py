@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import stochastic_sliding_window_gb300 as sa
-from gpu_helpers import KERNEL_IDS, KERNELS, Inputs, compare, dev_bf16, must_support, perms
+from gpu_helpers import (KERNEL_IDS, KERNELS, Inputs, compare, dev_bf16, gather_rows,
+                         must_support, perms, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -99,10 +100,10 @@ def test_tensor_core_and_simt_kernels_agree():
                           kernel=sa.KERNEL_TCGEN05_GATHER)
         assert torch.equal(a, b)
     for w in (32, 128):
-        # the flash kernel streams the same windows in chunks (online softmax)
+        # the chunk kernel streams the same windows in chunks (online softmax)
         a = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_TCGEN05_RING)
         b = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
-                          kernel=sa.KERNEL_TCGEN05_FLASH)
+                          kernel=sa.KERNEL_TCGEN05_CHUNK)
         assert (a.float() - b.float()).abs().max().item() <= 2e-2
     for w in (32, 128, 256):
         a = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_TCGEN05)
@@ -122,11 +123,11 @@ def test_auto_kernel_choice():
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 128)
     assert sa.last_kernel() == sa.KERNEL_TCGEN05_RING and sa.last_launch_count() == 1
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 256)
-    assert sa.last_kernel() == sa.KERNEL_TCGEN05_FLASH
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_CHUNK
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2048)
-    assert sa.last_kernel() == sa.KERNEL_TCGEN05_FLASH
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_CHUNK
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 2048, kernel=sa.KERNEL_TCGEN05)
-    assert sa.last_kernel() == sa.KERNEL_TCGEN05_FLASH
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_CHUNK
     sa.sa_forward(inp.q, inp.k, inp.v, perm_d, 256, kernel=sa.KERNEL_TCGEN05_GATHER)
     assert sa.last_kernel() == sa.KERNEL_TCGEN05_GATHER
     for k in (sa.KERNEL_TCGEN05_GATHER, sa.KERNEL_TCGEN05_RING):
@@ -213,3 +214,48 @@ def test_writes_stay_inside_out(kernel, path):
     assert sa.check_error(err) == sa.SA_OK
     assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + numel:]).all()
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------ bounded waits
+
+TC_KERNELS = [sa.KERNEL_TCGEN05_RING, sa.KERNEL_TCGEN05_CHUNK, sa.KERNEL_TCGEN05_GATHER]
+
+
+@pytest.mark.parametrize("kernel", TC_KERNELS, ids=["ring", "chunk", "gather"])
+@pytest.mark.parametrize("path", ["sa", "gated"])
+def test_short_wait_bound_gives_up_cleanly(kernel, path):
+    """A 200-cycle bound on every pipeline wait is far shorter than the first
+    wait for data from memory, so the call must give up: the kernel returns,
+    the error word reports SA_ERR_TIMEOUT, and the next call on the same
+    context (default bound) is correct."""
+    n, w = 2048, 64
+    inp = Inputs(1, n, 32, 8, 128, seed=19, gates=True)
+    perm, perm_d = perms(19, 0, 1, n)
+
+    def run(err):
+        if path == "sa":
+            return sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=kernel,
+                                 err=err)
+        return sa.sa_swa_gated_forward(inp.q, inp.k, inp.v, perm_d, inp.ga, inp.gw, w,
+                                       causal=True, kernel=kernel, err=err)
+
+    for attempt in range(2):
+        err = _err()
+        try:
+            sa.set_wait_limit(200)
+            run(err)
+            status = sa.check_error(err)  # synchronises: every CTA has returned
+        finally:
+            sa.set_wait_limit(0)
+        assert status == sa.SA_ERR_TIMEOUT, (attempt, status)
+        assert int(err.item()) & sa.ERRBIT_TIMEOUT
+        assert not int(err.item()) & sa.ERRBIT_INTERNAL
+        err2 = _err()
+        y = run(err2)
+        assert sa.check_error(err2) == sa.SA_OK
+        rows = sample_rows(1, n, 96, seed=attempt)
+        want = (oracle.sa_rows(inp.case.q, inp.case.k, inp.case.v, perm, w, True, rows=rows)
+                if path == "sa" else
+                oracle.gated_rows(inp.case.q, inp.case.k, inp.case.v, perm, inp.case.gate_sa,
+                                  inp.case.gate_swa, w, None, True, rows=rows))
+        compare(gather_rows(y, rows), want, f"after timeout, {path}")

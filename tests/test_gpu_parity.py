@@ -136,14 +136,14 @@ def test_long_prefill_gqa_causal_sa(long_prefill, w):
     err = _err()
     y = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, err=err)
     assert sa.check_error(err) == sa.SA_OK
-    assert sa.last_kernel() == (sa.KERNEL_TCGEN05_RING if w <= 128 else sa.KERNEL_TCGEN05_FLASH)
+    assert sa.last_kernel() == (sa.KERNEL_TCGEN05_RING if w <= 128 else sa.KERNEL_TCGEN05_CHUNK)
     want = oracle.sa_rows(inp.case.q, inp.case.k, inp.case.v, perm, w, True, rows=rows)
     compare(gather_rows(y, rows), want, f"c3 w={w}")
     # the chunked online-softmax kernel on the same rows
     yf = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
-                       kernel=sa.KERNEL_TCGEN05_FLASH, err=err)
+                       kernel=sa.KERNEL_TCGEN05_CHUNK, err=err)
     assert sa.check_error(err) == sa.SA_OK
-    compare(gather_rows(yf, rows), want, f"c3 flash w={w}")
+    compare(gather_rows(yf, rows), want, f"c3 chunk w={w}")
     # the gather kernel computes the same MMAs and softmax: identical bits
     yg = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
                        kernel=sa.KERNEL_TCGEN05_GATHER, err=err)
@@ -166,15 +166,17 @@ def test_very_long_context_gated(w):
     err = _err()
     y = sa.sa_swa_gated_forward(inp.q, inp.k, inp.v, perm_d, inp.ga, inp.gw, w, causal=True, err=err)
     assert sa.check_error(err) == sa.SA_OK
-    assert sa.last_kernel() == sa.KERNEL_TCGEN05_FLASH and sa.last_launch_count() == 2
+    assert sa.last_kernel() == sa.KERNEL_TCGEN05_CHUNK and sa.last_launch_count() == 2
     compare(gather_rows(y, rows), _want("gated", inp, perm, w, True, rows=rows), f"c4 w={w}")
 
 
 # ------------------------------------------------------------ length sweep
 
-@pytest.mark.parametrize("n", [2048, 8192, 262144])
+@pytest.mark.parametrize("n", [2048, 8192, 32768, 131072, 262144])
 def test_length_sweep_causal_sa(n):
-    layers = 8 if n <= 8192 else 1
+    """Every length of the sweep, each layer with its own sigma and inputs:
+    all 8 layers up to n = 8192, two independent layers beyond."""
+    layers = 8 if n <= 8192 else 2
     for layer in range(layers):
         inp = Inputs(1, n, 16, 16, 128, seed=1000 * layer + n, gates=False)
         perm, perm_d = perms(41, layer, 1, n)
@@ -189,7 +191,7 @@ def test_length_sweep_causal_sa(n):
 # ------------------------------------------------------------ online-softmax corrections
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_flash_kernel_rescales_when_scores_grow_across_chunks(causal):
+def test_chunk_kernel_rescales_when_scores_grow_across_chunks(causal):
     """With sigma = identity and key scores rising along the sequence (by 256
     per 128 keys, i.e. ~33 in the kernel's base-2 units), every later 128-key
     chunk's maximum exceeds the running reference by far more than 2^8, so the
@@ -210,12 +212,12 @@ def test_flash_kernel_rescales_when_scores_grow_across_chunks(causal):
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
     err = _err()
     y = sa.sa_forward(dev(q), dev(k), dev(v), perm_d, w, causal=causal,
-                      kernel=sa.KERNEL_TCGEN05_FLASH, err=err)
+                      kernel=sa.KERNEL_TCGEN05_CHUNK, err=err)
     assert sa.check_error(err) == sa.SA_OK
     rows = sample_rows(b, n, 200, seed=5)
     want = oracle.sa_rows(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64),
                           ident, w, causal, rows=rows)
-    compare(gather_rows(y, rows), want, f"flash rescale causal={causal}")
+    compare(gather_rows(y, rows), want, f"chunk rescale causal={causal}")
     ys = sa.sa_forward(dev(q), dev(k), dev(v), perm_d, w, causal=causal, kernel=sa.KERNEL_SIMT,
                        err=err)
     assert (y.float() - ys.float()).abs().max().item() <= 2e-2
