@@ -43,6 +43,7 @@ from .attention import (
 )
 from .backward import (
     sa_backward,
+    sa_dq_rows,
     swa_backward,
     gated_backward,
     sa_lse,
@@ -74,6 +75,7 @@ __all__ = [
     "full_attention",
     "masked_attention",
     "sa_backward",
+    "sa_dq_rows",
     "swa_backward",
     "gated_backward",
     "sa_lse",

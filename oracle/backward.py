@@ -80,6 +80,30 @@ def sa_backward(q, k, v, perm, dy, window: int, causal: bool, scale: float | Non
                      lambda b, i: neighbours_sa(perm[b], window, causal, i, invs[b]), scale)
 
 
+def sa_dq_rows(q, k, v, perm, dy, window: int, causal: bool, rows, scale: float | None = None):
+    """dQ rows [R, Hq, d] of SA for the (b, i) pairs in ``rows`` only: a
+    query row's gradient depends on its own window alone, so large cases can
+    be checked on a sample (same per-token chain rule as ``sa_backward``)."""
+    q, k, v, dy = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dy)
+    _check(q, k, v)
+    bsz, n, hq, d = q.shape
+    perm = np.asarray(perm, dtype=np.int64).reshape(bsz, n)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    hm = _head_map(hq, k.shape[2])
+    invs, out = {}, []
+    for b, i in rows:
+        b, i = int(b), int(i)
+        if b not in invs:
+            invs[b] = inverse_perm(perm[b])
+        keys = neighbours_sa(perm[b], window, causal, i, invs[b])
+        dq = np.empty((hq, d))
+        dk_sink = np.zeros_like(k[b])
+        dv_sink = np.zeros_like(v[b])
+        _row_backward(q[b, i], k[b], v[b], keys, hm, scale, dy[b, i], dq, dk_sink, dv_sink)
+        out.append(dq)
+    return np.asarray(out).reshape(-1, hq, d)
+
+
 def swa_backward(q, k, v, dy, window: int, scale: float | None = None):
     """(dQ, dK, dV) of SWA over keys [max(0, i-w+1), i] ("Problem statement")."""
     n = np.shape(q)[1]

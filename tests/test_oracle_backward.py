@@ -142,6 +142,15 @@ def test_key_gradients_sum_to_zero_and_value_gradients_to_dy(causal):
     np.testing.assert_allclose(dv.sum(axis=1), want, rtol=1e-12, atol=1e-12)
 
 
+def test_sampled_dq_rows_equal_the_full_gradient():
+    q, k, v, dy, _, _, perm = _case(b=2, n=16, seed=13)
+    dq, _, _ = oracle.sa_backward(q, k, v, perm, dy, 6, True)
+    rows = [(0, 0), (1, 15), (1, 3), (0, 9)]
+    got = oracle.sa_dq_rows(q, k, v, perm, dy, 6, True, rows)
+    for r, (b, i) in enumerate(rows):
+        np.testing.assert_array_equal(got[r], dq[b, i])
+
+
 def test_identity_sigma_causal_sa_gradients_equal_swa():
     q, k, v, dy, _, _, _ = _case(b=1, n=14, seed=5)
     ident = np.arange(14)[None]
