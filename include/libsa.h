@@ -132,6 +132,51 @@ sa_status_t sa_swa_gated_forward(const sa_params_t* params, const void* q, const
 size_t sa_gated_workspace_size(const sa_params_t* params);
 
 /*
+ * Backward pass.  The summary pretrains a model from scratch with the gated
+ * SA + SWA pair ("Main contributions", item 3; "Results", first bullet),
+ * which needs the gradients of each path's output; they follow from the
+ * forward definitions above by the chain rule.  Given the upstream gradient
+ * dout (bf16 [B, n, Hq, d], the gradient of the loss with respect to out),
+ * a call writes
+ *   dq bf16 [B, n, Hq, d],  dk, dv bf16 [B, n, Hkv, d]
+ * (the kv-head gradients summed over the query heads that read them) and,
+ * for the gated call, the gate-logit gradients dgate_* fp32 [B, n, Hq]
+ * (NULL skips one).  Softmax normalisers are recomputed from q and k; the
+ * forward outputs are not needed.  Every row of dq, dk, dv is written.
+ * Layouts and pointer rules as for the forward calls; outputs must not alias
+ * inputs or each other.  Caller-owned device workspace of at least the
+ * *_workspace_size bytes, 256-byte aligned, contents ignored on entry.
+ * Supported: head_dim 64 or 128, Hq/Hkv dividing 128, and a key span of at
+ * most 256 per 128-row tile (128/g + 2*floor(w/2) keys for SA, 128/g + w - 1
+ * for SWA); else SA_ERR_UNSUPPORTED.  params->kernel must be SA_KERNEL_AUTO
+ * or SA_KERNEL_TCGEN05.  Asynchronous on `stream` (2 kernel launches per
+ * path; 7 for the gated call).
+ */
+sa_status_t sa_backward(const sa_params_t* params, const void* q, const void* k, const void* v,
+                        const int32_t* perm, const void* dout, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+sa_status_t swa_backward(const sa_params_t* params, const void* q, const void* k, const void* v,
+                         const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+/* Workspace of sa_backward / swa_backward: two fp32 values per (token, query head). */
+size_t sa_backward_workspace_size(const sa_params_t* params);
+
+/*
+ * Gradients of the gated dual path ("Gated SA and SWA" equation).  The
+ * gate-logit gradient of a row is g (1 - g) <dout, Y_path> with g its
+ * sigmoid.  The two paths' dq, dk, dv are summed in fp32 in the workspace and
+ * rounded to bf16 once.
+ */
+sa_status_t sa_swa_gated_backward(const sa_params_t* params, const void* q, const void* k,
+                                  const void* v, const int32_t* perm,
+                                  const float* gate_sa_logits, const float* gate_swa_logits,
+                                  const void* dout, void* dq, void* dk, void* dv, float* dgate_sa,
+                                  float* dgate_swa, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+/* Workspace of sa_swa_gated_backward: the above plus fp32 dq, dk and dv. */
+size_t sa_swa_gated_backward_workspace_size(const sa_params_t* params);
+
+/*
  * sigma^{-1} ("Core mechanism" step 3; "Theoretical properties": an O(n)
  * index operation): inv[b, perm[b, p]] = p for every sequence b.  perm and
  * inv are device int32 [batch, n] and must not overlap.  Entries of perm
@@ -195,8 +240,9 @@ const char* sa_last_error_message(void);
  * this thread launched (0 before any; for the gated path, the SA pass's). */
 int32_t sa_last_kernel(void);
 
-/* Number of kernel launches the last successful forward call on this thread
- * made (1 for SA/SWA, 2 for the gated path). */
+/* Number of kernel launches the last successful forward or backward call on
+ * this thread made (forward: 1 for SA/SWA, 2 for the gated path; backward:
+ * 2 per path, 7 for the gated call). */
 int32_t sa_last_launch_count(void);
 
 #ifdef __cplusplus

@@ -35,10 +35,13 @@ from ._libsa import (
     load,
     make_perm,
     make_perms,
+    sa_backward,
     sa_forward,
     sa_inverse_perm,
+    sa_swa_gated_backward,
     sa_swa_gated_forward,
     set_wait_limit,
+    swa_backward,
     swa_forward,
 )
 
@@ -48,4 +51,5 @@ __all__ = [
     "SA_OK", "SIGNATURES", "SaError", "SaParams", "check_error", "clear_error", "last_kernel",
     "last_launch_count", "load", "make_perm", "make_perms", "sa_forward", "sa_inverse_perm",
     "sa_swa_gated_forward", "set_wait_limit", "get_wait_limit", "swa_forward",
+    "sa_backward", "swa_backward", "sa_swa_gated_backward",
 ]

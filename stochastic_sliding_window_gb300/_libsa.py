@@ -30,6 +30,11 @@ SIGNATURES = {
     "sa_swa_gated_forward": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "sa_gated_workspace_size": (c_size_t, [c_void_p]),
+    "sa_backward": (c_int32, [c_void_p] * 10 + [c_size_t, c_void_p]),
+    "swa_backward": (c_int32, [c_void_p] * 9 + [c_size_t, c_void_p]),
+    "sa_backward_workspace_size": (c_size_t, [c_void_p]),
+    "sa_swa_gated_backward": (c_int32, [c_void_p] * 14 + [c_size_t, c_void_p]),
+    "sa_swa_gated_backward_workspace_size": (c_size_t, [c_void_p]),
     "sa_inverse_perm": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
     "sa_make_perm": (c_int32, [c_uint64, c_int32, c_int32, c_int32, POINTER(c_int32)]),
     "sa_check_error": (c_int32, [c_void_p, c_void_p]),
@@ -214,6 +219,89 @@ def sa_swa_gated_forward(q, k, v, perm, gate_sa, gate_swa, window: int, window_s
                                         work.data_ptr() if work is not None else None, ws,
                                         _stream(q, stream)))
     return out
+
+
+def _grads(q, k, dq, dk, dv):
+    import torch
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, k)):
+        _need(t, name, torch.bfloat16, 4)
+        _shape(t, name, like.shape)
+    return dq, dk, dv
+
+
+def _workspace(nbytes, device):
+    import torch
+    # 256-byte aligned: torch's caching allocator returns at least 512-byte
+    # aligned blocks
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def sa_backward(q, k, v, perm, dout, window: int, causal: bool = True, softmax_scale: float = 0.0,
+                dq=None, dk=None, dv=None, err=None, stream=None):
+    """Gradients (dq, dk, dv) of sa_forward for the upstream gradient dout."""
+    import torch
+    _validate(q, k, v, dout, perm=perm, err=err)
+    dq, dk, dv = _grads(q, k, dq, dk, dv)
+    _on_device(q, "q", [("dq", dq), ("dk", dk), ("dv", dv)])
+    prm = _params(q, k, window, 0, causal, softmax_scale, KERNEL_AUTO, err)
+    lib = load()
+    with torch.cuda.device(q.device):
+        ws = lib.sa_backward_workspace_size(byref(prm))
+        work = _workspace(ws, q.device)
+        _check(lib.sa_backward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                               perm.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), work.data_ptr(), ws, _stream(q, stream)))
+    return dq, dk, dv
+
+
+def swa_backward(q, k, v, dout, window: int, softmax_scale: float = 0.0, dq=None, dk=None,
+                 dv=None, err=None, stream=None):
+    """Gradients (dq, dk, dv) of swa_forward for the upstream gradient dout."""
+    import torch
+    _validate(q, k, v, dout, err=err)
+    dq, dk, dv = _grads(q, k, dq, dk, dv)
+    _on_device(q, "q", [("dq", dq), ("dk", dk), ("dv", dv)])
+    prm = _params(q, k, window, 0, True, softmax_scale, KERNEL_AUTO, err)
+    lib = load()
+    with torch.cuda.device(q.device):
+        ws = lib.sa_backward_workspace_size(byref(prm))
+        work = _workspace(ws, q.device)
+        _check(lib.swa_backward(byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                work.data_ptr(), ws, _stream(q, stream)))
+    return dq, dk, dv
+
+
+def sa_swa_gated_backward(q, k, v, perm, gate_sa, gate_swa, dout, window: int,
+                          window_swa: int = 0, causal: bool = True, softmax_scale: float = 0.0,
+                          dq=None, dk=None, dv=None, dgate_sa=None, dgate_swa=None, err=None,
+                          stream=None):
+    """Gradients (dq, dk, dv, dgate_sa, dgate_swa) of sa_swa_gated_forward."""
+    import torch
+    _validate(q, k, v, dout, perm=perm, gates=(("gate_sa", gate_sa), ("gate_swa", gate_swa)),
+              err=err)
+    dq, dk, dv = _grads(q, k, dq, dk, dv)
+    dgate_sa = torch.empty_like(gate_sa) if dgate_sa is None else dgate_sa
+    dgate_swa = torch.empty_like(gate_swa) if dgate_swa is None else dgate_swa
+    for name, t in (("dgate_sa", dgate_sa), ("dgate_swa", dgate_swa)):
+        _need(t, name, torch.float32, 3)
+        _shape(t, name, gate_sa.shape)
+    _on_device(q, "q", [("dq", dq), ("dk", dk), ("dv", dv), ("dgate_sa", dgate_sa),
+                        ("dgate_swa", dgate_swa)])
+    prm = _params(q, k, window, window_swa, causal, softmax_scale, KERNEL_AUTO, err)
+    lib = load()
+    with torch.cuda.device(q.device):
+        ws = lib.sa_swa_gated_backward_workspace_size(byref(prm))
+        work = _workspace(ws, q.device)
+        _check(lib.sa_swa_gated_backward(
+            byref(prm), q.data_ptr(), k.data_ptr(), v.data_ptr(), perm.data_ptr(),
+            gate_sa.data_ptr(), gate_swa.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+            dk.data_ptr(), dv.data_ptr(), dgate_sa.data_ptr(), dgate_swa.data_ptr(),
+            work.data_ptr(), ws, _stream(q, stream)))
+    return dq, dk, dv, dgate_sa, dgate_swa
 
 
 def sa_inverse_perm(perm, inv=None, err=None, stream=None):

@@ -90,6 +90,14 @@ static Problem make_problem(const sa_params_t* prm, const void* q, const void* k
   return pb;
 }
 
+static sa_status_t finish_bwd(sa_status_t st, int32_t launches) {
+  if (st == SA_OK) {
+    g_last_launches = launches;
+    g_msg[0] = '\0';
+  }
+  return st;
+}
+
 static sa_status_t finish(sa_status_t st, int32_t kernel, int32_t launches) {
   if (st == SA_OK) {
     g_last_kernel = kernel;
@@ -196,6 +204,150 @@ extern "C" sa_status_t sa_swa_gated_forward(const sa_params_t* params, const voi
     return finish(launch_kernel(k_sa, pb, kPathSA, pb.gate_sa, 1, stream), k_sa, 2);
   }
   return finish(launch_simt(pb, kPathGated, stream), SA_KERNEL_SIMT, 1);
+}
+
+// ------------------------------------------------------------------ backward
+
+namespace sa {
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of one backward path: the rows' log2 normaliser and D (fp32).
+static size_t rows_bytes(const sa_params_t* p) {
+  return align256(size_t(p->batch) * p->seqlen * p->num_q_heads * sizeof(float));
+}
+
+static size_t gated_bwd_bytes(const sa_params_t* p) {
+  const size_t tok = size_t(p->batch) * p->seqlen * p->head_dim;
+  return 2 * rows_bytes(p) + align256(tok * p->num_q_heads * 4) +
+         2 * align256(tok * p->num_kv_heads * 4);
+}
+
+static sa_status_t check_bwd(const sa_params_t* prm, const void* dout, const void* dq,
+                             const void* dk, const void* dv, const void* q, const void* k,
+                             const void* v, void* ws, size_t ws_bytes, size_t need) {
+  if (!dout || !dq || !dk || !dv) return fail(SA_ERR_INVALID_ARG, "dout, dq, dk and dv must be non-NULL");
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(SA_ERR_INVALID_ARG, "dout, dq, dk and dv must be 16-byte aligned");
+  const void* outs[3] = {dq, dk, dv};
+  const void* ins[4] = {q, k, v, dout};
+  for (const void* o : outs)
+    for (const void* i : ins)
+      if (o == i) return fail(SA_ERR_INVALID_ARG, "a gradient output aliases an input");
+  if (dq == dk || dq == dv || dk == dv) return fail(SA_ERR_INVALID_ARG, "dq, dk and dv must differ");
+  if (ws_bytes < need || ws == nullptr)
+    return fail(SA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(SA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (prm->kernel != SA_KERNEL_AUTO && prm->kernel != SA_KERNEL_TCGEN05)
+    return fail(SA_ERR_UNSUPPORTED, "the backward pass runs on its tcgen05 kernels only");
+  return SA_OK;
+}
+
+static sa_status_t run_bwd_single(const sa_params_t* params, const void* q, const void* k,
+                                  const void* v, const int32_t* perm, const void* dout, void* dq,
+                                  void* dk, void* dv, void* ws, size_t ws_bytes, Path path,
+                                  cudaStream_t stream) {
+  sa_status_t st = check_params(params, true);
+  if (st != SA_OK) return st;
+  if ((st = check_ptrs(q, k, v, dq)) != SA_OK) return st;
+  if (path == kPathSA && perm == nullptr) return fail(SA_ERR_INVALID_ARG, "perm must be non-NULL");
+  const size_t rb = rows_bytes(params);
+  if ((st = check_bwd(params, dout, dq, dk, dv, q, k, v, ws, ws_bytes, 2 * rb)) != SA_OK) return st;
+  Problem pb = make_problem(params, q, k, v, perm, dq);
+  if (path == kPathSWA) pb.window_swa = params->window;
+  if (pb.err == nullptr) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  if (!bwd_supported(pb, path))
+    return fail(SA_ERR_UNSUPPORTED, "the backward kernels need d in {64, 128}, Hq/Hkv dividing 128, "
+                "a key span of at most 256 per 128-row tile, and an sm_103 device");
+  BwdArgs a{};
+  a.dout = dout;
+  a.lse2 = static_cast<float*>(ws);
+  a.dsum = reinterpret_cast<float*>(static_cast<char*>(ws) + rb);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.out_mode = 0;
+  return finish_bwd(launch_bwd(pb, path, a, stream), 2);
+}
+
+}  // namespace sa
+
+extern "C" size_t sa_backward_workspace_size(const sa_params_t* params) {
+  if (params == nullptr || params->batch < 1 || params->seqlen < 1 || params->num_q_heads < 1)
+    return 0;
+  return 2 * rows_bytes(params);
+}
+
+extern "C" size_t sa_swa_gated_backward_workspace_size(const sa_params_t* params) {
+  if (params == nullptr || params->batch < 1 || params->seqlen < 1 || params->num_q_heads < 1 ||
+      params->num_kv_heads < 1 || params->head_dim < 1)
+    return 0;
+  return gated_bwd_bytes(params);
+}
+
+extern "C" sa_status_t sa_backward(const sa_params_t* params, const void* q, const void* k,
+                                   const void* v, const int32_t* perm, const void* dout, void* dq,
+                                   void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  return run_bwd_single(params, q, k, v, perm, dout, dq, dk, dv, workspace, workspace_bytes,
+                        kPathSA, stream);
+}
+
+extern "C" sa_status_t swa_backward(const sa_params_t* params, const void* q, const void* k,
+                                    const void* v, const void* dout, void* dq, void* dk, void* dv,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return run_bwd_single(params, q, k, v, nullptr, dout, dq, dk, dv, workspace, workspace_bytes,
+                        kPathSWA, stream);
+}
+
+extern "C" sa_status_t sa_swa_gated_backward(const sa_params_t* params, const void* q,
+                                             const void* k, const void* v, const int32_t* perm,
+                                             const float* gate_sa_logits,
+                                             const float* gate_swa_logits, const void* dout,
+                                             void* dq, void* dk, void* dv, float* dgate_sa,
+                                             float* dgate_swa, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream) {
+  sa_status_t st = check_params(params, true);
+  if (st != SA_OK) return st;
+  if ((st = check_ptrs(q, k, v, dq)) != SA_OK) return st;
+  if (!perm || !gate_sa_logits || !gate_swa_logits)
+    return fail(SA_ERR_INVALID_ARG, "perm and both gate logit arrays must be non-NULL");
+  const size_t need = gated_bwd_bytes(params);
+  if ((st = check_bwd(params, dout, dq, dk, dv, q, k, v, workspace, workspace_bytes, need)) != SA_OK)
+    return st;
+  Problem pb = make_problem(params, q, k, v, perm, dq);
+  if (pb.err == nullptr) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  if (!bwd_supported(pb, kPathSA) || !bwd_supported(pb, kPathSWA))
+    return fail(SA_ERR_UNSUPPORTED, "the backward kernels need d in {64, 128}, Hq/Hkv dividing 128, "
+                "a key span of at most 256 per 128-row tile, and an sm_103 device");
+  const size_t rb = rows_bytes(params);
+  const size_t tok = size_t(params->batch) * params->seqlen * params->head_dim;
+  char* w = static_cast<char*>(workspace);
+  float* dq32 = reinterpret_cast<float*>(w + 2 * rb);
+  float* dk32 = reinterpret_cast<float*>(w + 2 * rb + align256(tok * params->num_q_heads * 4));
+  float* dv32 = reinterpret_cast<float*>(reinterpret_cast<char*>(dk32) +
+                                         align256(tok * params->num_kv_heads * 4));
+  BwdArgs a{};
+  a.dout = dout;
+  a.lse2 = reinterpret_cast<float*>(w);
+  a.dsum = reinterpret_cast<float*>(w + rb);
+  a.dq = dq32;
+  a.dk = dk32;
+  a.dv = dv32;
+  // SA path with its gate: stores; SWA path with its gate: adds.
+  a.gate = gate_sa_logits;
+  a.dgate = dgate_sa;
+  a.out_mode = 1;
+  if ((st = launch_bwd(pb, kPathSA, a, stream)) != SA_OK) return st;
+  a.gate = gate_swa_logits;
+  a.dgate = dgate_swa;
+  a.out_mode = 2;
+  if ((st = launch_bwd(pb, kPathSWA, a, stream)) != SA_OK) return st;
+  if ((st = launch_to_bf16(dq32, dq, tok * params->num_q_heads, stream)) != SA_OK) return st;
+  if ((st = launch_to_bf16(dk32, dk, tok * params->num_kv_heads, stream)) != SA_OK) return st;
+  if ((st = launch_to_bf16(dv32, dv, tok * params->num_kv_heads, stream)) != SA_OK) return st;
+  return finish_bwd(SA_OK, 7);
 }
 
 extern "C" sa_status_t sa_inverse_perm(const int32_t* perm, int32_t* inv, int32_t batch,

@@ -77,6 +77,26 @@ bool chunk_supported(const Problem& pb, Path path);
 // entry point or the encoding fails).
 bool encode_row_map(CUtensorMap* m, const void* base, uint64_t rows, int d, int box_rows);
 
+// Backward pass (sa_bwd.cu).  One path (SA or SWA) per call: the dQ kernel
+// over query tiles (writes the rows' log2 normaliser and D, and the
+// gate-logit gradient when a gate is given), then the dK/dV kernel over
+// 128-key tiles.  out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 add.
+struct BwdArgs {
+  const void* dout;    // bf16 [B, n, Hq, d]
+  const float* gate;   // [B, n, Hq] logits or nullptr
+  float* lse2;         // [B, n, Hq] workspace
+  float* dsum;         // [B, n, Hq] workspace
+  float* dgate;        // [B, n, Hq] or nullptr
+  void* dq;            // [B, n, Hq, d]
+  void* dk;            // [B, n, Hkv, d]
+  void* dv;
+  int out_mode;
+};
+bool bwd_supported(const Problem& pb, Path path);
+sa_status_t launch_bwd(const Problem& pb, Path path, const BwdArgs& a, cudaStream_t stream);
+// fp32 -> bf16 conversion of `count` values (a multiple of 4).
+sa_status_t launch_to_bf16(const float* src, void* dst, size_t count, cudaStream_t stream);
+
 // sigma^{-1} kernels.
 sa_status_t launch_inverse_perm(const int32_t* perm, int32_t* inv, int batch, int n,
                                 int32_t* err, cudaStream_t stream);
