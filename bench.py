@@ -95,12 +95,27 @@ def algorithmic(wl) -> tuple[int, float]:
     return bytes_alg, flops
 
 
-def metric_of(wl) -> str:
-    if wl is WORKLOAD:
+def algorithmic_bwd(wl) -> tuple[int, float]:
+    """Backward pass: bytes it must move (Q, K, V, dY and sigma read once;
+    dQ, dK, dV written once; the gate logits read and their gradients written
+    when gated) and FLOPs it must do (QK^T, dY V^T, dS K, dS^T Q, P^T dY:
+    2d each per attended pair; the recomputation of S and dP by the key-tile
+    kernel is implementation overhead, not counted)."""
+    b, n, hq, hkv, d = wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"], wl["head_dim"]
+    bytes_alg = 2 * b * n * d * (2 * hq + 2 * hkv) + 2 * b * n * d * (hq + 2 * hkv) + 4 * b * n
+    pairs = causal_sa_pairs(n, wl["window"])
+    if wl["path"] == "gated":
+        bytes_alg += 4 * 4 * b * n * hq
+        pairs += swa_pairs(n, wl["window"])
+    return bytes_alg, 10.0 * d * hq * b * pairs
+
+
+def metric_of(wl, bwd: bool = False) -> str:
+    if wl is WORKLOAD and not bwd:
         return METRIC
     what = "gated SA+SWA" if wl["path"] == "gated" else "SA"
-    return (f"{what} fwd tokens/s and % roofline (bf16, n={wl['seq_len']}, w={wl['window']}, "
-            f"{wl['num_q_heads']}q/{wl['num_kv_heads']}kv, d={wl['head_dim']})")
+    return (f"{what} {'bwd' if bwd else 'fwd'} tokens/s and % roofline (bf16, n={wl['seq_len']}, "
+            f"w={wl['window']}, {wl['num_q_heads']}q/{wl['num_kv_heads']}kv, d={wl['head_dim']})")
 
 
 def load_peaks() -> dict:
@@ -140,6 +155,10 @@ def profiled_traffic() -> int | None:
 
 def _oracle_rows(rows):
     import oracle
+    if _G.get("bwd"):
+        oracle.sa_dq_rows(_G["q"], _G["k"], _G["v"], _G["perm"], _G["dy"], _G["window"],
+                          _G["causal"], rows)
+        return
     if _G["path"] == "gated":
         oracle.gated_rows(_G["q"], _G["k"], _G["v"], _G["perm"], _G["ga"], _G["gw"], _G["window"],
                           None, _G["causal"], rows=rows)
@@ -152,10 +171,12 @@ def _oracle_chunk(rows):
     return len(rows)
 
 
-def publish_oracle_inputs(case, perm, wl):
-    """Make the inputs visible to oracle workers forked after this call."""
+def publish_oracle_inputs(case, perm, wl, dy=None):
+    """Make the inputs visible to oracle workers forked after this call.  With
+    dy, the oracle times the backward pass per query token (its row's dQ and
+    its contributions to dK and dV)."""
     _G.update(q=case.q, k=case.k, v=case.v, perm=perm, window=wl["window"], causal=wl["causal"],
-              path=wl["path"], ga=case.gate_sa, gw=case.gate_swa)
+              path=wl["path"], ga=case.gate_sa, gw=case.gate_swa, dy=dy, bwd=dy is not None)
 
 
 def oracle_throughput(case, perm, wl, seconds: float, pool=None, cores: int = 1) -> dict:
@@ -293,7 +314,10 @@ def run_reference(args, wl=WORKLOAD):
     case = make_inputs(wl)
     perm = np.stack([oracle.make_perm(wl["seed"], 0, b, wl["seq_len"]) for b in range(wl["batch"])])
     cores = len(os.sched_getaffinity(0))
-    publish_oracle_inputs(case, perm, wl)
+    bwd = getattr(args, "pass_", "fwd") == "bwd"
+    dy = (np.random.default_rng(wl["seed"] + 7).standard_normal(case.q.shape).astype(np.float32)
+          if bwd else None)
+    publish_oracle_inputs(case, perm, wl, dy)
     pool = make_pool(cores)
     per_step = max(0.5, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -303,7 +327,7 @@ def run_reference(args, wl=WORKLOAD):
     tokens = sum(r["value"] * r["seconds"] for r in runs)
     secs = sum(r["seconds"] for r in runs)
     value = tokens / secs
-    line = dict(impl="reference", metric=metric_of(wl), value=value, unit="tokens/s", n_gpus=world,
+    line = dict(impl="reference", metric=metric_of(wl, bwd), value=value, unit="tokens/s", n_gpus=world,
                 steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * secs / args.steps,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
                 data="synthetic",
@@ -323,6 +347,12 @@ def run_ours(args, wl=WORKLOAD):
     from sa_synth import bf16_bits
     case = make_inputs(wl)
     gated = wl["path"] == "gated"
+    bwd = getattr(args, "pass_", "fwd") == "bwd"
+    if bwd and gated and not args.no_cpu_baseline:
+        args.no_cpu_baseline = True  # the oracle's per-row backward covers the SA path only
+    dy_np = None
+    if bwd:  # upstream gradient ~ N(0, 1), bf16
+        dy_np = np.random.default_rng(wl["seed"] + 7).standard_normal(case.q.shape).astype(np.float32)
 
     import stochastic_sliding_window_gb300 as sa
     sa.load()
@@ -331,7 +361,7 @@ def run_ours(args, wl=WORKLOAD):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = len(os.sched_getaffinity(0))
-        publish_oracle_inputs(case, perm_np.astype(np.int64), wl)
+        publish_oracle_inputs(case, perm_np.astype(np.int64), wl, dy_np)
         pool = make_pool(cores)  # before the first CUDA call
         cpu = oracle_throughput(case, perm_np.astype(np.int64), wl, args.cpu_seconds, pool, cores)
         pool.close()
@@ -345,30 +375,53 @@ def run_ours(args, wl=WORKLOAD):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    def to_dev(x):
-        return torch.from_numpy(bf16_bits(x).view(np.int16)).to(dev).view(torch.bfloat16)
+    def host_bf16(x):
+        return torch.from_numpy(bf16_bits(x).view(np.int16)).view(torch.bfloat16)
 
-    q, k, v = to_dev(case.q), to_dev(case.k), to_dev(case.v)
-    perm = torch.from_numpy(perm_np).to(dev)
-    ga = torch.from_numpy(case.gate_sa).to(dev) if gated else None
-    gw = torch.from_numpy(case.gate_swa).to(dev) if gated else None
-    out = torch.empty_like(q)
+    # Host inputs of one step, in call order; outputs are allocated per slot.
+    hins = [host_bf16(case.q), host_bf16(case.k), host_bf16(case.v), torch.from_numpy(perm_np)]
+    if gated:
+        hins += [torch.from_numpy(case.gate_sa), torch.from_numpy(case.gate_swa)]
+    if bwd:
+        hins.append(host_bf16(dy_np))
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-
     kern = {"auto": sa.KERNEL_AUTO, "simt": sa.KERNEL_SIMT, "gather": sa.KERNEL_TCGEN05_GATHER,
             "ring": sa.KERNEL_TCGEN05_RING, "chunk": sa.KERNEL_TCGEN05_CHUNK}[args.kernel]
 
-    def forward(q_, k_, v_, p_, ga_, gw_, o_, st=stream):
+    def make_outs():
+        q_, k_ = hins[0], hins[1]
+        if not bwd:
+            return [torch.empty(q_.shape, dtype=torch.bfloat16, device=dev)]
+        outs = [torch.empty(q_.shape, dtype=torch.bfloat16, device=dev),
+                torch.empty(k_.shape, dtype=torch.bfloat16, device=dev),
+                torch.empty(k_.shape, dtype=torch.bfloat16, device=dev)]
         if gated:
-            sa.sa_swa_gated_forward(q_, k_, v_, p_, ga_, gw_, wl["window"], causal=wl["causal"],
-                                    out=o_, err=err, stream=st, kernel=kern)
+            outs += [torch.empty(hins[4].shape, dtype=torch.float32, device=dev) for _ in range(2)]
+        return outs
+
+    def call(d, o, st=stream):
+        w = wl["window"]
+        if not bwd:
+            if gated:
+                sa.sa_swa_gated_forward(d[0], d[1], d[2], d[3], d[4], d[5], w, causal=wl["causal"],
+                                        out=o[0], err=err, stream=st, kernel=kern)
+            else:
+                sa.sa_forward(d[0], d[1], d[2], d[3], w, causal=wl["causal"], out=o[0], err=err,
+                              stream=st, kernel=kern)
+        elif gated:
+            sa.sa_swa_gated_backward(d[0], d[1], d[2], d[3], d[4], d[5], d[6], w,
+                                     causal=wl["causal"], dq=o[0], dk=o[1], dv=o[2],
+                                     dgate_sa=o[3], dgate_swa=o[4], err=err, stream=st)
         else:
-            sa.sa_forward(q_, k_, v_, p_, wl["window"], causal=wl["causal"], out=o_, err=err,
-                          stream=st, kernel=kern)
+            sa.sa_backward(d[0], d[1], d[2], d[3], d[4], w, causal=wl["causal"], dq=o[0], dk=o[1],
+                           dv=o[2], err=err, stream=st)
+
+    ins = [x.to(dev) for x in hins]
+    outs = make_outs()
 
     def step():
-        forward(q, k, v, perm, ga, gw, out)
+        call(ins, outs)
 
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
     for _ in range(args.warmup):
@@ -381,7 +434,7 @@ def run_ours(args, wl=WORKLOAD):
     sampler.start()
     t_soak = time.perf_counter()
     while time.perf_counter() - t_soak < args.soak_seconds:  # settle clocks before timing
-        for _ in range(50):
+        for _ in range(50 if not bwd else 5):
             step()
         torch.cuda.synchronize(dev)
 
@@ -401,47 +454,40 @@ def run_ours(args, wl=WORKLOAD):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
     total_ms = max_over_ranks(float(sum(step_ms)), dev)
     status = sa.check_error(err)
     if status != sa.SA_OK:
         raise RuntimeError(f"device error word reports status {status}")
 
-    # end to end: pinned host buffers in, result out, copies inside the timing.
+    # end to end: pinned host buffers in, results out, copies inside the timing.
     # Two streams take alternate steps, each with its own device buffers and
-    # host result buffer, so one step's result copy overlaps the next step's
+    # host result buffers, so one step's result copy overlaps the next step's
     # input copy (the host link is full duplex).  Every step still copies all
     # of its inputs in and its whole result out.
-    hq = torch.from_numpy(bf16_bits(case.q).view(np.int16)).view(torch.bfloat16).pin_memory()
-    hk = torch.from_numpy(bf16_bits(case.k).view(np.int16)).view(torch.bfloat16).pin_memory()
-    hv = torch.from_numpy(bf16_bits(case.v).view(np.int16)).view(torch.bfloat16).pin_memory()
-    hp = torch.from_numpy(perm_np).pin_memory()
-    hins = [hq, hk, hv, hp]
-    if gated:
-        hins += [torch.from_numpy(case.gate_sa).pin_memory(),
-                 torch.from_numpy(case.gate_swa).pin_memory()]
+    hins = [t.pin_memory() for t in hins]
     h2d = sum(t.numel() * t.element_size() for t in hins)
-    d2h = out.numel() * out.element_size()
-    slots = [dict(stream=torch.cuda.Stream(dev),
-                  dins=[torch.empty_like(x, device=dev) for x in hins],
-                  out=torch.empty_like(out),
-                  hout=torch.empty(out.shape, dtype=torch.bfloat16).pin_memory())
-             for _ in range(2)]
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    slots = []
+    for _ in range(2):
+        souts = make_outs()
+        slots.append(dict(stream=torch.cuda.Stream(dev),
+                          dins=[torch.empty_like(x, device=dev) for x in hins], outs=souts,
+                          houts=[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in souts]))
 
     def e2e_step(i):
         sl = slots[i & 1]
         with torch.cuda.stream(sl["stream"]):
             for dst, src in zip(sl["dins"], hins):
                 dst.copy_(src, non_blocking=True)
-            d = sl["dins"]
-            forward(d[0], d[1], d[2], d[3], d[4] if gated else None, d[5] if gated else None,
-                    sl["out"], st=sl["stream"])
-            sl["hout"].copy_(sl["out"], non_blocking=True)
+            call(sl["dins"], sl["outs"], st=sl["stream"])
+            for hdst, dsrc in zip(sl["houts"], sl["outs"]):
+                hdst.copy_(dsrc, non_blocking=True)
 
     for i in range(4):
         e2e_step(i)
     torch.cuda.synchronize(dev)
-    e2e_steps = max(4, min(args.steps, 50 if wl is WORKLOAD else 10))
+    e2e_steps = max(4, min(args.steps, 50 if (wl is WORKLOAD and not bwd) else 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for sl in slots:
@@ -453,17 +499,17 @@ def run_ours(args, wl=WORKLOAD):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    ref_out = out.cpu().view(torch.int16)
     for sl in slots:
-        if not torch.equal(sl["hout"].view(torch.int16), ref_out):
-            raise RuntimeError("end-to-end output differs from the device-resident run")
+        for hres, dres in zip(sl["houts"], outs):
+            if not torch.equal(hres.view(torch.uint8), dres.cpu().view(torch.uint8)):
+                raise RuntimeError("end-to-end result differs from the device-resident run")
 
     if rank != 0:
         return 0
     tokens = wl["batch"] * wl["seq_len"]
     ms_per_step = total_ms / args.steps
     value = job_tokens_per_s(world, tokens, ms_per_step)
-    bytes_alg, flops_alg = algorithmic(wl)
+    bytes_alg, flops_alg = algorithmic_bwd(wl) if bwd else algorithmic(wl)
     peaks = load_peaks()
     secs = ms_per_step * 1e-3
     tensor_bound = flops_alg / (peaks["bf16_tflops"] * 1e12) > bytes_alg / (peaks["hbm_gbs"] * 1e9)
@@ -474,19 +520,21 @@ def run_ours(args, wl=WORKLOAD):
         roof = dict(bound="hbm", achieved=bytes_alg / secs / 1e9, peak=peaks["hbm_gbs"],
                     unit="GB/s", peak_source=f"{peaks['source']} hbm_gbs (copy, read+write)")
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profiled_traffic() if wl is WORKLOAD else None
+    roof["traffic"] = profiled_traffic() if (wl is WORKLOAD and not bwd) else None
     roof.update(bytes_per_launch=bytes_alg, flops_per_launch=flops_alg,
                 hbm_frac=bytes_alg / secs / 1e9 / peaks["hbm_gbs"],
                 tensor_frac=flops_alg / secs / 1e12 / peaks["bf16_tflops"])
+    kname = {sa.KERNEL_SIMT: "simt", sa.KERNEL_TCGEN05_GATHER: "tcgen05-gather",
+             sa.KERNEL_TCGEN05_RING: "tcgen05-ring",
+             sa.KERNEL_TCGEN05_CHUNK: "tcgen05-chunk"}.get(kernel, str(kernel))
     line = dict(
-        metric=metric_of(wl), value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
+        metric=metric_of(wl, bwd), value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
         warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True, scaling="weak",
         vs_baseline=None, dtype="bf16", data="synthetic",
         config=config_of(wl),
-        run=dict(kernel={sa.KERNEL_SIMT: "simt", sa.KERNEL_TCGEN05_GATHER: "tcgen05-gather",
-                         sa.KERNEL_TCGEN05_RING: "tcgen05-ring",
-                         sa.KERNEL_TCGEN05_CHUNK: "tcgen05-chunk"}.get(kernel, str(kernel)),
-                 parallelism="replicas" if world > 1 else "single-gpu"),
+        run=dict(kernel="tcgen05-backward (dq, dkv)" if bwd else kname,
+                 parallelism="replicas" if world > 1 else "single-gpu",
+                 **({"pass": "backward"} if bwd else {})),
         roofline=roof,
         cpu_baseline=cpu,
         e2e=dict(value=job_tokens_per_s(world, tokens, e2e_ms), unit="tokens/s",
@@ -512,6 +560,8 @@ def main():
                     help="shape to time (default: the long-prefill GQA headline)")
     ap.add_argument("--window", type=int, default=0, help="override the workload's window")
     ap.add_argument("--seq-len", type=int, default=0, help="override the workload's length")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward pass (default) or the backward pass")
     ap.add_argument("--kernel", choices=["auto", "simt", "gather", "ring", "chunk"],
                     default="auto", help="force one of the library's kernels (default: its choice)")
     args = ap.parse_args()
