@@ -162,6 +162,31 @@ sa_status_t swa_backward(const sa_params_t* params, const void* q, const void* k
 size_t sa_backward_workspace_size(const sa_params_t* params);
 
 /*
+ * sa_backward without a workspace argument and without any allocation.  The
+ * pages have no counterpart to this call: it exists for callers that cannot
+ * allocate device memory at the point where they run the backward pass --
+ * for example a training or serving loop whose device memory is reserved
+ * once at start-up, a host framework that owns every device allocation and
+ * hands the library only tensors, or a plain C caller with no allocator of
+ * its own.  The scratch that sa_backward takes from its workspace (two fp32
+ * values per (token, query head)) lives instead in a fixed device array
+ * inside this library, sized for batch * seqlen * num_q_heads <= 1048576
+ * (8 MiB, held on every device that loads the library until the process
+ * exits).  Larger problems return SA_ERR_UNSUPPORTED with a message naming
+ * the limit; use sa_backward for them.  Arguments, results and the other
+ * rules are those of sa_backward; the call itself allocates nothing.  The
+ * first call on each device looks up the array's address on that device, so
+ * make that first call before any stream capture.  Every call on a device
+ * shares the one array: calls whose kernels may overlap on the GPU (different
+ * streams without ordering between them) race on it, so order them.  The
+ * array keeps the last call's contents; each call writes every value it
+ * reads first, so nothing is cleared between calls.
+ */
+sa_status_t sa_backward_noalloc(const sa_params_t* params, const void* q, const void* k,
+                                const void* v, const int32_t* perm, const void* dout, void* dq,
+                                void* dk, void* dv, cudaStream_t stream);
+
+/*
  * Gradients of the gated dual path ("Gated SA and SWA" equation).  The
  * gate-logit gradient of a row is g (1 - g) <dout, Y_path> with g its
  * sigmoid.  The two paths' dq, dk, dv are summed in fp32 in the workspace and

@@ -33,6 +33,7 @@ SIGNATURES = {
     "sa_backward": (c_int32, [c_void_p] * 10 + [c_size_t, c_void_p]),
     "swa_backward": (c_int32, [c_void_p] * 9 + [c_size_t, c_void_p]),
     "sa_backward_workspace_size": (c_size_t, [c_void_p]),
+    "sa_backward_noalloc": (c_int32, [c_void_p] * 10),
     "sa_swa_gated_backward": (c_int32, [c_void_p] * 14 + [c_size_t, c_void_p]),
     "sa_swa_gated_backward_workspace_size": (c_size_t, [c_void_p]),
     "sa_inverse_perm": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p]),

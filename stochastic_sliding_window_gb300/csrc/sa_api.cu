@@ -4,6 +4,7 @@
 // attention itself runs in the CUDA kernels of sa_tc_ring.cu, sa_tc_chunk.cu,
 // sa_tc.cu and sa_simt.cu; sigma^-1 in sa_perm.cu.
 #include <atomic>
+#include <mutex>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -299,6 +300,65 @@ extern "C" sa_status_t swa_backward(const sa_params_t* params, const void* q, co
                                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return run_bwd_single(params, q, k, v, nullptr, dout, dq, dk, dv, workspace, workspace_bytes,
                         kPathSWA, stream);
+}
+
+// ------------------------------------------------------------------ backward, no allocation
+
+namespace sa {
+
+// Scratch of sa_backward_noalloc: the per-row log2 normaliser and D of the
+// backward kernels (two fp32 values per (token, query head)), for at most
+// kNoallocMaxRows rows, i.e. 8 MiB.  A file-scope device array: every device
+// that loads this library holds it until the process exits.
+constexpr size_t kNoallocMaxRows = size_t(1) << 20;
+static __device__ __align__(256) float g_noalloc_scratch[2 * kNoallocMaxRows];
+
+// The array's device address on each device, looked up once per device with
+// that device current (in host code the array's name is only a stand-in).
+constexpr int kNoallocMaxDevices = 64;
+static std::mutex g_noalloc_mu;
+static float* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+static sa_status_t noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+  if (dev < 0 || dev >= kNoallocMaxDevices)
+    return fail(SA_ERR_UNSUPPORTED, "device index %d beyond the %d this entry point tracks", dev,
+                kNoallocMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    ce = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (ce != cudaSuccess || p == nullptr)
+      return fail(SA_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s",
+                  cudaGetErrorString(ce));
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return SA_OK;
+}
+
+}  // namespace sa
+
+extern "C" sa_status_t sa_backward_noalloc(const sa_params_t* params, const void* q,
+                                           const void* k, const void* v, const int32_t* perm,
+                                           const void* dout, void* dq, void* dk, void* dv,
+                                           cudaStream_t stream) {
+  sa_status_t st = check_params(params, true);
+  if (st != SA_OK) return st;
+  const size_t rows = size_t(params->batch) * params->seqlen * params->num_q_heads;
+  if (rows > kNoallocMaxRows)
+    return fail(SA_ERR_UNSUPPORTED,
+                "sa_backward_noalloc: batch * seqlen * num_q_heads = %zu exceeds the %zu rows "
+                "its static scratch holds; use sa_backward with a workspace",
+                rows, kNoallocMaxRows);
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != SA_OK) return st;
+  // Both halves are written for every row before they are read within the
+  // call, so nothing needs clearing between calls.
+  return run_bwd_single(params, q, k, v, perm, dout, dq, dk, dv, scratch,
+                        2 * kNoallocMaxRows * sizeof(float), kPathSA, stream);
 }
 
 extern "C" sa_status_t sa_swa_gated_backward(const sa_params_t* params, const void* q,
