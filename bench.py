@@ -547,6 +547,58 @@ def run_ours(args, wl=WORKLOAD):
     return 0
 
 
+def run_receptive(args):
+    """Receptive-field analytics of stacked SA layers at the length-sweep
+    size: |R_l(t)| for l = 1..8 and a seeded sample of target tokens, each
+    layer with its own sigma.  One step = one sa_receptive_field call."""
+    import numpy as np
+    import torch
+    import stochastic_sliding_window_gb300 as sa
+    rank, world, local = dist_env()
+    n, w, layers, ntargets = args.seq_len or 262144, args.window or 128, 8, 4096
+    causal = args.causal_rf
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    perms = torch.from_numpy(np.stack([sa.make_perm(0, l, 0, n) for l in range(layers)])).to(dev)
+    targets = torch.from_numpy(np.random.default_rng(1).integers(0, n, ntargets).astype(np.int32)).to(dev)
+    sizes = torch.empty((layers, ntargets), dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        sa.receptive_field(perms, w, targets, causal=causal, sizes=sizes, err=err)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        sa.receptive_field(perms, w, targets, causal=causal, sizes=sizes, err=err)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if sa.check_error(err) != sa.SA_OK:
+        raise RuntimeError("device error word set")
+    cov = (sizes.double().mean(dim=1) / n).cpu().tolist()
+    # work: every layer application visits n positions x (2h + 1) window slots;
+    # R_L costs L applications, for every group of 64 targets
+    h = min(w // 2, n - 1)
+    apps = (ntargets + 63) // 64 * layers * (layers + 1) // 2
+    slots = apps * n * (2 * h + 1)
+    if rank == 0:
+        print(json.dumps(dict(
+            metric=f"SA receptive-field analytics fields/s (n={n}, w={w}, {layers} layers, "
+                   f"{'causal' if causal else 'non-causal'})",
+            value=ntargets * layers / (ms * 1e-3), unit="target-layer fields/s", n_gpus=world,
+            steps=args.steps, warmup=args.warmup, ms_per_step=ms, higher_is_better=True,
+            scaling="weak", vs_baseline=None, dtype="int64", data="synthetic",
+            config=dict(workload="receptive_field", seq_len=n, window=w, layers=layers,
+                        targets=ntargets, causal=causal),
+            window_slots_per_s=slots / (ms * 1e-3), mean_coverage_per_layer=cov,
+            gpu_launches=args.steps * ((ntargets + 63) // 64) * (layers * 3 + layers * (layers + 1) // 2),
+            clocks=clocks)), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -560,8 +612,11 @@ def main():
                     help="shape to time (default: the long-prefill GQA headline)")
     ap.add_argument("--window", type=int, default=0, help="override the workload's window")
     ap.add_argument("--seq-len", type=int, default=0, help="override the workload's length")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
-                    help="time the forward pass (default) or the backward pass")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "receptive"], default="fwd",
+                    help="time the forward pass (default), the backward pass, or the "
+                         "receptive-field analytics of stacked layers")
+    ap.add_argument("--causal-rf", action="store_true",
+                    help="receptive fields of causal SA (default: non-causal)")
     ap.add_argument("--kernel", choices=["auto", "simt", "gather", "ring", "chunk"],
                     default="auto", help="force one of the library's kernels (default: its choice)")
     args = ap.parse_args()
@@ -570,6 +625,8 @@ def main():
     wl = WORKLOADS[args.workload]
     if args.window or args.seq_len:
         wl = dict(wl, window=args.window or wl["window"], seq_len=args.seq_len or wl["seq_len"])
+    if args.pass_ == "receptive":
+        return run_receptive(args)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -214,6 +214,28 @@ sa_status_t sa_inverse_perm(const int32_t* perm, int32_t* inv, int32_t batch, in
                             int32_t* d_err, cudaStream_t stream);
 
 /*
+ * Receptive fields of L stacked SA layers ("Theoretical properties",
+ * receptive-field bullet: with an independent sigma per layer the field grows
+ * far faster than sliding-window attention's and covers the sequence in
+ * O(log_w n) layers).  With N_l(i) the neighbour set of token i in layer l
+ * (window `window`, causal or not, as in sa_forward) and R_0(i) = {i},
+ * R_l(i) = union over j in N_l(i) of R_{l-1}(j); layer 1 acts first on the
+ * inputs, so R_L(i) applies layer L to {i}, then L-1, ..., 1.
+ *   perms    device int32 [layers, n]: sigma of each layer (one sequence)
+ *   targets  device int32 [num_targets]: tokens whose fields are measured
+ *   sizes    device int64 [layers, num_targets] out: sizes[l-1][t] = |R_l(targets[t])|
+ * Exact integer counts.  Workspace: sa_receptive_field_workspace_size(n)
+ * bytes, 16-byte aligned.  1 <= layers <= 64, floor(window/2) <= 1024.  Perm
+ * or target entries outside [0, n) set SA_ERRBIT_RANGE in *d_err (NULL: the
+ * library's word).  Asynchronous on `stream`.
+ */
+size_t sa_receptive_field_workspace_size(int32_t n);
+sa_status_t sa_receptive_field(const int32_t* perms, int32_t layers, int32_t n, int32_t window,
+                               int32_t causal, const int32_t* targets, int32_t num_targets,
+                               int64_t* sizes, void* workspace, size_t workspace_bytes,
+                               int32_t* d_err, cudaStream_t stream);
+
+/*
  * Host: draw sigma ~ Uniform(S_n) for (seed, layer, batch_index) ("Core
  * mechanism" step 1: one independent permutation per layer) into perm_host
  * (int32[n], caller-owned).  Generator: the stream state is the output of one

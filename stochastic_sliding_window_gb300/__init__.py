@@ -35,6 +35,7 @@ from ._libsa import (
     load,
     make_perm,
     make_perms,
+    receptive_field,
     sa_backward,
     sa_forward,
     sa_inverse_perm,
@@ -51,5 +52,5 @@ __all__ = [
     "SA_OK", "SIGNATURES", "SaError", "SaParams", "check_error", "clear_error", "last_kernel",
     "last_launch_count", "load", "make_perm", "make_perms", "sa_forward", "sa_inverse_perm",
     "sa_swa_gated_forward", "set_wait_limit", "get_wait_limit", "swa_forward",
-    "sa_backward", "swa_backward", "sa_swa_gated_backward",
+    "sa_backward", "swa_backward", "sa_swa_gated_backward", "receptive_field",
 ]

@@ -37,6 +37,9 @@ SIGNATURES = {
     "sa_swa_gated_backward": (c_int32, [c_void_p] * 14 + [c_size_t, c_void_p]),
     "sa_swa_gated_backward_workspace_size": (c_size_t, [c_void_p]),
     "sa_inverse_perm": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
+    "sa_receptive_field_workspace_size": (c_size_t, [c_int32]),
+    "sa_receptive_field": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,
+                                     c_int32, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
     "sa_make_perm": (c_int32, [c_uint64, c_int32, c_int32, c_int32, POINTER(c_int32)]),
     "sa_check_error": (c_int32, [c_void_p, c_void_p]),
     "sa_clear_error": (c_int32, [c_void_p, c_void_p]),
@@ -320,6 +323,33 @@ def sa_inverse_perm(perm, inv=None, err=None, stream=None):
                                       err.data_ptr() if err is not None else None,
                                       _stream(perm, stream)))
     return inv
+
+
+def receptive_field(perms, window: int, targets, causal: bool = False, sizes=None, err=None,
+                    stream=None):
+    """|R_l(t)| for l = 1..L of stacked SA layers with sigma perms[l-1]
+    (device int32 [L, n]) for each target token (device int32 [T]): int64
+    [L, T] on the device."""
+    import torch
+    _need(perms, "perms", torch.int32, 2)
+    _need(targets, "targets", torch.int32, 1)
+    layers, n = perms.shape
+    sizes = torch.empty((layers, targets.numel()), dtype=torch.int64, device=perms.device) \
+        if sizes is None else sizes
+    _need(sizes, "sizes", torch.int64, 2)
+    _shape(sizes, "sizes", (layers, targets.numel()))
+    _check_err(err)
+    _on_device(perms, "perms", [("targets", targets), ("sizes", sizes), ("err", err)])
+    lib = load()
+    with torch.cuda.device(perms.device):
+        ws = lib.sa_receptive_field_workspace_size(n)
+        work = torch.empty(ws, dtype=torch.uint8, device=perms.device)
+        _check(lib.sa_receptive_field(perms.data_ptr(), layers, n, int(window), int(bool(causal)),
+                                      targets.data_ptr(), targets.numel(), sizes.data_ptr(),
+                                      work.data_ptr(), ws,
+                                      err.data_ptr() if err is not None else None,
+                                      _stream(perms, stream)))
+    return sizes
 
 
 def check_error(err=None, stream=None) -> int:

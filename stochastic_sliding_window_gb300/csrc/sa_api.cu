@@ -410,6 +410,31 @@ extern "C" sa_status_t sa_swa_gated_backward(const sa_params_t* params, const vo
   return finish_bwd(SA_OK, 7);
 }
 
+extern "C" size_t sa_receptive_field_workspace_size(int32_t n) {
+  return n < 1 ? 0 : receptive_field_workspace_bytes(n);
+}
+
+extern "C" sa_status_t sa_receptive_field(const int32_t* perms, int32_t layers, int32_t n,
+                                          int32_t window, int32_t causal, const int32_t* targets,
+                                          int32_t num_targets, int64_t* sizes, void* workspace,
+                                          size_t workspace_bytes, int32_t* d_err,
+                                          cudaStream_t stream) {
+  if (!perms || !targets || !sizes || !workspace)
+    return fail(SA_ERR_INVALID_ARG, "perms, targets, sizes and workspace must be non-NULL");
+  if (layers < 1 || layers > 64 || n < 1 || window < 1 || num_targets < 1)
+    return fail(SA_ERR_INVALID_ARG, "need 1 <= layers <= 64, n >= 1, window >= 1, num_targets >= 1");
+  if (workspace_bytes < receptive_field_workspace_bytes(n))
+    return fail(SA_ERR_INVALID_ARG, "workspace of %zu bytes needed", receptive_field_workspace_bytes(n));
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0 || (reinterpret_cast<uintptr_t>(sizes) & 7u) != 0)
+    return fail(SA_ERR_INVALID_ARG, "workspace must be 16-byte and sizes 8-byte aligned");
+  int32_t* err = d_err ? d_err : default_error_word();
+  if (!err) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  sa_status_t st = launch_receptive_field(perms, layers, n, window, causal ? 1 : 0, targets,
+                                          num_targets, sizes, workspace, err, stream);
+  if (st == SA_OK) g_msg[0] = '\0';
+  return st;
+}
+
 extern "C" sa_status_t sa_inverse_perm(const int32_t* perm, int32_t* inv, int32_t batch,
                                        int32_t n, int32_t* d_err, cudaStream_t stream) {
   if (!perm || !inv) return fail(SA_ERR_INVALID_ARG, "perm and inv must be non-NULL");

@@ -97,6 +97,12 @@ sa_status_t launch_bwd(const Problem& pb, Path path, const BwdArgs& a, cudaStrea
 // fp32 -> bf16 conversion of `count` values (a multiple of 4).
 sa_status_t launch_to_bf16(const float* src, void* dst, size_t count, cudaStream_t stream);
 
+// Receptive fields of stacked SA layers (sa_graph.cu).
+size_t receptive_field_workspace_bytes(int n);
+sa_status_t launch_receptive_field(const int32_t* perms, int layers, int n, int window, int causal,
+                                   const int32_t* targets, int num_targets, int64_t* sizes,
+                                   void* workspace, int32_t* err, cudaStream_t s);
+
 // sigma^{-1} kernels.
 sa_status_t launch_inverse_perm(const int32_t* perm, int32_t* inv, int batch, int n,
                                 int32_t* err, cudaStream_t stream);
