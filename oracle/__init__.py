@@ -20,6 +20,9 @@ gist.science/ja/paper/2604.00754 and gist.science/ko/paper/2604.00754):
                   Q, K, V and the gate logits, and each row's log-sum-exp
                   (the chain rule through the forward definition; the pages
                   use SA to pretrain a model: "Main contributions", item 3).
+* ``prologue``  -- the two gate projections of the layer input and the
+                  rotary position embedding by original token index that
+                  feed the attention paths ("Gated SA and SWA" section).
 * ``graph``     -- neighbour sets, the pairwise connection probability and the
                   receptive-field growth over stacked layers
                   (section "Core mechanism", last paragraph; "Theoretical
@@ -49,6 +52,7 @@ from .backward import (
     sa_lse,
     swa_lse,
 )
+from .prologue import gate_logits, rope, rope_angles
 from .graph import (
     neighbours_sa,
     neighbours_swa,
@@ -74,6 +78,9 @@ __all__ = [
     "gated_forward",
     "full_attention",
     "masked_attention",
+    "gate_logits",
+    "rope",
+    "rope_angles",
     "sa_backward",
     "sa_dq_rows",
     "swa_backward",
