@@ -214,6 +214,36 @@ sa_status_t sa_inverse_perm(const int32_t* perm, int32_t* inv, int32_t batch, in
                             int32_t* d_err, cudaStream_t stream);
 
 /*
+ * The gate logits of the dual path ("Gated SA and SWA": the two paths are
+ * mixed through independent sigmoid projections).  Both projections of the
+ * layer input x (bf16 [tokens, d_model], row-major; tokens = B * n in BSHD
+ * token order) in one tensor-core GEMM:
+ *   gate_sa_logits  = x W_sa^T  + b_sa,   gate_swa_logits = x W_swa^T + b_swa,
+ * W_* bf16 [num_q_heads, d_model], b_* fp32 [num_q_heads] or NULL, outputs
+ * fp32 [tokens, num_q_heads] -- exactly the logits sa_swa_gated_forward and
+ * sa_swa_gated_backward take (they apply the sigmoid).  d_model a multiple
+ * of 64, num_q_heads <= 128, x and weights 16-byte aligned.  fp32
+ * accumulation of bf16 products.  Asynchronous on `stream`.
+ */
+sa_status_t sa_gate_projection(const void* x, int32_t tokens, int32_t d_model,
+                               int32_t num_q_heads, const void* w_sa, const void* w_swa,
+                               const float* b_sa, const float* b_swa, float* gate_sa_logits,
+                               float* gate_swa_logits, int32_t* d_err, cudaStream_t stream);
+
+/*
+ * Rotary position embedding by ORIGINAL token index, applied in place to a
+ * bf16 BSHD tensor (Q or K) before the sigma-gather, so that a score depends
+ * on the distance i - j between the two tokens in the original order
+ * whatever permutation brings them into one window.  Convention: for
+ * k < head_dim/2 the pair (x_k, x_{k + head_dim/2}) of token i is rotated by
+ * the angle i * base^(-2k/head_dim).  head_dim even and <= 128, base > 1.
+ * Angles are reduced in fp64, rotations done in fp32, results rounded to
+ * bf16.  Asynchronous on `stream`.
+ */
+sa_status_t sa_rope(void* x, int32_t batch, int32_t seqlen, int32_t heads, int32_t head_dim,
+                    double base, cudaStream_t stream);
+
+/*
  * Receptive fields of L stacked SA layers ("Theoretical properties",
  * receptive-field bullet: with an independent sigma per layer the field grows
  * far faster than sliding-window attention's and covers the sequence in

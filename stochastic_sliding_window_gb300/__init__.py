@@ -35,7 +35,9 @@ from ._libsa import (
     load,
     make_perm,
     make_perms,
+    gate_projection,
     receptive_field,
+    rope_,
     sa_backward,
     sa_forward,
     sa_inverse_perm,
@@ -53,4 +55,5 @@ __all__ = [
     "last_launch_count", "load", "make_perm", "make_perms", "sa_forward", "sa_inverse_perm",
     "sa_swa_gated_forward", "set_wait_limit", "get_wait_limit", "swa_forward",
     "sa_backward", "swa_backward", "sa_swa_gated_backward", "receptive_field",
+    "gate_projection", "rope_",
 ]

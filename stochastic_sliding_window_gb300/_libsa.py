@@ -10,7 +10,8 @@ fallback implementation.
 from __future__ import annotations
 
 import ctypes
-from ctypes import POINTER, byref, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+from ctypes import (POINTER, byref, c_char_p, c_double, c_float, c_int32, c_int64, c_size_t,
+                    c_uint64, c_void_p)
 from pathlib import Path
 
 import numpy as np
@@ -37,6 +38,9 @@ SIGNATURES = {
     "sa_swa_gated_backward": (c_int32, [c_void_p] * 14 + [c_size_t, c_void_p]),
     "sa_swa_gated_backward_workspace_size": (c_size_t, [c_void_p]),
     "sa_inverse_perm": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
+    "sa_gate_projection": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "sa_rope": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_double, c_void_p]),
     "sa_receptive_field_workspace_size": (c_size_t, [c_int32]),
     "sa_receptive_field": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,
                                      c_int32, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
@@ -323,6 +327,52 @@ def sa_inverse_perm(perm, inv=None, err=None, stream=None):
                                       err.data_ptr() if err is not None else None,
                                       _stream(perm, stream)))
     return inv
+
+
+def gate_projection(x, w_sa, w_swa, b_sa=None, b_swa=None, gate_sa=None, gate_swa=None, err=None,
+                    stream=None):
+    """Both gate logits of the layer input x (bf16 [B, n, d_model]) with
+    weights [Hq, d_model] (bf16) and optional biases [Hq] (fp32): fp32
+    [B, n, Hq] each, in one GEMM."""
+    import torch
+    _need(x, "x", torch.bfloat16, 3)
+    _need(w_sa, "w_sa", torch.bfloat16, 2)
+    _need(w_swa, "w_swa", torch.bfloat16, 2)
+    b, n, dm = x.shape
+    hq = w_sa.shape[0]
+    _shape(w_sa, "w_sa", (hq, dm))
+    _shape(w_swa, "w_swa", (hq, dm))
+    for name, t in (("b_sa", b_sa), ("b_swa", b_swa)):
+        if t is not None:
+            _need(t, name, torch.float32, 1)
+            _shape(t, name, (hq,))
+    gate_sa = torch.empty((b, n, hq), dtype=torch.float32, device=x.device) if gate_sa is None else gate_sa
+    gate_swa = torch.empty((b, n, hq), dtype=torch.float32, device=x.device) if gate_swa is None else gate_swa
+    for name, t in (("gate_sa", gate_sa), ("gate_swa", gate_swa)):
+        _need(t, name, torch.float32, 3)
+        _shape(t, name, (b, n, hq))
+    _check_err(err)
+    _on_device(x, "x", [("w_sa", w_sa), ("w_swa", w_swa), ("b_sa", b_sa), ("b_swa", b_swa),
+                        ("gate_sa", gate_sa), ("gate_swa", gate_swa), ("err", err)])
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    with torch.cuda.device(x.device):
+        _check(load().sa_gate_projection(x.data_ptr(), b * n, dm, hq, w_sa.data_ptr(),
+                                         w_swa.data_ptr(), ptr(b_sa), ptr(b_swa),
+                                         gate_sa.data_ptr(), gate_swa.data_ptr(), ptr(err),
+                                         _stream(x, stream)))
+    return gate_sa, gate_swa
+
+
+def rope_(x, base: float = 10000.0, stream=None):
+    """Rotate x (bf16 [B, n, H, d], in place) by each token's original index."""
+    import torch
+    _need(x, "x", torch.bfloat16, 4)
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    b, n, h, d = x.shape
+    with torch.cuda.device(x.device):
+        _check(load().sa_rope(x.data_ptr(), b, n, h, d, float(base), _stream(x, stream)))
+    return x
 
 
 def receptive_field(perms, window: int, targets, causal: bool = False, sizes=None, err=None,

@@ -410,6 +410,42 @@ extern "C" sa_status_t sa_swa_gated_backward(const sa_params_t* params, const vo
   return finish_bwd(SA_OK, 7);
 }
 
+extern "C" sa_status_t sa_gate_projection(const void* x, int32_t tokens, int32_t d_model,
+                                          int32_t num_q_heads, const void* w_sa,
+                                          const void* w_swa, const float* b_sa,
+                                          const float* b_swa, float* gate_sa_logits,
+                                          float* gate_swa_logits, int32_t* d_err,
+                                          cudaStream_t stream) {
+  if (!x || !w_sa || !w_swa || !gate_sa_logits || !gate_swa_logits)
+    return fail(SA_ERR_INVALID_ARG, "x, both weights and both logit outputs must be non-NULL");
+  if (tokens < 1 || num_q_heads < 1 || d_model < 1)
+    return fail(SA_ERR_INVALID_ARG, "tokens, d_model and num_q_heads must be >= 1");
+  if (d_model % 64 != 0 || num_q_heads > 128)
+    return fail(SA_ERR_UNSUPPORTED, "d_model must be a multiple of 64 and num_q_heads <= 128");
+  if (!aligned16(x) || !aligned16(w_sa) || !aligned16(w_swa))
+    return fail(SA_ERR_INVALID_ARG, "x and the weights must be 16-byte aligned");
+  if (double(tokens) * d_model >= 9.0e18 || double(tokens) * num_q_heads >= 2147483647.0)
+    return fail(SA_ERR_UNSUPPORTED, "problem too large");
+  int32_t* err = d_err ? d_err : default_error_word();
+  if (!err) return fail(SA_ERR_CUDA, "cannot resolve the library error word");
+  sa_status_t st = launch_gate_projection(x, tokens, d_model, num_q_heads, w_sa, w_swa, b_sa, b_swa,
+                                          gate_sa_logits, gate_swa_logits, err, stream);
+  if (st == SA_OK) g_msg[0] = '\0';
+  return st;
+}
+
+extern "C" sa_status_t sa_rope(void* x, int32_t batch, int32_t seqlen, int32_t heads,
+                               int32_t head_dim, double base, cudaStream_t stream) {
+  if (!x) return fail(SA_ERR_INVALID_ARG, "x must be non-NULL");
+  if (batch < 1 || seqlen < 1 || heads < 1 || head_dim < 2 || head_dim % 2 != 0 || head_dim > 128)
+    return fail(SA_ERR_INVALID_ARG, "need batch, seqlen, heads >= 1 and an even head_dim <= 128");
+  if (!(base > 1.0)) return fail(SA_ERR_INVALID_ARG, "base must be > 1");
+  if (double(batch) * seqlen >= 2147483647.0) return fail(SA_ERR_UNSUPPORTED, "batch * seqlen too large");
+  sa_status_t st = launch_rope(x, batch, seqlen, heads, head_dim, base, stream);
+  if (st == SA_OK) g_msg[0] = '\0';
+  return st;
+}
+
 extern "C" size_t sa_receptive_field_workspace_size(int32_t n) {
   return n < 1 ? 0 : receptive_field_workspace_bytes(n);
 }

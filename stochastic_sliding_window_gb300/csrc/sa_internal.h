@@ -103,6 +103,13 @@ sa_status_t launch_receptive_field(const int32_t* perms, int layers, int n, int 
                                    const int32_t* targets, int num_targets, int64_t* sizes,
                                    void* workspace, int32_t* err, cudaStream_t s);
 
+// The gate projections and RoPE (sa_prologue.cu).
+sa_status_t launch_gate_projection(const void* x, int tokens, int d_model, int hq, const void* w_sa,
+                                   const void* w_swa, const float* b_sa, const float* b_swa,
+                                   float* a_sa, float* a_swa, int32_t* err, cudaStream_t stream);
+sa_status_t launch_rope(void* x, int batch, int n, int heads, int head_dim, double base,
+                        cudaStream_t stream);
+
 // sigma^{-1} kernels.
 sa_status_t launch_inverse_perm(const int32_t* perm, int32_t* inv, int batch, int n,
                                 int32_t* err, cudaStream_t stream);

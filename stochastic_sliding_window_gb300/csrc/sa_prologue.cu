@@ -1,0 +1,278 @@
+// What feeds the attention paths: the two gate projections and the rotary
+// position embedding by original token index.
+//
+// Gates ("Gated SA and SWA" section of the Stochastic Attention summary: the
+// two paths are mixed through independent sigmoid projections).  The logits
+// of both projections of the layer input come out of ONE tcgen05 GEMM,
+//   [a_sa | a_swa] = x [W_sa ; W_swa]^T + [b_sa | b_swa],
+// M = 128 tokens per tile, N = 2 Hq (padded to 32), K = d_model in 64-column
+// blocks: x and both weight blocks are gathered with cp.async into
+// double-buffered shared memory (128-byte swizzle) while the previous block's
+// MMAs run; the bias is added in the epilogue and each token's two logit rows
+// are written.  The sigmoid is applied where the paths merge (the attention
+// epilogues), so the logits are what the gated calls take.
+//
+// RoPE before the gather: Q and K are rotated by each token's ORIGINAL index
+// i (pairs (x_k, x_{k+d/2}) turned by i * theta_k, theta_k = base^(-2k/d)),
+// so that a score depends on i - j whatever permutation brings the two
+// tokens into one window.  One block per token; the angle is reduced to
+// [-pi, pi] in fp64 before the fp32 sine and cosine, so positions in the
+// hundreds of thousands keep their precision.
+#include "sa_internal.h"
+#include "sa_tc_common.cuh"
+
+#include <cmath>
+#include <cstring>
+
+namespace sa {
+namespace pro {
+
+using namespace tcc;
+
+constexpr int kThreads = 128;
+constexpr int kKB = 64;  // d_model columns per block (128 bytes of bf16)
+
+struct GateParams {
+  const __nv_bfloat16* x;    // [M, D]
+  const __nv_bfloat16* w_sa;  // [Hq, D]
+  const __nv_bfloat16* w_swa;
+  const float* b_sa;          // [Hq] or nullptr
+  const float* b_swa;
+  float* a_sa;                // [M, Hq]
+  float* a_swa;
+  int32_t* err;
+  int M, D, Hq, n_pad, num_tiles;
+  uint32_t x_bytes, w_bytes, off_bar;  // one stage's x and w blocks; barrier offset
+  long long timeout_cycles;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) sa_gate_proj_kernel(const __grid_constant__ GateParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t stage_bytes = P.x_bytes + P.w_bytes;
+  const uint32_t bars = sbase + P.off_bar;  // [2] MMA of the stage done, [1] drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.off_bar + 24);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.off_bar + 28);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(bars, 1);
+    mbar_init(bars + 8, 1);
+    mbar_init(bars + 16, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // padded weight rows stay zero in both stages
+  for (int s = 0; s < 2; ++s)
+    for (int i = 2 * P.Hq * 128 + tid * 16; i < P.n_pad * 128; i += kThreads * 16)
+      *reinterpret_cast<uint4*>(smem + s * stage_bytes + P.x_bytes + i) = make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(256u)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
+  const int nkb = P.D / kKB;
+  const uint32_t id = idesc_bf16(kBM, P.n_pad, 0);
+  uint32_t phase[2] = {0, 0};
+  bool alive = true;
+  for (int tile = blockIdx.x; tile < P.num_tiles && alive; tile += gridDim.x) {
+    const int m0 = tile * kBM;
+    // one 64-column block of x (128 rows) and of both weights (2 Hq rows)
+    auto load = [&](int kb, int s) {
+      const uint32_t xs = sbase + s * stage_bytes, ws = xs + P.x_bytes;
+      for (int idx = tid; idx < kBM * 8; idx += kThreads) {
+        const int r = idx >> 3, c = idx & 7;
+        const int m = min(m0 + r, P.M - 1);
+        cp_async16(xs + r * 128 + ((c ^ (r & 7)) << 4), P.x + size_t(m) * P.D + kb * kKB + c * 8);
+      }
+      for (int idx = tid; idx < 2 * P.Hq * 8; idx += kThreads) {
+        const int r = idx >> 3, c = idx & 7;
+        const __nv_bfloat16* w = r < P.Hq ? P.w_sa + size_t(r) * P.D : P.w_swa + size_t(r - P.Hq) * P.D;
+        cp_async16(ws + r * 128 + ((c ^ (r & 7)) << 4), w + kb * kKB + c * 8);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    load(0, 0);
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb & 1;
+      if (kb + 1 < nkb) {
+        // stage 1 - s was last read by the MMAs of block kb - 1
+        if (kb >= 1) {
+          const bool ok = bounded_wait(bars + 8 * (1 - s), phase[1 - s], P.timeout_cycles, P.err,
+                                       abort_flag);
+          phase[1 - s] ^= 1;
+          if (__syncthreads_or(ok ? 0 : 1)) {
+            alive = false;
+            break;
+          }
+        }
+        load(kb + 1, 1 - s);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t xs = sbase + s * stage_bytes;
+        const uint64_t a0 = sdesc_sw128(xs, 16, 1024), b0 = sdesc_sw128(xs + P.x_bytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kKB / 16; ++kk)
+          umma_bf16(tmem, a0 + 2 * kk, b0 + 2 * kk, id, (kb > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bars + 8 * s);
+      }
+    }
+    if (!alive) break;
+    // the last block's MMAs (and with them all earlier ones) are done
+    {
+      const int s = (nkb - 1) & 1;
+      const bool ok = bounded_wait(bars + 8 * s, phase[s], P.timeout_cycles, P.err, abort_flag);
+      phase[s] ^= 1;
+      if (nkb >= 2) {  // the other stage's last commit was consumed by the loop's wait or is done
+        const int o = 1 - s;
+        const bool ok2 = nkb >= 2 && bounded_wait(bars + 8 * o, phase[o], P.timeout_cycles, P.err,
+                                                   abort_flag);
+        phase[o] ^= 1;
+        if (__syncthreads_or((ok && ok2) ? 0 : 1)) break;
+      } else if (__syncthreads_or(ok ? 0 : 1)) {
+        break;
+      }
+    }
+    tc_fence_after();
+    const int m = m0 + tid;
+    for (int c0 = 0; c0 < P.n_pad; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(trow + c0, v);  // every lane: the load is warp-collective
+      if (m < P.M) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = c0 + e;
+          if (col < P.Hq) {
+            P.a_sa[size_t(m) * P.Hq + col] =
+                __uint_as_float(v[e]) + (P.b_sa ? P.b_sa[col] : 0.f);
+          } else if (col < 2 * P.Hq) {
+            P.a_swa[size_t(m) * P.Hq + col - P.Hq] =
+                __uint_as_float(v[e]) + (P.b_swa ? P.b_swa[col - P.Hq] : 0.f);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // TMEM is overwritten by the next tile
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (tid == 0) {
+    umma_commit(bars + 16);
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bars + 16, 0) && clock64() - t0 < kDrainCycles) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256u)
+                 : "memory");
+  }
+}
+
+struct RopeParams {
+  __nv_bfloat16* x;  // [B, n, H, d], rotated in place
+  int n, H, d;
+  double theta[64];  // base^(-2k/d), k < d/2
+};
+
+__global__ void __launch_bounds__(kThreads) sa_rope_kernel(const __grid_constant__ RopeParams P) {
+  __shared__ float s_cos[64], s_sin[64];
+  const long long row = blockIdx.x;  // (b, i)
+  const int i = int(row % P.n);
+  const int half = P.d / 2;
+  if (threadIdx.x < half) {
+    const double a = double(i) * P.theta[threadIdx.x];
+    const double two_pi = 6.283185307179586476925286766559;
+    const float r = float(a - two_pi * rint(a / two_pi));  // in [-pi, pi]
+    float sn, cs;
+    sincosf(r, &sn, &cs);
+    s_cos[threadIdx.x] = cs;
+    s_sin[threadIdx.x] = sn;
+  }
+  __syncthreads();
+  __nv_bfloat16* base = P.x + size_t(row) * P.H * P.d;
+  for (int idx = threadIdx.x; idx < P.H * half; idx += blockDim.x) {
+    const int h = idx / half, k = idx - (idx / half) * half;
+    __nv_bfloat16* px = base + size_t(h) * P.d;
+    const float lo = __bfloat162float(px[k]), hi = __bfloat162float(px[k + half]);
+    const float c = s_cos[k], s = s_sin[k];
+    px[k] = __float2bfloat16_rn(lo * c - hi * s);
+    px[k + half] = __float2bfloat16_rn(hi * c + lo * s);
+  }
+}
+
+}  // namespace pro
+
+sa_status_t launch_gate_projection(const void* x, int tokens, int d_model, int hq, const void* w_sa,
+                                   const void* w_swa, const float* b_sa, const float* b_swa,
+                                   float* a_sa, float* a_swa, int32_t* err, cudaStream_t stream) {
+  using namespace pro;
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3) return fail(SA_ERR_UNSUPPORTED, "device is not sm_103");
+  GateParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.x = static_cast<const __nv_bfloat16*>(x);
+  P.w_sa = static_cast<const __nv_bfloat16*>(w_sa);
+  P.w_swa = static_cast<const __nv_bfloat16*>(w_swa);
+  P.b_sa = b_sa;
+  P.b_swa = b_swa;
+  P.a_sa = a_sa;
+  P.a_swa = a_swa;
+  P.err = err;
+  P.M = tokens;
+  P.D = d_model;
+  P.Hq = hq;
+  P.n_pad = (2 * hq + 31) / 32 * 32;
+  P.num_tiles = (tokens + kBM - 1) / kBM;
+  P.x_bytes = kBM * 128;
+  P.w_bytes = uint32_t(P.n_pad) * 128;
+  P.off_bar = 2 * (P.x_bytes + P.w_bytes);
+  P.timeout_cycles = wait_limit_cycles();
+  const uint32_t smem = P.off_bar + 32 + 1024;
+  cudaError_t ce = cudaFuncSetAttribute(sa_gate_proj_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (ce == cudaSuccess) {
+    const int grid = P.num_tiles < sms ? P.num_tiles : sms;
+    sa_gate_proj_kernel<<<grid, kThreads, smem, stream>>>(P);
+    ce = cudaGetLastError();
+  }
+  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "gate projection launch: %s", cudaGetErrorString(ce));
+  return SA_OK;
+}
+
+sa_status_t launch_rope(void* x, int batch, int n, int heads, int head_dim, double base,
+                        cudaStream_t stream) {
+  using namespace pro;
+  RopeParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.x = static_cast<__nv_bfloat16*>(x);
+  P.n = n;
+  P.H = heads;
+  P.d = head_dim;
+  for (int k = 0; k < head_dim / 2; ++k) P.theta[k] = std::pow(base, -2.0 * k / head_dim);
+  sa_rope_kernel<<<unsigned(size_t(batch) * n), kThreads, 0, stream>>>(P);
+  const cudaError_t ce = cudaGetLastError();
+  if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(ce));
+  return SA_OK;
+}
+
+}  // namespace sa
