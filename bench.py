@@ -599,6 +599,71 @@ def run_receptive(args):
     return 0
 
 
+def run_prologue(args, wl):
+    """The prologue of one layer at a workload's shape: both gate logits of
+    the layer input (d_model = Hq * d) in one GEMM, then RoPE of Q and K by
+    original index.  One step = sa_gate_projection + two sa_rope calls."""
+    import numpy as np
+    import torch
+    import stochastic_sliding_window_gb300 as sa
+    rank, world, local = dist_env()
+    b, n, hq, hkv, d = wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"], wl["head_dim"]
+    dm = hq * d
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = torch.randn((b, n, dm), device=dev, generator=g).to(torch.bfloat16)
+    w1 = (torch.randn((hq, dm), device=dev, generator=g) * dm ** -0.5).to(torch.bfloat16)
+    w2 = (torch.randn((hq, dm), device=dev, generator=g) * dm ** -0.5).to(torch.bfloat16)
+    b1 = torch.zeros(hq, device=dev)
+    b2 = torch.zeros(hq, device=dev)
+    q = torch.randn((b, n, hq, d), device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn((b, n, hkv, d), device=dev, generator=g).to(torch.bfloat16)
+    a1 = torch.empty((b, n, hq), device=dev)
+    a2 = torch.empty((b, n, hq), device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        sa.gate_projection(x, w1, w2, b1, b2, gate_sa=a1, gate_swa=a2, err=err)
+        sa.rope_(q)
+        sa.rope_(k)
+
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps
+    if sa.check_error(err) != sa.SA_OK:
+        raise RuntimeError("device error word set")
+    # algorithmic bytes: x and both weights read, both logit arrays written,
+    # Q and K read and written once
+    bytes_alg = 2 * b * n * dm + 2 * 2 * hq * dm + 2 * 4 * b * n * hq + 2 * 2 * b * n * d * (hq + hkv)
+    peaks = load_peaks()
+    ach = bytes_alg / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps(dict(
+            metric=f"SA layer prologue tokens/s (gate projections d_model={dm} -> 2x{hq} logits, "
+                   f"RoPE of Q and K; n={n})",
+            value=b * n / (ms * 1e-3), unit="tokens/s", n_gpus=world, steps=args.steps,
+            warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+            vs_baseline=None, dtype="bf16", data="synthetic", config=config_of(wl),
+            roofline=dict(bound="hbm", achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s",
+                          frac=ach / peaks["hbm_gbs"], traffic=None, bytes_per_launch=bytes_alg),
+            gpu_launches=3 * args.steps, clocks=clocks)), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -612,7 +677,7 @@ def main():
                     help="shape to time (default: the long-prefill GQA headline)")
     ap.add_argument("--window", type=int, default=0, help="override the workload's window")
     ap.add_argument("--seq-len", type=int, default=0, help="override the workload's length")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "receptive"], default="fwd",
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "receptive", "prologue"], default="fwd",
                     help="time the forward pass (default), the backward pass, or the "
                          "receptive-field analytics of stacked layers")
     ap.add_argument("--causal-rf", action="store_true",
@@ -627,6 +692,8 @@ def main():
         wl = dict(wl, window=args.window or wl["window"], seq_len=args.seq_len or wl["seq_len"])
     if args.pass_ == "receptive":
         return run_receptive(args)
+    if args.pass_ == "prologue":
+        return run_prologue(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
