@@ -266,6 +266,33 @@ sa_status_t sa_receptive_field(const int32_t* perms, int32_t layers, int32_t n, 
                                int32_t* d_err, cudaStream_t stream);
 
 /*
+ * Host routing plan of sigma-routed sequence sharding: one sequence split
+ * over `world` ranks (one per GPU) with chunk c = ceil(n / world).  Rank r
+ * holds the original tokens [r c, (r+1) c) of Q, K, V and of the output, and
+ * computes the SA rows of the permuted positions [r c, (r+1) c) ("Core
+ * mechanism": sliding-window attention over the permuted order), working on
+ * the span [r c - floor(w/2), (r+1) c + floor(w/2)) clipped to [0, n).
+ *   tokens      out [span]: the span's tokens in ascending original order --
+ *               the local rows of Q, K and V that rank r gathers from their
+ *               owners (token t lives on rank t / c)
+ *   local_perm  out [span]: local row of the token at span position j; the
+ *               relabelling is monotone, so sa_forward on (local rows,
+ *               local_perm, the same window and causal rule) computes the
+ *               owned positions' rows exactly as the whole sequence would
+ *   span_begin  out: first permuted position of the span
+ *   own_begin, own_end  out: the permuted positions rank r owns; their rows
+ *               are local rows local_perm[own - span_begin] of the local
+ *               output, for tokens perm[own], returned to their owners
+ * capacity >= sa_shard_span(n, window, world, rank).  perm_host is the
+ * whole sigma (host int32 [n]) and must be a permutation (SA_ERR_BAD_PERM
+ * otherwise).  Host only, O(n + span log span).
+ */
+int32_t sa_shard_span(int32_t n, int32_t window, int32_t world, int32_t rank);
+sa_status_t sa_shard_plan(const int32_t* perm_host, int32_t n, int32_t window, int32_t world,
+                          int32_t rank, int32_t* tokens, int32_t* local_perm, int32_t capacity,
+                          int32_t* span_begin, int32_t* own_begin, int32_t* own_end);
+
+/*
  * Host: draw sigma ~ Uniform(S_n) for (seed, layer, batch_index) ("Core
  * mechanism" step 1: one independent permutation per layer) into perm_host
  * (int32[n], caller-owned).  Generator: the stream state is the output of one

@@ -45,6 +45,10 @@ SIGNATURES = {
     "sa_receptive_field": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,
                                      c_int32, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
     "sa_make_perm": (c_int32, [c_uint64, c_int32, c_int32, c_int32, POINTER(c_int32)]),
+    "sa_shard_span": (c_int32, [c_int32, c_int32, c_int32, c_int32]),
+    "sa_shard_plan": (c_int32, [POINTER(c_int32), c_int32, c_int32, c_int32, c_int32,
+                                POINTER(c_int32), POINTER(c_int32), c_int32, POINTER(c_int32),
+                                POINTER(c_int32), POINTER(c_int32)]),
     "sa_check_error": (c_int32, [c_void_p, c_void_p]),
     "sa_clear_error": (c_int32, [c_void_p, c_void_p]),
     "sa_set_wait_limit": (c_int32, [c_int64]),

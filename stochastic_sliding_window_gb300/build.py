@@ -22,7 +22,7 @@ BUILD = PKG / "_build"
 LIB = PKG / "libsa.so"
 
 SOURCES = ["sa_api.cu", "sa_perm.cu", "sa_simt.cu", "sa_tc.cu", "sa_tc_ring.cu", "sa_tc_chunk.cu",
-           "sa_bwd.cu", "sa_graph.cu", "sa_prologue.cu"]
+           "sa_bwd.cu", "sa_graph.cu", "sa_prologue.cu", "sa_shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]
