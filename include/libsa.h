@@ -122,6 +122,10 @@ sa_status_t swa_forward(const sa_params_t* params, const void* q, const void* k,
  * head, broadcast over head_dim.  The merge happens in place in out (the SWA
  * term is written first, the SA term is added by the second kernel), so the
  * workspace is unused: pass NULL / 0 (sa_gated_workspace_size returns 0).
+ * Rounding: on the tensor-core kernels the SWA term is stored in out as bf16
+ * and the SA pass adds its term in fp32 and rounds again (two bf16
+ * roundings); the CUDA-core kernel (SA_KERNEL_SIMT) merges in registers and
+ * rounds once.
  */
 sa_status_t sa_swa_gated_forward(const sa_params_t* params, const void* q, const void* k,
                                  const void* v, const int32_t* perm, const float* gate_sa_logits,

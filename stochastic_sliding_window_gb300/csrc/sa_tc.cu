@@ -605,11 +605,37 @@ bool encode_row_map(CUtensorMap* m, const void* base, uint64_t rows, int d, int 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace tc {
+// Whether the variant was compiled to the launch register count its
+// register split assumes (checked once per variant).
+template <int D>
+static bool regs_ok(int nch) {
+  static int cache[6] = {-1, -1, -1, -1, -1, -1};
+  const int i = nch < 0 ? 0 : (nch > 5 ? 0 : nch);
+  if (cache[i] < 0) {
+    cudaFuncAttributes fa;
+    cudaError_t ce;
+    switch (i) {
+      case 1: ce = cudaFuncGetAttributes(&fa, sa_tc_kernel<D, 1>); break;
+      case 2: ce = cudaFuncGetAttributes(&fa, sa_tc_kernel<D, 2>); break;
+      case 3: ce = cudaFuncGetAttributes(&fa, sa_tc_kernel<D, 3>); break;
+      case 4: ce = cudaFuncGetAttributes(&fa, sa_tc_kernel<D, 4>); break;
+      case 5: ce = cudaFuncGetAttributes(&fa, sa_tc_kernel<D, 5>); break;
+      default: ce = cudaFuncGetAttributes(&fa, sa_tc_kernel<D, 0>); break;
+    }
+    cache[i] = (ce == cudaSuccess && fa.numRegs == kLaunchRegs) ? 1 : 0;
+  }
+  return cache[i] == 1;
+}
+}  // namespace tc
+
 bool tc_supported(const Problem& pb, Path path) {
   if (path != kPathSA && path != kPathSWA) return false;
   if (!tc::device_has_tcgen05(nullptr)) return false;
   tc::Config c;
-  return tc::make_config(pb, path, c);
+  if (!tc::make_config(pb, path, c)) return false;
+  const int nch = c.span_pad / 32 <= tc::kMaxRegChunks ? c.span_pad / 32 : 0;
+  return pb.d == 128 ? tc::regs_ok<128>(nch) : tc::regs_ok<64>(nch);
 }
 
 sa_status_t launch_tc(const Problem& pb, Path path, const float* gate, int accumulate,

@@ -761,11 +761,27 @@ static cudaError_t launch_one(int grid, uint32_t smem, cudaStream_t stream, cons
 
 }  // namespace chunk
 
+namespace chunk {
+// Whether the variant was compiled to the launch register count its
+// setmaxnreg split assumes (checked once per variant).
+template <int D>
+static bool regs_ok() {
+  static int cache = -1;
+  if (cache < 0) {
+    cudaFuncAttributes fa;
+    const cudaError_t ce = cudaFuncGetAttributes(&fa, sa_chunk_kernel<D>);
+    cache = (ce == cudaSuccess && fa.numRegs == kLaunchRegs) ? 1 : 0;
+  }
+  return cache == 1;
+}
+}  // namespace chunk
+
 bool chunk_supported(const Problem& pb, Path path) {
   if (path != kPathSA && path != kPathSWA) return false;
   if (!chunk::device_sm103(nullptr)) return false;
   chunk::Config c;
-  return chunk::make_config(pb, path, c);
+  if (!chunk::make_config(pb, path, c)) return false;
+  return pb.d == 128 ? chunk::regs_ok<128>() : chunk::regs_ok<64>();
 }
 
 sa_status_t launch_chunk(const Problem& pb, Path path, const float* gate, int accumulate,

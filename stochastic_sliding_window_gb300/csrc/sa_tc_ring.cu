@@ -846,13 +846,38 @@ static cudaError_t launch_variant(int nch, int grid, uint32_t smem, cudaStream_t
   }
 }
 
+// Whether the variant a shape launches was compiled to exactly the launch
+// register count its setmaxnreg split assumes (checked once per variant), so
+// that the automatic kernel choice never picks a kernel that would refuse to
+// launch.
+template <int D>
+static bool regs_ok(int nch) {
+  static int cache[6] = {-1, -1, -1, -1, -1, -1};
+  const int i = nch < 1 ? 1 : (nch > 5 ? 5 : nch);
+  if (cache[i] < 0) {
+    cudaFuncAttributes fa;
+    cudaError_t ce;
+    switch (i) {
+      case 1: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 1>); break;
+      case 2: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 2>); break;
+      case 3: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 3>); break;
+      case 4: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 4>); break;
+      default: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 5>); break;
+    }
+    cache[i] = (ce == cudaSuccess && fa.numRegs == kLaunchRegs) ? 1 : 0;
+  }
+  return cache[i] == 1;
+}
+
 }  // namespace ring
 
 bool ring_supported(const Problem& pb, Path path) {
   if (path != kPathSA && path != kPathSWA) return false;
   if (!ring::device_sm103(nullptr)) return false;
   ring::Config c;
-  return ring::make_config(pb, path, c);
+  if (!ring::make_config(pb, path, c)) return false;
+  const int nch = c.span_pad / 32;
+  return pb.d == 128 ? ring::regs_ok<128>(nch) : ring::regs_ok<64>(nch);
 }
 
 sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int accumulate,
