@@ -46,7 +46,7 @@ struct GateParams {
   long long timeout_cycles;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) sa_gate_proj_kernel(const __grid_constant__ GateParams P) {
+__global__ void __launch_bounds__(kThreads, 2) sa_gate_proj_kernel(const __grid_constant__ GateParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -206,13 +206,26 @@ __global__ void __launch_bounds__(kThreads) sa_rope_kernel(const __grid_constant
   }
   __syncthreads();
   __nv_bfloat16* base = P.x + size_t(row) * P.H * P.d;
-  for (int idx = threadIdx.x; idx < P.H * half; idx += blockDim.x) {
-    const int h = idx / half, k = idx - (idx / half) * half;
-    __nv_bfloat16* px = base + size_t(h) * P.d;
-    const float lo = __bfloat162float(px[k]), hi = __bfloat162float(px[k + half]);
-    const float c = s_cos[k], s = s_sin[k];
-    px[k] = __float2bfloat16_rn(lo * c - hi * s);
-    px[k + half] = __float2bfloat16_rn(hi * c + lo * s);
+  if ((half & 1) == 0) {  // two adjacent pairs per thread, bf16x2 accesses
+    const int h2 = half / 2;
+    for (int idx = threadIdx.x; idx < P.H * h2; idx += blockDim.x) {
+      const int h = idx / h2, k = 2 * (idx - (idx / h2) * h2);
+      __nv_bfloat162* plo = reinterpret_cast<__nv_bfloat162*>(base + size_t(h) * P.d + k);
+      __nv_bfloat162* phi = reinterpret_cast<__nv_bfloat162*>(base + size_t(h) * P.d + k + half);
+      const float2 lo = __bfloat1622float2(*plo), hi = __bfloat1622float2(*phi);
+      const float c0 = s_cos[k], s0 = s_sin[k], c1 = s_cos[k + 1], s1 = s_sin[k + 1];
+      *plo = __floats2bfloat162_rn(lo.x * c0 - hi.x * s0, lo.y * c1 - hi.y * s1);
+      *phi = __floats2bfloat162_rn(hi.x * c0 + lo.x * s0, hi.y * c1 + lo.y * s1);
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < P.H * half; idx += blockDim.x) {
+      const int h = idx / half, k = idx - (idx / half) * half;
+      __nv_bfloat16* px = base + size_t(h) * P.d;
+      const float lo = __bfloat162float(px[k]), hi = __bfloat162float(px[k + half]);
+      const float c = s_cos[k], s = s_sin[k];
+      px[k] = __float2bfloat16_rn(lo * c - hi * s);
+      px[k + half] = __float2bfloat16_rn(hi * c + lo * s);
+    }
   }
 }
 
@@ -247,11 +260,16 @@ sa_status_t launch_gate_projection(const void* x, int tokens, int d_model, int h
   P.w_bytes = uint32_t(P.n_pad) * 128;
   P.off_bar = 2 * (P.x_bytes + P.w_bytes);
   P.timeout_cycles = wait_limit_cycles();
-  const uint32_t smem = P.off_bar + 32 + 1024;
+  // at least 80 KB per CTA: at most two CTAs share an SM, so their two
+  // 256-column TMEM allocations always fit
+  const uint32_t need = P.off_bar + 32 + 1024;
+  const uint32_t smem = need > 80u * 1024 ? need : 80u * 1024;
   cudaError_t ce = cudaFuncSetAttribute(sa_gate_proj_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (ce == cudaSuccess) {
-    const int grid = P.num_tiles < sms ? P.num_tiles : sms;
+    // two CTAs per SM (256 TMEM columns each) so one's loads overlap the
+    // other's MMAs and epilogue
+    const int grid = P.num_tiles < 2 * sms ? P.num_tiles : 2 * sms;
     sa_gate_proj_kernel<<<grid, kThreads, smem, stream>>>(P);
     ce = cudaGetLastError();
   }
