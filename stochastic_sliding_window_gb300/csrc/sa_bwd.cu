@@ -46,7 +46,7 @@ namespace bwd {
 
 using namespace tcc;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr uint32_t kMaxSmem = 232448;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -202,6 +202,9 @@ __device__ __forceinline__ void write_row(const Params& P, void* base, size_t ro
 }
 
 // ------------------------------------------------------------------ dQ
+// 256 threads: warp w reads TMEM lane quarter w % 4 (rows 32 (w % 4) ..),
+// and the two warps of a quarter split each row's 32-column pieces between
+// them (piece ch goes to half ch % 2); row reductions meet in shared memory.
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
@@ -211,9 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
   volatile int* abort_flag;
   const uint32_t tmem_base = cta_setup(P, smem, bars, abort_flag);
   int32_t* sig = reinterpret_cast<int32_t*>(smem + P.off_sig);  // span column -> token (-1: none)
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int t = tid >> P.log2g, j = tid & (P.g - 1);
-  const uint32_t trow = tmem_base + (uint32_t(warp * 32) << 16);
+  float* red = reinterpret_cast<float*>(smem + P.off_col);       // [3][2][128] row partials
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, part = warp >> 2;
+  const int r = quarter * 32 + lane;  // this thread's TMEM lane = MMA row
+  const int t = r >> P.log2g, j = r & (P.g - 1);
+  const uint32_t trow = tmem_base + (uint32_t(quarter * 32) << 16);
   const uint32_t sq = sbase + P.off_q, sdy = sbase + P.off_dy, sk = sbase + P.off_k,
                  sv = sbase + P.off_v;
   const int sp = P.span_pad;
@@ -239,11 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
     // Q and dY rows of the tile (r = t*g + j), K and V rows of the span;
     // rows past the sequence end read token 0 and are never written.
     const size_t qh = size_t(kvh) * P.g;
-    auto qrow = [&](int r) {
-      const int tk = max(sig[P.left + (r >> P.log2g)], 0);
-      return ((tokb + tk) * P.Hq + qh + (r & (P.g - 1))) * D;
+    auto qrow = [&](int rr) {
+      const int tk = max(sig[P.left + (rr >> P.log2g)], 0);
+      return ((tokb + tk) * P.Hq + qh + (rr & (P.g - 1))) * D;
     };
-    auto krow = [&](int s) { return ((tokb + max(sig[s], 0)) * P.Hkv + kvh) * D; };
+    auto krow = [&](int s_) { return ((tokb + max(sig[s_], 0)) * P.Hkv + kvh) * D; };
     gather_rows<D>(sq, kBM * 128, kBM, P.q, qrow);
     gather_rows<D>(sdy, kBM * 128, kBM, P.dy, qrow);
     gather_rows<D>(sk, sp * 128, sp, P.k, krow);
@@ -293,49 +299,59 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
       return bits;
     };
     const int nch = sp / 32;
-    // pass 1: the attended maximum of the raw scores
+    // pass 1: the attended maximum of the raw scores (this half's pieces)
     float mx = -INFINITY;
 #pragma unroll 1
-    for (int ch = 0; ch < nch; ++ch) {
-      uint32_t s[32];
-      tmem_ld32(trow + ch * 32, s);
+    for (int ch = part; ch < nch; ch += 2) {
+      uint32_t s_[32];
+      tmem_ld32(trow + ch * 32, s_);
       const uint32_t bits = bits_of(ch);
 #pragma unroll
       for (int e = 0; e < 32; ++e)
-        if ((bits >> e) & 1u) mx = fmaxf(mx, __uint_as_float(s[e]));
+        if ((bits >> e) & 1u) mx = fmaxf(mx, __uint_as_float(s_[e]));
     }
+    red[part * kBM + r] = mx;
+    __syncthreads();
+    mx = fmaxf(red[r], red[kBM + r]);
     const float ms = mx == -INFINITY ? 0.f : mx * P.scale_log2;
     // pass 2: normaliser l and sum of e * dP
     float l = 0.f, pd = 0.f;
 #pragma unroll 1
-    for (int ch = 0; ch < nch; ++ch) {
-      uint32_t s[32], dp[32];
-      tmem_ld32(trow + ch * 32, s);
+    for (int ch = part; ch < nch; ch += 2) {
+      uint32_t s_[32], dp[32];
+      tmem_ld32(trow + ch * 32, s_);
       tmem_ld32(trow + sp + ch * 32, dp);
       const uint32_t bits = bits_of(ch);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float ex = (bits >> e) & 1u ? fast_exp2(fmaf(__uint_as_float(s[e]), P.scale_log2, -ms))
+        const float ex = (bits >> e) & 1u ? fast_exp2(fmaf(__uint_as_float(s_[e]), P.scale_log2, -ms))
                                           : 0.f;
         l += ex;
         pd = fmaf(ex, __uint_as_float(dp[e]), pd);
       }
     }
+    red[2 * kBM + part * kBM + r] = l;
+    red[4 * kBM + part * kBM + r] = pd;
+    __syncthreads();
+    l = red[2 * kBM + r] + red[3 * kBM + r];
+    pd = red[4 * kBM + r] + red[5 * kBM + r];
     const float dsum = l > 0.f ? pd / l : 0.f;
     float gl = 1.f;
     if (P.gate != nullptr && row_valid) gl = 1.f / (1.f + expf(-P.gate[orow]));
     // p' = g * p = 2^(s * scale * log2e - lse2'), lse2' = log2(l) + ms - log2(g)
     const float lse2 = ms + log2f(l > 0.f ? l : 1.f) - log2f(gl);
-    if (row_valid) {
+    if (row_valid && part == 0) {
       P.lse2[orow] = lse2;
       P.dsum[orow] = dsum;
       if (P.dgate != nullptr) P.dgate[orow] = gl * (1.f - gl) * dsum;
     }
-    // pass 3: dS = p' (dP - D), bf16, over the row's own S columns
+    // pass 3: dS = p' (dP - D), bf16, over the first 16 columns of the same
+    // 32-column S piece (the two warps of a row work on different pieces at
+    // once, so nothing may land on a piece the other warp still reads)
 #pragma unroll 1
-    for (int ch = 0; ch < nch; ++ch) {
-      uint32_t s[32], dp[32];
-      tmem_ld32(trow + ch * 32, s);
+    for (int ch = part; ch < nch; ch += 2) {
+      uint32_t s_[32], dp[32];
+      tmem_ld32(trow + ch * 32, s_);
       tmem_ld32(trow + sp + ch * 32, dp);
       const uint32_t bits = bits_of(ch);
       uint32_t pk[16];
@@ -346,24 +362,26 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
         for (int u = 0; u < 2; ++u) {
           const int e = 2 * e2 + u;
           const float p = (bits >> e) & 1u
-                              ? fast_exp2(fmaf(__uint_as_float(s[e]), P.scale_log2, -lse2))
+                              ? fast_exp2(fmaf(__uint_as_float(s_[e]), P.scale_log2, -lse2))
                               : 0.f;
           d2[u] = p * (__uint_as_float(dp[e]) - dsum);
         }
         pk[e2] = pack_bf16x2(d2[0], d2[1]);
       }
-      tmem_st16(trow + ch * 16, pk);
+      tmem_st16(trow + ch * 32, pk);
     }
     tmem_wait_st();
     tc_fence_before();
     __syncthreads();
-    // dQ = dS K: A = dS from TMEM, B = the span's K rows (MN-major)
+    // dQ = dS K: A = dS from TMEM (16 key columns per K step, packed in the
+    // first half of each 32-column piece), B = the span's K rows (MN-major)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t id = idesc_bf16(kBM, D, 1);
       uint64_t bd = sdesc_sw128(sk, sp * 128, 1024);
       for (int kk = 0; kk < sp / 16; ++kk) {
-        umma_bf16_ts(tmem_base + sp, tmem_base + 8 * kk, bd, id, kk > 0 ? 1u : 0u);
+        umma_bf16_ts(tmem_base + sp, tmem_base + (kk >> 1) * 32 + (kk & 1) * 8, bd, id,
+                     kk > 0 ? 1u : 0u);
         bd += 128;  // 16 key rows of 128 B
       }
       umma_commit(bars + 8 * kBarMma);
@@ -373,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
     tc_fence_after();
     // tcgen05.ld is warp-collective: every lane loads, valid rows store.
 #pragma unroll 1
-    for (int ch = 0; ch < D / 32; ++ch) {
+    for (int ch = part; ch < D / 32; ch += 2) {
       uint32_t o[32];
       tmem_ld32(trow + sp + ch * 32, o);
       if (row_valid) write_row<D>(P, P.dq, orow, o, ch * 32, P.scale);
@@ -385,6 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
 }
 
 // ------------------------------------------------------------------ dK, dV
+// 256 threads as in the dQ kernel (two warps per TMEM lane quarter, pieces
+// split between them).  The query chunks' Q and dY rows are double-buffered:
+// chunk c + 1 is gathered while chunk c is computed.
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
@@ -394,13 +415,15 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
   volatile int* abort_flag;
   const uint32_t tmem_base = cta_setup(P, smem, bars, abort_flag);
   int32_t* ktok = reinterpret_cast<int32_t*>(smem + P.off_sig);  // [128] key tokens (-1: none)
-  int32_t* qtok = ktok + kBM;                                    // [Bt] chunk query tokens
-  float* col_lse = reinterpret_cast<float*>(smem + P.off_col);   // [128] per chunk row
-  float* col_d = col_lse + kBM;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const uint32_t trow = tmem_base + (uint32_t(warp * 32) << 16);
-  const uint32_t sq = sbase + P.off_q, sdy = sbase + P.off_dy, sk = sbase + P.off_k,
-                 sv = sbase + P.off_v;
+  int32_t* qtok = ktok + kBM;                                    // [2][128] chunk query tokens
+  float* col_lse = reinterpret_cast<float*>(smem + P.off_col);   // [2][128] per chunk row
+  float* col_d = col_lse + 2 * kBM;                              // [2][128]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, part = warp >> 2;
+  const int m = quarter * 32 + lane;  // this thread's key row (TMEM lane)
+  const uint32_t trow = tmem_base + (uint32_t(quarter * 32) << 16);
+  const uint32_t sk = sbase + P.off_k, sv = sbase + P.off_v;
+  const uint32_t chunk_bytes = kBM * D * 2;
   const uint32_t c_st = 0, c_dpt = kBM, c_dv = 2 * kBM, c_dk = 2 * kBM + D;  // TMEM columns
   uint32_t mma_phase = 0;
   for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x) {
@@ -408,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
     const int k0 = (tile - seq * P.tiles_per_seq) * kBM;
     const int b = seq / P.Hkv, kvh = seq - (seq / P.Hkv) * P.Hkv;
     const size_t tokb = size_t(b) * P.n;
-    {
+    if (tid < kBM) {
       const int pos = k0 + tid;
       int tok = -1;
       if (pos < P.n) {
@@ -421,20 +444,21 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
       ktok[tid] = tok;
     }
     __syncthreads();
-    auto krow = [&](int m) { return ((tokb + max(ktok[m], 0)) * P.Hkv + kvh) * D; };
+    auto krow = [&](int mm) { return ((tokb + max(ktok[mm], 0)) * P.Hkv + kvh) * D; };
     gather_rows<D>(sk, kBM * 128, kBM, P.k, krow);
     gather_rows<D>(sv, kBM * 128, kBM, P.v, krow);
     // Query positions whose window covers a key of the tile.
     const int qlo = max(0, k0 - P.right);
     const int qhi = min(P.n - 1, k0 + kBM - 1 + P.left);
     const int nchunks = (qhi - qlo + P.Bt) / P.Bt;
-    const int kpos = k0 + tid;
-    const int sig_k = ktok[tid];
+    const int kpos = k0 + m;
+    const int sig_k = ktok[m];
     const size_t qh = size_t(kvh) * P.g;
-    bool alive = true;
-    for (int c = 0; c < nchunks && alive; ++c) {
+    // Tokens, rows and per-row values of chunk c into stage st (every
+    // thread; ends with the chunk's copies committed as one group).
+    auto prepare = [&](int c, int st) {
       const int c0 = qlo + c * P.Bt;
-      if (c > 0) __syncthreads();  // the previous chunk's tokens and rows are no longer read
+      int32_t* qt = qtok + st * kBM;
       for (int i = tid; i < P.Bt; i += kThreads) {
         const int pos = c0 + i;
         int tok = -1;
@@ -442,24 +466,38 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
           tok = P.perm ? __ldg(P.perm + tokb + pos) : pos;
           if (unsigned(tok) >= unsigned(P.n)) tok = -1;  // reported by the dQ kernel
         }
-        qtok[i] = tok;
+        qt[i] = tok;
       }
       __syncthreads();
-      auto qrow = [&](int r) {
-        const int tk = max(qtok[r >> P.log2g], 0);
-        return ((tokb + tk) * P.Hq + qh + (r & (P.g - 1))) * D;
+      auto qrow = [&](int rr) {
+        const int tk = max(qt[rr >> P.log2g], 0);
+        return ((tokb + tk) * P.Hq + qh + (rr & (P.g - 1))) * D;
       };
-      gather_rows<D>(sq, kBM * 128, kBM, P.q, qrow);
-      gather_rows<D>(sdy, kBM * 128, kBM, P.dy, qrow);
-      {
-        const int tk = qtok[tid >> P.log2g];
+      gather_rows<D>(sbase + P.off_q + st * chunk_bytes, kBM * 128, kBM, P.q, qrow);
+      gather_rows<D>(sbase + P.off_dy + st * chunk_bytes, kBM * 128, kBM, P.dy, qrow);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (tid < kBM) {
+        const int tk = qt[tid >> P.log2g];
         const size_t orow = (tokb + max(tk, 0)) * P.Hq + qh + (tid & (P.g - 1));
-        col_lse[tid] = tk >= 0 ? P.lse2[orow] : INFINITY;  // 2^(-inf): nothing from that row
-        col_d[tid] = tk >= 0 ? P.dsum[orow] : 0.f;
+        col_lse[st * kBM + tid] = tk >= 0 ? P.lse2[orow] : INFINITY;  // 2^(-inf): nothing
+        col_d[st * kBM + tid] = tk >= 0 ? P.dsum[orow] : 0.f;
       }
-      asm volatile("cp.async.wait_all;" ::: "memory");
+    };
+    prepare(0, 0);
+    bool alive = true;
+    for (int c = 0; c < nchunks && alive; ++c) {
+      const int st = c & 1;
+      const int c0 = qlo + c * P.Bt;
+      asm volatile("cp.async.wait_all;" ::: "memory");  // chunk c (and the tile's K, V)
       fence_proxy_async_smem();
       __syncthreads();
+      // The other stage was last read by chunk c - 1, whose MMAs are done.
+      if (c + 1 < nchunks) prepare(c + 1, st ^ 1);
+      const uint32_t sq = sbase + P.off_q + st * chunk_bytes;
+      const uint32_t sdy = sbase + P.off_dy + st * chunk_bytes;
+      const int32_t* qt = qtok + st * kBM;
+      const float* cl = col_lse + st * kBM;
+      const float* cd = col_d + st * kBM;
       if (tid == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16(kBM, kBM, 0);
@@ -480,11 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
       mma_phase ^= 1;
       tc_fence_after();
       // P'^T = 2^(s * scale * log2e - lse2') and dS^T = P'^T (dP^T - D) for
-      // attended (key, query row) pairs, bf16 over S^T and dP^T.
+      // attended (key, query row) pairs, bf16 over the first 16 columns of
+      // their own 32-column pieces of S^T and dP^T.
 #pragma unroll 1
-      for (int ch = 0; ch < kBM / 32; ++ch) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(trow + c_st + ch * 32, s);
+      for (int ch = part; ch < kBM / 32; ch += 2) {
+        uint32_t s_[32], dp[32];
+        tmem_ld32(trow + c_st + ch * 32, s_);
         tmem_ld32(trow + c_dpt + ch * 32, dp);
         uint32_t pk[16], dk2[16];
 #pragma unroll
@@ -492,23 +531,23 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
           float pv[2], dv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int r = ch * 32 + 2 * e2 + u;
-            const int tq = r >> P.log2g;
+            const int rr = ch * 32 + 2 * e2 + u;
+            const int tq = rr >> P.log2g;
             const int qpos = c0 + tq;
-            const int qt = qtok[tq];
-            bool ok = sig_k >= 0 && qt >= 0 && kpos >= qpos - P.left && kpos <= qpos + P.right;
-            if (kCausal) ok = ok && sig_k <= qt;
-            const float p = ok ? fast_exp2(fmaf(__uint_as_float(s[2 * e2 + u]), P.scale_log2,
-                                                -col_lse[r]))
+            const int qtk = qt[tq];
+            bool ok = sig_k >= 0 && qtk >= 0 && kpos >= qpos - P.left && kpos <= qpos + P.right;
+            if (kCausal) ok = ok && sig_k <= qtk;
+            const float p = ok ? fast_exp2(fmaf(__uint_as_float(s_[2 * e2 + u]), P.scale_log2,
+                                                -cl[rr]))
                                : 0.f;
             pv[u] = p;
-            dv[u] = p * (__uint_as_float(dp[2 * e2 + u]) - col_d[r]);
+            dv[u] = p * (__uint_as_float(dp[2 * e2 + u]) - cd[rr]);
           }
           pk[e2] = pack_bf16x2(pv[0], pv[1]);
           dk2[e2] = pack_bf16x2(dv[0], dv[1]);
         }
-        tmem_st16(trow + c_st + ch * 16, pk);
-        tmem_st16(trow + c_dpt + ch * 16, dk2);
+        tmem_st16(trow + c_st + ch * 32, pk);
+        tmem_st16(trow + c_dpt + ch * 32, dk2);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -520,8 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
         uint64_t by = sdesc_sw128(sdy, kBM * 128, 1024), bq = sdesc_sw128(sq, kBM * 128, 1024);
         for (int kk = 0; kk < kBM / 16; ++kk) {
           const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
-          umma_bf16_ts(tmem_base + c_dv, tmem_base + c_st + 8 * kk, by, id, acc);
-          umma_bf16_ts(tmem_base + c_dk, tmem_base + c_dpt + 8 * kk, bq, id, acc);
+          const uint32_t a = uint32_t((kk >> 1) * 32 + (kk & 1) * 8);  // 16 rows per K step
+          umma_bf16_ts(tmem_base + c_dv, tmem_base + c_st + a, by, id, acc);
+          umma_bf16_ts(tmem_base + c_dk, tmem_base + c_dpt + a, bq, id, acc);
           by += 128;
           bq += 128;
         }
@@ -540,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
       // sequence store.
       const size_t krow_out = (tokb + max(sig_k, 0)) * P.Hkv + kvh;
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = part; ch < D / 32; ch += 2) {
         uint32_t o[32];
         tmem_ld32(trow + c_dv + ch * 32, o);
         if (sig_k >= 0) write_row<D>(P, P.dv, krow_out, o, ch * 32, 1.f);
@@ -565,9 +605,12 @@ __global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __r
 }
 
 // ------------------------------------------------------------------ host
+struct Layout {  // shared-memory layout of one of the two kernels
+  uint32_t off_q, off_dy, off_k, off_v, off_sig, off_col, off_bar, smem;
+};
 struct Config {
   int Bt, log2g, left, right, span_pad, tmem_alloc;
-  uint32_t off_q, off_dy, off_k, off_v, off_sig, off_col, off_bar, smem_dq, smem_dkv;
+  Layout dq, dkv;
 };
 
 static uint32_t round_up(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
@@ -589,18 +632,20 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
   c.span_pad = int(round_up(uint32_t(span), 32));
   c.tmem_alloc = 512;
   const uint32_t rowb = uint32_t(pb.d) * 2;
-  c.off_q = 0;
-  c.off_dy = c.off_q + kBM * rowb;
-  c.off_k = c.off_dy + kBM * rowb;
-  // dq: K and V of the span; dkv: K and V of the 128-key tile
-  const uint32_t kv_rows = uint32_t(c.span_pad > kBM ? c.span_pad : kBM);
-  c.off_v = c.off_k + kv_rows * rowb;
-  c.off_sig = c.off_v + kv_rows * rowb;
-  c.off_col = round_up(c.off_sig + 4u * uint32_t(kv_rows + kBM), 16);
-  c.off_bar = round_up(c.off_col + 8u * kBM, 64);
-  c.smem_dq = c.off_bar + 8 * kNumBars + 8 + 1024;
-  c.smem_dkv = c.smem_dq;
-  return c.smem_dq <= kMaxSmem;
+  // qstages: stages of the 128-row Q and dY blocks; kv_rows: K and V rows.
+  auto layout = [&](Layout& L, uint32_t qstages, uint32_t kv_rows) {
+    L.off_q = 0;
+    L.off_dy = L.off_q + qstages * kBM * rowb;
+    L.off_k = L.off_dy + qstages * kBM * rowb;
+    L.off_v = L.off_k + kv_rows * rowb;
+    L.off_sig = L.off_v + kv_rows * rowb;
+    L.off_col = round_up(L.off_sig + 4u * (kv_rows + 2 * kBM), 16);
+    L.off_bar = round_up(L.off_col + 4u * 6 * kBM, 64);  // dq: 3 x 2 x 128 partials; dkv: 2 x 2 x 128
+    L.smem = L.off_bar + 8 * kNumBars + 8 + 1024;
+  };
+  layout(c.dq, 1, uint32_t(c.span_pad));  // the query tile and its key span
+  layout(c.dkv, 2, kBM);                  // two query-chunk stages, the 128-key tile
+  return c.dq.smem <= kMaxSmem && c.dkv.smem <= kMaxSmem;
 }
 
 static bool device_sm103(int* sms) {
@@ -671,37 +716,41 @@ sa_status_t launch_bwd(const Problem& pb, Path path, const BwdArgs& a, cudaStrea
   P.scale = pb.scale;
   P.scale_log2 = pb.scale * kLog2e;
   P.tmem_alloc = c.tmem_alloc;
-  P.off_q = c.off_q;
-  P.off_dy = c.off_dy;
-  P.off_k = c.off_k;
-  P.off_v = c.off_v;
-  P.off_sig = c.off_sig;
-  P.off_col = c.off_col;
-  P.off_bar = c.off_bar;
+  auto use = [&](const Layout& L) {
+    P.off_q = L.off_q;
+    P.off_dy = L.off_dy;
+    P.off_k = L.off_k;
+    P.off_v = L.off_v;
+    P.off_sig = L.off_sig;
+    P.off_col = L.off_col;
+    P.off_bar = L.off_bar;
+  };
   P.timeout_cycles = wait_limit_cycles();
   // dQ over query tiles
+  use(c.dq);
   P.tiles_per_seq = (pb.n + c.Bt - 1) / c.Bt;
   P.num_tiles = P.tiles_per_seq * pb.B * pb.Hkv;
   int grid = P.num_tiles < sms ? P.num_tiles : sms;
   cudaError_t ce;
   const bool causal = P.causal != 0;
   if (pb.d == 128)
-    ce = causal ? launch_k(sa_bwd_dq_kernel<128, true>, grid, c.smem_dq, stream, P)
-                : launch_k(sa_bwd_dq_kernel<128, false>, grid, c.smem_dq, stream, P);
+    ce = causal ? launch_k(sa_bwd_dq_kernel<128, true>, grid, c.dq.smem, stream, P)
+                : launch_k(sa_bwd_dq_kernel<128, false>, grid, c.dq.smem, stream, P);
   else
-    ce = causal ? launch_k(sa_bwd_dq_kernel<64, true>, grid, c.smem_dq, stream, P)
-                : launch_k(sa_bwd_dq_kernel<64, false>, grid, c.smem_dq, stream, P);
+    ce = causal ? launch_k(sa_bwd_dq_kernel<64, true>, grid, c.dq.smem, stream, P)
+                : launch_k(sa_bwd_dq_kernel<64, false>, grid, c.dq.smem, stream, P);
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "backward dQ launch: %s", cudaGetErrorString(ce));
   // dK, dV over 128-key tiles
+  use(c.dkv);
   P.tiles_per_seq = (pb.n + kBM - 1) / kBM;
   P.num_tiles = P.tiles_per_seq * pb.B * pb.Hkv;
   grid = P.num_tiles < sms ? P.num_tiles : sms;
   if (pb.d == 128)
-    ce = causal ? launch_k(sa_bwd_dkv_kernel<128, true>, grid, c.smem_dkv, stream, P)
-                : launch_k(sa_bwd_dkv_kernel<128, false>, grid, c.smem_dkv, stream, P);
+    ce = causal ? launch_k(sa_bwd_dkv_kernel<128, true>, grid, c.dkv.smem, stream, P)
+                : launch_k(sa_bwd_dkv_kernel<128, false>, grid, c.dkv.smem, stream, P);
   else
-    ce = causal ? launch_k(sa_bwd_dkv_kernel<64, true>, grid, c.smem_dkv, stream, P)
-                : launch_k(sa_bwd_dkv_kernel<64, false>, grid, c.smem_dkv, stream, P);
+    ce = causal ? launch_k(sa_bwd_dkv_kernel<64, true>, grid, c.dkv.smem, stream, P)
+                : launch_k(sa_bwd_dkv_kernel<64, false>, grid, c.dkv.smem, stream, P);
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "backward dK/dV launch: %s", cudaGetErrorString(ce));
   return SA_OK;
 }
