@@ -12,10 +12,13 @@
 // sequence share all but Bt rows of their key span, so K and V live in a
 // ring of R = span + 2*Bt rows and each tile fetches only its Bt new rows
 // (plus its 128 Q rows); the first tile of a run fetches the whole span.
-// Producer warps fetch rows with 16-byte cp.async copies (the widest
-// random-row gather path measured on this part), computing the 128-byte
-// swizzle themselves.  Q and K of a tile are needed only by S = Q K^T, V only
-// by O = P V, so they land on separate barriers and are released separately:
+// Producer warps fetch rows with TMA four-row gathers (tile::gather4: one
+// 128-byte column block of four arbitrary rows per copy, swizzled by the
+// copy engine), spread over the lanes of seven warps: the copy engine's
+// intake grows with the number of warps issuing, and the copies take no
+// load/store-unit slots from the softmax warps.  Q and K of a tile are
+// needed only by S = Q K^T, V only by O = P V, so they land on separate
+// barriers and are released separately:
 // a Q stage is free once the S MMA of the tile two back has completed, the K
 // rows a tile overwrites once that of the tile three back has, V rows once
 // its O MMA has.  The sigma values of the next tile's new positions are
@@ -24,9 +27,8 @@
 // contiguous array.
 //
 // Roles (four warpgroups, 512 threads):
-//   warps 0-6   producers: sigma of new positions, cp.async of Q / K / V rows
-//               (seven warps, so that their copy streams hide each other's
-//               latency next to the softmax warps)
+//   warps 0-6   producers: sigma of new positions, TMA gathers of Q / K / V
+//               rows (seven warps issuing side by side)
 //   warp 7      lane 0 issues the MMAs (in whichever order their operands
 //               become ready); the warp owns TMEM
 //   warps 8-11  softmax + epilogue of even tiles (TMEM stage 0)
@@ -40,8 +42,8 @@
 // TMEM and V used MN-major straight from the ring; the epilogue scales by
 // 1/rowsum, optionally applies the gate and the previous out row, and
 // scatters row sigma[p0+t].
-// Every wait is bounded (SA_ERRBIT_TIMEOUT); producer copies are drained
-// before exit.
+// Every wait is bounded (SA_ERRBIT_TIMEOUT); the producers wait for their
+// last copies to land before exit.
 #include "sa_internal.h"
 #include "sa_tc_common.cuh"
 
@@ -87,9 +89,9 @@ struct Params {
 // Barrier slots (8 bytes each) after off_bar.  Q families are indexed by
 // it % kQStages, V families by it % kVDepth, warpgroup families by it & 1.
 enum : uint32_t {
-  kFullQK = 0,   // [kQStages] Q stage and new K rows of tile it landed (cp.async)
+  kFullQK = 0,   // [kQStages] Q stage and new K rows of tile it landed (TMA bytes)
   kQKdone = 3,   // [kQStages] S MMA of tile it done: its Q stage and K rows are free
-  kFullV = 6,    // [kVDepth] new V rows of tile it landed (cp.async)
+  kFullV = 6,    // [kVDepth] new V rows of tile it landed (TMA bytes)
   kPVdone = 9,   // [kVDepth] O MMA of tile it done: its V rows are free
   kSready = 12,  // [2] sigma of tile it written (per softmax warpgroup)
   kSfree = 14,   // [2] the warpgroup has read the sigma it needs for tile it
@@ -204,16 +206,15 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 }
 
 template <int D>
-__device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, uint32_t bars,
-                              volatile int* abort_flag, volatile int* votes) {
-  constexpr int CPR = D / 8;             // 16-byte chunks per row
-  constexpr int RPP = kProducers / CPR;  // rows per pass of the producer threads
-  constexpr int kBatch = 8;              // rows whose tokens are read before their copies
+__device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUtensorMap* tk,
+                              const CUtensorMap* tv, uint8_t* smem, uint32_t sbase,
+                              uint32_t bars, volatile int* abort_flag, volatile int* votes) {
+  constexpr int KB = D / 64;  // 128-byte column blocks per row
   const int tid = threadIdx.x;
-  const int c = tid % CPR;
-  const int r_first = tid / CPR;
-  const int kb = c >> 3;
-  const int c8 = c & 7;
+  // This thread's place in a tile's TMA issue order.  Consecutive copies go
+  // to different warps: one warp issues its lanes' copies one after another,
+  // while the seven warps' streams run side by side.
+  const int issue_idx = (tid & 31) * (kProducers / 32) + (tid >> 5);
   int32_t* sig2 = reinterpret_cast<int32_t*>(smem + P.off_sig);
   int32_t* vtok = reinterpret_cast<int32_t*>(smem + P.off_vtok);  // [2][span_pad] new tokens
   const uint32_t sk = sbase + P.off_k, sv = sbase + P.off_v;
@@ -249,41 +250,16 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
     }
   };
 
-  // V rows of tile x: they overwrite those of tile x - 3 (a new run: of
-  // every tile in flight); the Q/K barrier before them covers that wait.
-  auto v_upto = [&](int x, const TileWalk& w) { return w.new_seg ? x - 1 : x - kVDepth; };
-  auto load_v = [&](int x, const TileWalk& w) {
-    const int32_t* vt = vtok + (x & 1) * P.span_pad;
-    const size_t rowbase = size_t(w.b) * P.n;
-    for (int i0 = r_first; i0 < w.nld; i0 += RPP * kBatch) {
-      int tok[kBatch];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int i = i0 + RPP * k;
-        tok[k] = i < w.nld ? vt[i] : 0;
-      }
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int i = i0 + RPP * k;
-        if (i < w.nld) {
-          const int sl = w.slot_of(P, i);
-          const size_t off = ((rowbase + tok[k]) * P.Hkv + w.kvh) * D + c * 8;
-          cp_async16(sv + kb * (P.R * 128) + sl * 128 + ((c8 ^ (sl & 7)) << 4), P.v + off);
-        }
-      }
-    }
-    cp_async_arrive_noinc(bars + 8 * (kFullV + x % kVDepth));
-    return true;
-  };
-
-  // sigma, Q and K of tile it.  Its Q stage belongs to tile it - kQStages and
-  // the K rows it overwrites to tile it - 3 (a new run: to every tile in
-  // flight, and it rewrites the whole sigma ring, which the warpgroups of
-  // those tiles must have read: their O MMA being done implies it).
-  // pv_upto: the O MMAs the V load that follows in this iteration needs.
-  auto load_qk = [&](int it, const TileWalk& w, TileWalk& nx, int (&pre)[2], bool has_next,
-                     int pv_upto) {
+  // Tile it: its sigma, then TMA copies of its Q rows, new K rows and new V
+  // rows.  Its Q stage belongs to tile it - kQStages, the K and V rows it
+  // overwrites to tile it - 3 (a new run: to every tile in flight, and it
+  // rewrites the whole sigma ring, which the warpgroups of those tiles must
+  // have read: their O MMA being done implies it).
+  auto load = [&](int it, const TileWalk& w, TileWalk& nx, int (&pre)[2], bool has_next,
+                  int pv_upto) {
     const int s = it % kQStages;
+    const uint32_t full_qk = bars + 8 * (kFullQK + s);
+    const uint32_t full_v = bars + 8 * (kFullV + it % kVDepth);
     bool ok = true;
     if (tid == 0) {
       ok = retire(kQKdone, kQStages, qk_seen, w.new_seg ? it - 1 : it - kQStages);
@@ -306,52 +282,47 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
         vt[i] = tok;
       }
     }
+    if (tid == 0) {  // the bytes the tile's copies will deliver, before any is issued
+      const uint32_t kv_bytes = uint32_t(w.nld) * D * 2;
+      mbar_arrive_expect_tx(full_qk, P.q_bytes + kv_bytes);
+      mbar_arrive_expect_tx(full_v, kv_bytes);
+    }
     asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
     if (has_next) {  // loaded now, stored at the next tile
       nx.step(P, 0);
       fetch(nx, pre);
     }
-    // Q: 128 rows (r = t*g + j), 2 K-blocks of [128 rows x 128 B], swizzled.
+    // Each copy is a 4-row gather of one 128-byte column block, landing as
+    // 512 contiguous swizzled bytes: Q rows r = t*g + j (4 per copy), then the
+    // new K rows, then the new V rows (4 ring slots per copy; ring slots and
+    // counts are multiples of 4, so a group never wraps).
+    const int nq = (kBM / 4) * KB, nk = (w.nld / 4) * KB;
+    const int total = nq + 2 * nk;
     const uint32_t sq = sbase + uint32_t(s) * P.q_bytes;
-    const int32_t* sig_win = sig2 + w.slot_a;
-    const size_t rowbase = size_t(w.b) * P.n;
-    for (int r0 = r_first; r0 < kBM; r0 += RPP * kBatch) {
-      int tok[kBatch];
+    const int32_t* sig_win = sig2 + w.slot_a + P.left;
+    const int rowbase = w.b * P.n;
+    for (int i = issue_idx; i < total; i += kProducers) {
+      int rows[4];
+      if (i < nq) {
+        const int rg = i / KB, kb = i - rg * KB;
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int r = r0 + RPP * k;
-        tok[k] = r < kBM ? sig_win[P.left + (r >> P.log2g)] : 0;
-      }
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int r = r0 + RPP * k;
-        if (r < kBM) {
-          const int j = r & (P.g - 1);
-          const __nv_bfloat16* src =
-              P.q + ((rowbase + tok[k]) * P.Hq + w.kvh * P.g + j) * D + c * 8;
-          cp_async16(sq + kb * (kBM * 128) + r * 128 + ((c8 ^ (r & 7)) << 4), src);
+        for (int e = 0; e < 4; ++e) {
+          const int r = 4 * rg + e;
+          rows[e] = (rowbase + sig_win[r >> P.log2g]) * P.Hq + w.kvh * P.g + (r & (P.g - 1));
         }
+        tma_gather4(sq + kb * (kBM * 128) + rg * 512, tq, kb * 64, rows[0], rows[1], rows[2],
+                    rows[3], full_qk);
+      } else {
+        const bool is_v = i >= nq + nk;
+        const int x = i - nq - (is_v ? nk : 0);
+        const int gi = x / KB, kb = x - gi * KB;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rows[e] = (rowbase + vt[4 * gi + e]) * P.Hkv + w.kvh;
+        const uint32_t dst = kb * (P.R * 128) + w.slot_of(P, 4 * gi) * 128;
+        tma_gather4((is_v ? sv : sk) + dst, is_v ? tv : tk, kb * 64, rows[0], rows[1], rows[2],
+                    rows[3], is_v ? full_v : full_qk);
       }
     }
-    // K: the new positions of the span
-    for (int i0 = r_first; i0 < w.nld; i0 += RPP * kBatch) {
-      int tok[kBatch];
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int i = i0 + RPP * k;
-        tok[k] = i < w.nld ? vt[i] : 0;
-      }
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int i = i0 + RPP * k;
-        if (i < w.nld) {
-          const int sl = w.slot_of(P, i);
-          const size_t off = ((rowbase + tok[k]) * P.Hkv + w.kvh) * D + c * 8;
-          cp_async16(sk + kb * (P.R * 128) + sl * 128 + ((c8 ^ (sl & 7)) << 4), P.k + off);
-        }
-      }
-    }
-    cp_async_arrive_noinc(bars + 8 * (kFullQK + s));
     if (tid == 0) {
       // Hand sigma to the softmax warpgroup of this tile once it has read
       // what it needed from its previous tile (so this barrier is never two
@@ -373,14 +344,29 @@ __device__ void producer_role(const Params& P, uint8_t* smem, uint32_t sbase, ui
     nxt.step(P, begin);
     fetch(nxt, pre);
   }
-  // Iteration it loads sigma, Q, K and V of tile it; the V rows' wait is
-  // folded into the Q/K barrier.
+  // V rows of tile x overwrite those of tile x - 3 (a new run: of every tile
+  // in flight); the wait is folded into the tile's first wait.
+  int issued = 0;
   for (int it = 0; it < ntiles; ++it) {
     cur = nxt;
-    if (!load_qk(it, cur, nxt, pre, it + 1 < ntiles, v_upto(it, cur))) break;
-    if (!load_v(it, cur)) break;
+    const int pv_upto = cur.new_seg ? it - 1 : it - kVDepth;
+    if (!load(it, cur, nxt, pre, it + 1 < ntiles, pv_upto)) break;
+    issued = it + 1;
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");  // own copies land before exit
+  // The copies of the last tiles land before the CTA may exit (each barrier
+  // below was last armed by the tile waited for, so no wait is ambiguous).
+  if (tid == 0 && issued > 0) {
+    const int last = issued - 1;
+    auto drain = [&](uint32_t bar, uint32_t par) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(bar, par) && clock64() - t0 < kDrainCycles) {
+      }
+    };
+    for (int x = max(0, last - kQStages + 1); x <= last; ++x)
+      drain(bars + 8 * (kFullQK + x % kQStages), (x / kQStages) & 1);
+    for (int x = max(0, last - kVDepth + 1); x <= last; ++x)
+      drain(bars + 8 * (kFullV + x % kVDepth), (x / kVDepth) & 1);
+  }
 }
 
 template <int D>
@@ -393,7 +379,6 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   const uint32_t p_col = 0, o_col = uint32_t(P.span_pad / 2);
   auto qk = [&](int it, int slot_a) {
     const int s = it % kQStages, ts = it & 1;
-    fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
     tc_fence_after();
     const uint32_t d = tmem_base + uint32_t(ts * P.cols_stage);
     const uint32_t qa = sbase + uint32_t(s) * P.q_bytes;
@@ -419,7 +404,6 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   };
   auto pv = [&](int it, int slot_a) {
     const int s = it % kVDepth, ts = it & 1;
-    fence_proxy_async_smem();  // V rows landed by cp.async
     tc_fence_after();
     const uint32_t stage = tmem_base + uint32_t(ts * P.cols_stage);
     const int ksteps = P.span_pad / 16;
@@ -687,7 +671,9 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
 }
 
 template <int D, int NCH>
-__global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sa_ring_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
   // Align by pointer arithmetic on the shared array (not through an integer)
   // so the compiler keeps the shared address space: ld/st.shared, not generic.
@@ -700,11 +686,11 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
-      mbar_init(bars + 8 * (kFullQK + s), kProducers);
+      mbar_init(bars + 8 * (kFullQK + s), 1);
       mbar_init(bars + 8 * (kQKdone + s), 1);
     }
     for (int s = 0; s < kVDepth; ++s) {
-      mbar_init(bars + 8 * (kFullV + s), kProducers);
+      mbar_init(bars + 8 * (kFullV + s), 1);
       mbar_init(bars + 8 * (kPVdone + s), 1);
     }
     for (int w = 0; w < 2; ++w) {
@@ -746,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_ring_kernel(const __grid_const
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     if (warp < kMmaWarp) {
-      producer_role<D>(P, smem, sbase, bars, abort_flag, votes);
+      producer_role<D>(P, &tm_q, &tm_k, &tm_v, smem, sbase, bars, abort_flag, votes);
     } else {
       if ((threadIdx.x & 31) == 0) mma_role<D>(P, sbase, tmem_base, bars, abort_flag);
       __syncwarp();
@@ -816,8 +802,13 @@ static bool device_sm103(int* sms) {
   return major == 10 && minor == 3;
 }
 
+struct Maps {
+  CUtensorMap q, k, v;
+};
+
 template <int D, int NCH>
-static cudaError_t launch_one(int grid, uint32_t smem, cudaStream_t stream, const Params& P) {
+static cudaError_t launch_one(int grid, uint32_t smem, cudaStream_t stream, const Maps& m,
+                              const Params& P) {
   cudaError_t ce = cudaFuncSetAttribute(sa_ring_kernel<D, NCH>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (ce != cudaSuccess) return ce;
@@ -830,19 +821,19 @@ static cudaError_t launch_one(int grid, uint32_t smem, cudaStream_t stream, cons
                                                      smem);
   if (ce != cudaSuccess) return ce;
   if (resident < 1) return cudaErrorInvalidConfiguration;
-  sa_ring_kernel<D, NCH><<<grid, kThreads, smem, stream>>>(P);
+  sa_ring_kernel<D, NCH><<<grid, kThreads, smem, stream>>>(m.q, m.k, m.v, P);
   return cudaGetLastError();
 }
 
 template <int D>
 static cudaError_t launch_variant(int nch, int grid, uint32_t smem, cudaStream_t stream,
-                                  const Params& P) {
+                                  const Maps& m, const Params& P) {
   switch (nch) {
-    case 1: return launch_one<D, 1>(grid, smem, stream, P);
-    case 2: return launch_one<D, 2>(grid, smem, stream, P);
-    case 3: return launch_one<D, 3>(grid, smem, stream, P);
-    case 4: return launch_one<D, 4>(grid, smem, stream, P);
-    default: return launch_one<D, 5>(grid, smem, stream, P);
+    case 1: return launch_one<D, 1>(grid, smem, stream, m, P);
+    case 2: return launch_one<D, 2>(grid, smem, stream, m, P);
+    case 3: return launch_one<D, 3>(grid, smem, stream, m, P);
+    case 4: return launch_one<D, 4>(grid, smem, stream, m, P);
+    default: return launch_one<D, 5>(grid, smem, stream, m, P);
   }
 }
 
@@ -923,10 +914,17 @@ sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int acc
   P.off_bits = c.off_bits;
   P.off_bar = c.off_bar;
   P.timeout_cycles = wait_limit_cycles();
+  // Row maps of Q [B*n*Hq, d] and K, V [B*n*Hkv, d]: the producers gather
+  // four arbitrary rows per copy.
+  Maps m;
+  const uint64_t qrows = uint64_t(pb.B) * pb.n * pb.Hq, kvrows = uint64_t(pb.B) * pb.n * pb.Hkv;
+  if (!encode_row_map(&m.q, pb.q, qrows, pb.d, 1) || !encode_row_map(&m.k, pb.k, kvrows, pb.d, 1) ||
+      !encode_row_map(&m.v, pb.v, kvrows, pb.d, 1))
+    return fail(SA_ERR_CUDA, "ring kernel: tensor map encoding failed");
   const int grid = P.num_tiles < sms ? P.num_tiles : sms;
   const int nch = c.span_pad / 32;
-  const cudaError_t ce = (pb.d == 128) ? launch_variant<128>(nch, grid, c.smem_bytes, stream, P)
-                                       : launch_variant<64>(nch, grid, c.smem_bytes, stream, P);
+  const cudaError_t ce = (pb.d == 128) ? launch_variant<128>(nch, grid, c.smem_bytes, stream, m, P)
+                                       : launch_variant<64>(nch, grid, c.smem_bytes, stream, m, P);
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "ring kernel launch: %s", cudaGetErrorString(ce));
   return SA_OK;
 }
