@@ -12,38 +12,39 @@
 // sequence share all but Bt rows of their key span, so K and V live in a
 // ring of R = span + 2*Bt rows and each tile fetches only its Bt new rows
 // (plus its 128 Q rows); the first tile of a run fetches the whole span.
-// Producer warps fetch rows with TMA four-row gathers (tile::gather4: one
+// Copier warps fetch rows with TMA four-row gathers (tile::gather4: one
 // 128-byte column block of four arbitrary rows per copy, swizzled by the
-// copy engine), spread over the lanes of seven warps: the copy engine's
+// copy engine), spread over the lanes of five warps: the copy engine's
 // intake grows with the number of warps issuing, and the copies take no
 // load/store-unit slots from the softmax warps.  Q and K of a tile are
 // needed only by S = Q K^T, V only by O = P V, so they land on separate
-// barriers and are released separately:
-// a Q stage is free once the S MMA of the tile two back has completed, the K
-// rows a tile overwrites once that of the tile three back has, V rows once
-// its O MMA has.  The sigma values of the next tile's new positions are
-// loaded into registers one tile ahead.  The key tokens sigma[q] of the ring
-// are kept twice (slots s and s + R) so that a tile's span is always a plain
-// contiguous array.
+// barriers and are released separately: a Q stage is free once the S MMA
+// of the tile two back has completed, the K rows a tile overwrites once
+// that of the tile three back has, V rows once its O MMA has.  The sigma
+// values of the next tile's new positions are loaded into registers one
+// tile ahead.  The key tokens sigma[q] of the ring are kept twice (slots s
+// and s + R) so that a tile's span is always a plain contiguous array.
 //
 // Roles (four warpgroups, 512 threads):
-//   warps 0-6   producers: sigma of new positions, TMA gathers of Q / K / V
-//               rows (seven warps issuing side by side)
-//   warp 7      lane 0 issues the MMAs (in whichever order their operands
-//               become ready); the warp owns TMEM
-//   warps 8-11  softmax + epilogue of even tiles (TMEM stage 0)
-//   warps 12-15 softmax + epilogue of odd tiles  (TMEM stage 1)
+//   warps 0-4   copiers: sigma of new positions, TMA gathers of Q / K / V rows
+//   warps 5-6   maskers: the tile's mask words (one 32-bit word per token and
+//               32-key chunk, from sigma), then the hand-over to the tile's
+//               softmax warpgroup
+//   warp 7      lane 0 issues S = Q K^T of every tile in order; the warp
+//               owns TMEM
+//   warps 8-11  softmax, O MMA and epilogue of even tiles (TMEM stage 0)
+//   warps 12-15 softmax, O MMA and epilogue of odd tiles  (TMEM stage 1)
 // Per tile: S = Q K^T (one or two MMAs when the span wraps the ring) into
-// TMEM; each softmax warp builds the mask words of its tokens (one 32-bit
-// word per token and 32-key chunk) from sigma; each row's window is read
-// from TMEM in 32-column chunks in two passes (the attended maximum, then
-// exponentials) and P is written back to TMEM as bf16 over its own S
-// columns; O = P V with P taken from
-// TMEM and V used MN-major straight from the ring; the epilogue scales by
-// 1/rowsum, optionally applies the gate and the previous out row, and
-// scatters row sigma[p0+t].
-// Every wait is bounded (SA_ERRBIT_TIMEOUT); the producers wait for their
-// last copies to land before exit.
+// TMEM; each row's window is read from TMEM in 32-column chunks in two
+// passes (the attended maximum, then exponentials) and P is written back to
+// TMEM as bf16 over its own S columns; one thread of the warpgroup then
+// issues O = P V with P taken from TMEM and V used MN-major straight from
+// the ring (so no other warp has to notice that P is ready); the epilogue
+// scales by 1/rowsum, optionally applies the gate and the previous out row,
+// and scatters row sigma[p0+t].  Mask words and copies are thus off the
+// softmax warps' path, which is the longest per tile.
+// Every wait is bounded (SA_ERRBIT_TIMEOUT); the copiers wait for their last
+// copies to land, and each O issuer for its last MMA, before exit.
 #include "sa_internal.h"
 #include "sa_tc_common.cuh"
 
@@ -55,7 +56,8 @@ namespace ring {
 using namespace tcc;
 
 constexpr int kThreads = 512;
-constexpr int kProducers = 224;  // warps 0-6
+constexpr int kCopiers = 160;   // warps 0-4: sigma of new positions, TMA copies
+constexpr int kMaskers = 64;    // warps 5-6: mask words, sigma hand-off
 constexpr int kMmaWarp = 7;
 constexpr int kFirstSoftmaxWarp = 8;
 constexpr int kLaunchRegs = 128;
@@ -96,14 +98,16 @@ enum : uint32_t {
   kSready = 12,  // [2] sigma of tile it written (per softmax warpgroup)
   kSfree = 14,   // [2] the warpgroup has read the sigma it needs for tile it
   kSfull = 16,   // [2] S of tile it in TMEM stage it & 1
-  kPfull = 18,   // [2] P of tile it written to TMEM
+  kPfull = 18,   // [2] P of tile it written to TMEM (the warpgroup's 4 warps)
   kOfull = 20,   // [2] O of tile it in TMEM
   kTempty = 22,  // [2] TMEM stage read out by the epilogue
-  kDrain = 24,   // final MMA completion
-  kNumBars = 25,
+  kDrain = 24,   // final completion of the S MMAs
+  kDrainWg = 25, // [2] final completion of the warpgroup's O MMAs
+  kSigW = 27,    // [4] sigma of tile it written to the ring (copiers -> maskers)
+  kNumBars = 31,
 };
 static_assert(kFullQK + kQStages <= kQKdone && kQKdone + kQStages <= kFullV, "barrier slots");
-static_assert(32 * kMaxChunks <= 2 * kProducers, "a tile's new positions: two per producer thread");
+static_assert(32 * kMaxChunks <= 2 * kCopiers, "a tile's new positions: two per copier thread");
 
 // Tiles of this CTA: a contiguous range, split evenly over the grid.
 __device__ __forceinline__ void cta_range(const Params& P, int& begin, int& end) {
@@ -205,16 +209,17 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Copiers (warps 0-4): per tile, wait for the slots it reuses to retire,
+// write sigma of its new positions to the ring, then issue its TMA copies.
 template <int D>
-__device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUtensorMap* tk,
-                              const CUtensorMap* tv, uint8_t* smem, uint32_t sbase,
-                              uint32_t bars, volatile int* abort_flag, volatile int* votes) {
+__device__ void copy_role(const Params& P, const CUtensorMap* tq, const CUtensorMap* tk,
+                          const CUtensorMap* tv, uint8_t* smem, uint32_t sbase, uint32_t bars,
+                          volatile int* abort_flag, volatile int* votes) {
   constexpr int KB = D / 64;  // 128-byte column blocks per row
   const int tid = threadIdx.x;
-  // This thread's place in a tile's TMA issue order.  Consecutive copies go
-  // to different warps: one warp issues its lanes' copies one after another,
-  // while the seven warps' streams run side by side.
-  const int issue_idx = (tid & 31) * (kProducers / 32) + (tid >> 5);
+  // This thread's place in a tile's TMA issue order: consecutive copies go to
+  // different warps (a warp issues its lanes' copies one after another).
+  const int issue_idx = (tid & 31) * (kCopiers / 32) + (tid >> 5);
   int32_t* sig2 = reinterpret_cast<int32_t*>(smem + P.off_sig);
   int32_t* vtok = reinterpret_cast<int32_t*>(smem + P.off_vtok);  // [2][span_pad] new tokens
   const uint32_t sk = sbase + P.off_k, sv = sbase + P.off_v;
@@ -231,32 +236,32 @@ __device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUte
     if (ok && upto > seen) seen = upto;
     return ok;
   };
-  // Thread 0's verdict, shared with the other producers.
+  // Thread 0's verdict, shared with the other copiers.
   auto agree = [&](volatile int* slot, bool ok) {
     if (tid == 0) *slot = ok ? 1 : 0;
-    asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kCopiers) : "memory");
     return *slot != 0;
   };
-  // sigma of a tile's new positions (two per thread at most), into registers
+  // sigma of a tile's new positions (two per thread at most), into registers;
+  // unconditional loads of clamped positions, so nothing waits on them here
   auto fetch = [&](const TileWalk& w, int (&pre)[2]) {
-    const int32_t* perm_b = P.identity ? nullptr : P.perm + size_t(w.b) * P.n;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = tid + kProducers * k;
-      if (i < w.nld) {
-        const int qc = min(max(w.ld0 + i, 0), P.n - 1);
-        pre[k] = perm_b ? __ldg(perm_b + qc) : qc;
-      }
+    const int q0 = min(max(w.ld0 + tid, 0), P.n - 1);
+    const int q1 = min(max(w.ld0 + tid + kCopiers, 0), P.n - 1);
+    if (P.identity) {
+      pre[0] = q0;
+      pre[1] = q1;
+    } else {
+      const int32_t* perm_b = P.perm + size_t(w.b) * P.n;
+      pre[0] = __ldg(perm_b + q0);
+      pre[1] = __ldg(perm_b + q1);
     }
   };
-
   // Tile it: its sigma, then TMA copies of its Q rows, new K rows and new V
   // rows.  Its Q stage belongs to tile it - kQStages, the K and V rows it
   // overwrites to tile it - 3 (a new run: to every tile in flight, and it
   // rewrites the whole sigma ring, which the warpgroups of those tiles must
   // have read: their O MMA being done implies it).
-  auto load = [&](int it, const TileWalk& w, TileWalk& nx, int (&pre)[2], bool has_next,
-                  int pv_upto) {
+  auto load = [&](int it, const TileWalk& w, int (&pre)[2], int pv_upto) {
     const int s = it % kQStages;
     const uint32_t full_qk = bars + 8 * (kFullQK + s);
     const uint32_t full_v = bars + 8 * (kFullV + it % kVDepth);
@@ -269,7 +274,7 @@ __device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUte
     int32_t* vt = vtok + (it & 1) * P.span_pad;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int i = tid + kProducers * k;
+      const int i = tid + kCopiers * k;
       if (i < w.nld) {
         int tok = pre[k];
         if (unsigned(tok) >= unsigned(P.n)) {
@@ -287,11 +292,8 @@ __device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUte
       mbar_arrive_expect_tx(full_qk, P.q_bytes + kv_bytes);
       mbar_arrive_expect_tx(full_v, kv_bytes);
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kProducers) : "memory");
-    if (has_next) {  // loaded now, stored at the next tile
-      nx.step(P, 0);
-      fetch(nx, pre);
-    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kCopiers) : "memory");
+    if (tid == 0) mbar_arrive(bars + 8 * (kSigW + (it & 3)));  // sigma visible to the maskers
     // Each copy is a 4-row gather of one 128-byte column block, landing as
     // 512 contiguous swizzled bytes: Q rows r = t*g + j (4 per copy), then the
     // new K rows, then the new V rows (4 ring slots per copy; ring slots and
@@ -301,7 +303,7 @@ __device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUte
     const uint32_t sq = sbase + uint32_t(s) * P.q_bytes;
     const int32_t* sig_win = sig2 + w.slot_a + P.left;
     const int rowbase = w.b * P.n;
-    for (int i = issue_idx; i < total; i += kProducers) {
+    for (int i = issue_idx; i < total; i += kCopiers) {
       int rows[4];
       if (i < nq) {
         const int rg = i / KB, kb = i - rg * KB;
@@ -323,15 +325,6 @@ __device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUte
                     rows[3], is_v ? full_v : full_qk);
       }
     }
-    if (tid == 0) {
-      // Hand sigma to the softmax warpgroup of this tile once it has read
-      // what it needed from its previous tile (so this barrier is never two
-      // phases ahead of its waiter).  Done after this thread's copies so
-      // that the wait never delays them; the next tile's sigma writes come
-      // after it.
-      const int wg = it & 1;
-      if (wait(bars + 8 * (kSfree + wg), ((it >> 1) & 1) ^ 1)) mbar_arrive(bars + 8 * (kSready + wg));
-    }
     return true;
   };
 
@@ -350,8 +343,13 @@ __device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUte
   for (int it = 0; it < ntiles; ++it) {
     cur = nxt;
     const int pv_upto = cur.new_seg ? it - 1 : it - kVDepth;
-    if (!load(it, cur, nxt, pre, it + 1 < ntiles, pv_upto)) break;
+    const bool ok = load(it, cur, pre, pv_upto);
+    if (!ok) break;
     issued = it + 1;
+    if (it + 1 < ntiles) {
+      nxt.step(P, 0);
+      fetch(nxt, pre);
+    }
   }
   // The copies of the last tiles land before the CTA may exit (each barrier
   // below was last armed by the tile waited for, so no wait is ambiguous).
@@ -369,14 +367,74 @@ __device__ void producer_role(const Params& P, const CUtensorMap* tq, const CUte
   }
 }
 
+// Maskers (warps 5-6): per tile, once its sigma is in the ring, the mask
+// words, one per (token, 32-key chunk): bit e set iff key column ch*32 + e
+// lies in the token's window (truncated at the sequence ends) and, when
+// causal, sigma[q] <= sigma[p]; then hand the tile to its softmax warpgroup.
+// Four word buffers, so that a warpgroup still reading the words of tile
+// it - 2 is never overwritten.
+template <int NCH>
+__device__ void mask_role(const Params& P, uint8_t* smem, uint32_t bars, volatile int* abort_flag,
+                          volatile int* votes) {
+  const int mt = threadIdx.x - kCopiers;  // 0 .. kMaskers - 1
+  const int lane = mt & 31, mw = mt >> 5;
+  const int32_t* sig2 = reinterpret_cast<const int32_t*>(smem + P.off_sig);
+  auto wait = [&](uint32_t bar, uint32_t par) {
+    return bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
+  };
+  int begin, end;
+  cta_range(P, begin, end);
+  const int ntiles = end - begin;
+  TileWalk w;
+  for (int it = 0; it < ntiles; ++it) {
+    w.step(P, begin + it);
+    bool ok = true;
+    if (mt == 0) ok = wait(bars + 8 * (kSigW + (it & 3)), (it >> 2) & 1);
+    if (mt == 0) votes[2] = ok ? 1 : 0;
+    asm volatile("bar.sync 2, %0;" ::"n"(kMaskers) : "memory");
+    if (!votes[2]) break;
+    const int32_t* sig = sig2 + w.slot_a;
+    uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem + P.off_bits) +
+                     ((it & 1) * 2 + ((it >> 1) & 1)) * (P.Bt * NCH);
+    const int nblk = (P.Bt + 31) >> 5;
+    for (int item = mw; item < nblk * NCH; item += kMaskers / 32) {
+      const int tb = item / NCH, ch = item - tb * NCH;
+      const int tt = tb * 32 + lane;
+      const int lo = max(tt, P.left - w.p0);
+      const int hi = w.p0 + tt < P.n ? min(tt + P.left + P.right, P.n - 1 - w.p0 + P.left) : -1;
+      uint32_t word = band_bits(lo, hi, ch * 32);
+      if (P.causal) {
+        const int ks = sig[ch * 32 + lane];
+        const int st = sig[P.left + min(tt, P.Bt - 1)];
+        uint32_t cw = 0u;
+#pragma unroll 8
+        for (int u = 0; u < 32; ++u) {
+          const uint32_t bb = __ballot_sync(0xffffffffu, ks <= __shfl_sync(0xffffffffu, st, u));
+          cw = u == lane ? bb : cw;
+        }
+        word &= cw;
+      }
+      if (tt < P.Bt) wbuf[tt * NCH + ch] = word;
+    }
+    asm volatile("bar.sync 2, %0;" ::"n"(kMaskers) : "memory");
+    if (mt == 0) {
+      // Hand the tile to its softmax warpgroup once the warpgroup has read
+      // what it needed from its previous tile (so this barrier is never two
+      // phases ahead of its waiter).
+      // A wait that gives up sets the abort flag, which ends every role's
+      // next wait (the maskers leave at the top of their next tile together).
+      const int wg = it & 1;
+      if (wait(bars + 8 * (kSfree + wg), ((it >> 1) & 1) ^ 1)) mbar_arrive(bars + 8 * (kSready + wg));
+    }
+  }
+}
+
 template <int D>
 __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, uint32_t bars,
                          volatile int* abort_flag) {
   int begin, end;
   cta_range(P, begin, end);
-  const uint32_t ka = sbase + P.off_k, va = sbase + P.off_v;
-  const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
-  const uint32_t p_col = 0, o_col = uint32_t(P.span_pad / 2);
+  const uint32_t ka = sbase + P.off_k;
   auto qk = [&](int it, int slot_a) {
     const int s = it % kQStages, ts = it & 1;
     tc_fence_after();
@@ -402,64 +460,20 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
     umma_commit(bars + 8 * (kSfull + ts));
     umma_commit(bars + 8 * (kQKdone + s));
   };
-  auto pv = [&](int it, int slot_a) {
-    const int s = it % kVDepth, ts = it & 1;
-    tc_fence_after();
-    const uint32_t stage = tmem_base + uint32_t(ts * P.cols_stage);
-    const int ksteps = P.span_pad / 16;
-    int vs = slot_a;
-    uint64_t bd = sdesc_sw128(va + vs * 128, P.R * 128, 1024);
-    const uint64_t wrap = uint64_t(P.R) * 8;  // R rows of 128 B, in 16-byte units
-    for (int kk = 0; kk < ksteps; ++kk) {
-      umma_bf16_ts(stage + o_col, stage + p_col + 8 * kk, bd, idesc_pv, kk > 0 ? 1u : 0u);
-      vs += 16;
-      bd += 128;  // 16 rows of 128 B
-      if (vs >= P.R) {
-        vs -= P.R;
-        bd -= wrap;
-      }
-    }
-    umma_commit(bars + 8 * (kOfull + ts));
-    umma_commit(bars + 8 * (kPVdone + s));
-  };
-  // Issue QK(qk_it) and PV(pv_it) in whichever order their operands become
-  // ready (pv_it <= qk_it), PV first when both are: the softmax warpgroup
-  // waits on its O, and a PV whose P is written never waits behind the next
-  // tile's loads.
+  // S = Q K^T of every tile in order, each once its Q and K rows have landed
+  // and its TMEM stage has been read out by the epilogue of the tile two
+  // back.  (The O MMAs are issued by the softmax warpgroups themselves.)
   const int ntiles = end - begin;
-  TileWalk tq, tp;
-  int qk_it = 0, pv_it = 0;
-  long long last = clock64();
-  while (pv_it < ntiles) {
-    bool progress = false;
-    if (pv_it < qk_it &&
-        mbar_test_wait(bars + 8 * (kPfull + (pv_it & 1)), (pv_it >> 1) & 1) &&
-        mbar_test_wait(bars + 8 * (kFullV + pv_it % kVDepth), (pv_it / kVDepth) & 1)) {
-      tp.step(P, begin + pv_it);
-      pv(pv_it, tp.slot_a);
-      ++pv_it;
-      progress = true;
-    }
-    if (qk_it < ntiles && qk_it < pv_it + 2) {
-      if (mbar_test_wait(bars + 8 * (kFullQK + qk_it % kQStages), (qk_it / kQStages) & 1) &&
-          mbar_test_wait(bars + 8 * (kTempty + (qk_it & 1)), ((qk_it >> 1) & 1) ^ 1)) {
-        tq.step(P, begin + qk_it);
-        qk(qk_it, tq.slot_a);
-        ++qk_it;
-        progress = true;
-      }
-    }
-    if (progress) {
-      last = clock64();
-    } else {
-      if (*abort_flag) break;
-      if (clock64() - last > P.timeout_cycles) {
-        *abort_flag = 1;
-        atomicOr(P.err, SA_ERRBIT_TIMEOUT);
-        break;
-      }
-      __nanosleep(20);
-    }
+  TileWalk tq;
+  for (int it = 0; it < ntiles; ++it) {
+    if (!bounded_wait(bars + 8 * (kFullQK + it % kQStages), (it / kQStages) & 1, P.timeout_cycles,
+                      P.err, abort_flag))
+      break;
+    if (!bounded_wait(bars + 8 * (kTempty + (it & 1)), ((it >> 1) & 1) ^ 1, P.timeout_cycles, P.err,
+                      abort_flag))
+      break;
+    tq.step(P, begin + it);
+    qk(it, tq.slot_a);
   }
   umma_commit(bars + 8 * kDrain);
   const long long t0 = clock64();
@@ -467,9 +481,19 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   }
 }
 
+// The row's mask word of 32-column chunk ch (the words are in registers; a
+// select chain, not a local-memory index).
+template <int NCH>
+__device__ __forceinline__ uint32_t word_of(const uint32_t (&wd)[NCH], int ch) {
+  uint32_t b = wd[0];
+#pragma unroll
+  for (int k = 1; k < NCH; ++k) b = ch == k ? wd[k] : b;
+  return b;
+}
+
 template <int D, int NCH, bool kCausal>
-__device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base, uint32_t bars,
-                             volatile int* abort_flag) {
+__device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
+                             uint32_t bars, volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int wg = (warp - kFirstSoftmaxWarp) >> 2;  // also this warpgroup's TMEM stage
@@ -480,6 +504,8 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
   const int32_t* sig2 = reinterpret_cast<const int32_t*>(smem + P.off_sig);
   const uint32_t trow = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(wg * P.cols_stage);
   const uint32_t o_col = uint32_t(P.span_pad / 2);
+  const bool issuer = quad == 0 && lane == 0;  // issues this warpgroup's O MMAs
+  bool issued = false;
   auto wwait = [&](uint32_t bar, uint32_t par) {
     const bool ok = bounded_wait(bar, par, P.timeout_cycles, P.err, abort_flag);
     return __all_sync(0xffffffffu, ok);
@@ -495,54 +521,24 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     if (!wwait(bars + 8 * (kSready + wg), ph)) break;  // sigma of the tile is visible
     const int32_t* sig = sig2 + tw.slot_a;            // sigma of span column c is sig[c]
     bool row_valid = tw.p0 + t < P.n;
-    int sig_p = sig[P.left + t];
+    const int sig_p = sig[P.left + t];
+    // the row's mask words (written by the maskers)
+    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(smem + P.off_bits) +
+                           (wg * 2 + ((it >> 1) & 1)) * (P.Bt * NCH) + t * NCH;
+    uint32_t wd[NCH];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) wd[ch] = wrow[ch];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kSfree + wg));  // sigma and words no longer read
     if (row_valid && unsigned(sig_p) >= unsigned(P.n)) {  // never expected: record, skip
       atomicOr(P.err, SA_ERRBIT_INTERNAL);
       row_valid = false;
     }
 
-    // Each warp first builds one 32-bit word per (token of its rows,
-    // 32-key chunk): bit e set iff key column ch*32 + e is attended, i.e. it
-    // lies in the token's window (truncated at the sequence ends) and, when
-    // causal, sigma[q] <= sigma[p]; each thread reads its chunk's sigma in one
-    // burst.  The passes below then need only the row's own words.
-    uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem + P.off_bits) +
-                     (wg * 2 + ((it >> 1) & 1)) * (P.Bt * NCH);
-    {
-      // each warp builds the words of its own tokens (rows quad*32 .. +31)
-      const int tpw = 32 >> P.log2g;
-      for (int w = lane; w < tpw * NCH; w += 32) {
-        const int tt = quad * tpw + w / NCH, ch = w % NCH;
-        const int lo = max(tt, P.left - tw.p0);
-        const int hi = tw.p0 + tt < P.n ? min(tt + P.left + P.right, P.n - 1 - tw.p0 + P.left) : -1;
-        uint32_t word = band_bits(lo, hi, ch * 32);
-        if (kCausal && word != 0u) {
-          const int sp = sig[P.left + tt];
-          const int4* s4p = reinterpret_cast<const int4*>(sig + ch * 32);
-          int4 s4[8];
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) s4[e4] = s4p[e4];
-          uint32_t cw = 0;
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            cw |= (s4[e4].x <= sp ? 1u : 0u) << (4 * e4);
-            cw |= (s4[e4].y <= sp ? 1u : 0u) << (4 * e4 + 1);
-            cw |= (s4[e4].z <= sp ? 1u : 0u) << (4 * e4 + 2);
-            cw |= (s4[e4].w <= sp ? 1u : 0u) << (4 * e4 + 3);
-          }
-          word &= cw;
-        }
-        wbuf[tt * NCH + ch] = word;
-      }
-    }
-    __syncwarp();
-    const uint32_t* wrow = wbuf + t * NCH;
-    if (lane == 0) mbar_arrive(bars + 8 * (kSfree + wg));  // sigma no longer read
-
     if (!wwait(bars + 8 * (kSfull + wg), ph)) break;
     tc_fence_after();
     // Two passes over the row's 32-column chunks, loops kept rolled so the
-    // code stays small (three roles share each SM's instruction cache):
+    // code stays small (the roles share each SM's instruction cache):
     // the attended maximum, then p = 2^(s*scale*log2e - max) for attended
     // columns (0 elsewhere) written back to TMEM as bf16 over the row's own S
     // columns (P column pair c/2 holds keys c and c+1; chunk ch's P lands on
@@ -552,7 +548,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     for (int ch = 0; ch < NCH; ++ch) {
       uint32_t v[32];
       tmem_ld32(trow + ch * 32, v);
-      const uint32_t bits = wrow[ch];
+      const uint32_t bits = word_of(wd, ch);
       float m0 = mx, m1 = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
@@ -573,7 +569,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     for (int ch = 0; ch < NCH; ++ch) {
       uint32_t v[32];
       tmem_ld32(trow + ch * 32, v);
-      const uint32_t bits = wrow[ch];
+      const uint32_t bits = word_of(wd, ch);
       uint32_t pk[16];
 #pragma unroll
       for (int e2 = 0; e2 < 16; ++e2) {
@@ -593,6 +589,34 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kPfull + wg));
+    // Once P of all 128 rows is in TMEM and the tile's V rows have landed,
+    // one thread of the warpgroup issues O = P V (A = P from this stage, B =
+    // V straight from the ring, MN-major).  Its waits are bounded like every
+    // other wait.
+    if (issuer &&
+        bounded_wait(bars + 8 * (kPfull + wg), ph, P.timeout_cycles, P.err, abort_flag) &&
+        bounded_wait(bars + 8 * (kFullV + it % kVDepth), (it / kVDepth) & 1, P.timeout_cycles,
+                     P.err, abort_flag)) {
+      tc_fence_after();
+      const uint32_t stage = tmem_base + uint32_t(wg * P.cols_stage);
+      const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
+      const int ksteps = P.span_pad / 16;
+      int vs = tw.slot_a;
+      uint64_t bd = sdesc_sw128(sbase + P.off_v + vs * 128, P.R * 128, 1024);
+      const uint64_t wrap = uint64_t(P.R) * 8;  // R rows of 128 B, in 16-byte units
+      for (int kk = 0; kk < ksteps; ++kk) {
+        umma_bf16_ts(stage + o_col, stage + 8 * kk, bd, idesc_pv, kk > 0 ? 1u : 0u);
+        vs += 16;
+        bd += 128;  // 16 rows of 128 B
+        if (vs >= P.R) {
+          vs -= P.R;
+          bd -= wrap;
+        }
+      }
+      umma_commit(bars + 8 * (kOfull + wg));
+      umma_commit(bars + 8 * (kPVdone + it % kVDepth));
+      issued = true;
+    }
 
     // epilogue
     if (!wwait(bars + 8 * (kOfull + wg), ph)) break;
@@ -668,6 +692,12 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
       }
     }
   }
+  if (issued) {  // an abort can leave this thread's last O MMA in flight
+    umma_commit(bars + 8 * (kDrainWg + wg));
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bars + 8 * (kDrainWg + wg), 0) && clock64() - t0 < kDrainCycles) {
+    }
+  }
 }
 
 template <int D, int NCH>
@@ -682,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = sbase + P.off_bar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.off_bar + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 4);
-  volatile int* votes = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 8);
+  volatile int* votes = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kNumBars + 8);  // [3]
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
@@ -698,13 +728,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars + 8 * (kSfree + w), 4);
       mbar_init(bars + 8 * (kSfull + w), 1);
       mbar_init(bars + 8 * (kPfull + w), 4);
+      mbar_init(bars + 8 * (kDrainWg + w), 1);
       mbar_init(bars + 8 * (kOfull + w), 1);
       mbar_init(bars + 8 * (kTempty + w), 4);
     }
     mbar_init(bars + 8 * kDrain, 1);
+    for (int x = 0; x < 4; ++x) mbar_init(bars + 8 * (kSigW + x), 1);
     *abort_flag = 0;
     votes[0] = 1;
     votes[1] = 1;
+    votes[2] = 1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -724,15 +757,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kFirstSoftmaxWarp) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     if (P.causal)
-      softmax_role<D, NCH, true>(P, smem, tmem_base, bars, abort_flag);
+      softmax_role<D, NCH, true>(P, smem, sbase, tmem_base, bars, abort_flag);
     else
-      softmax_role<D, NCH, false>(P, smem, tmem_base, bars, abort_flag);
+      softmax_role<D, NCH, false>(P, smem, sbase, tmem_base, bars, abort_flag);
     tc_fence_before();
     __syncthreads();
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
-    if (warp < kMmaWarp) {
-      producer_role<D>(P, &tm_q, &tm_k, &tm_v, smem, sbase, bars, abort_flag, votes);
+    if (warp < kCopiers / 32) {
+      copy_role<D>(P, &tm_q, &tm_k, &tm_v, smem, sbase, bars, abort_flag, votes);
+    } else if (warp < kMmaWarp) {
+      mask_role<NCH>(P, smem, bars, abort_flag, votes);
     } else {
       if ((threadIdx.x & 31) == 0) mma_role<D>(P, sbase, tmem_base, bars, abort_flag);
       __syncwarp();
@@ -789,7 +824,7 @@ static bool make_config(const Problem& pb, Path path, Config& c) {
   c.off_vtok = round_up(c.off_sig + 2u * c.R * 4, 16);
   c.off_bits = round_up(c.off_vtok + 2u * c.span_pad * 4, 16);
   c.off_bar = round_up(c.off_bits + 4u * c.Bt * (c.span_pad / 32) * 4, 64);
-  c.smem_bytes = c.off_bar + 8 * kNumBars + 16 + 1024;  // + slot, flags, alignment slack
+  c.smem_bytes = c.off_bar + 8 * kNumBars + 32 + 1024;  // + slot, flags, alignment slack
   return c.smem_bytes <= kMaxSmem;
 }
 
@@ -914,7 +949,7 @@ sa_status_t launch_ring(const Problem& pb, Path path, const float* gate, int acc
   P.off_bits = c.off_bits;
   P.off_bar = c.off_bar;
   P.timeout_cycles = wait_limit_cycles();
-  // Row maps of Q [B*n*Hq, d] and K, V [B*n*Hkv, d]: the producers gather
+  // Row maps of Q [B*n*Hq, d] and K, V [B*n*Hkv, d]: the copiers gather
   // four arbitrary rows per copy.
   Maps m;
   const uint64_t qrows = uint64_t(pb.B) * pb.n * pb.Hq, kvrows = uint64_t(pb.B) * pb.n * pb.Hkv;
