@@ -14,7 +14,7 @@
 // (plus its 128 Q rows); the first tile of a run fetches the whole span.
 // Copier warps fetch rows with TMA four-row gathers (tile::gather4: one
 // 128-byte column block of four arbitrary rows per copy, swizzled by the
-// copy engine), spread over the lanes of five warps: the copy engine's
+// copy engine), spread over the lanes of five or six warps: the copy engine's
 // intake grows with the number of warps issuing, and the copies take no
 // load/store-unit slots from the softmax warps.  Q and K of a tile are
 // needed only by S = Q K^T, V only by O = P V, so they land on separate
@@ -26,8 +26,10 @@
 // and s + R) so that a tile's span is always a plain contiguous array.
 //
 // Roles (four warpgroups, 512 threads):
-//   warps 0-4   copiers: sigma of new positions, TMA gathers of Q / K / V rows
-//   warps 5-6   maskers: the tile's mask words (one 32-bit word per token and
+//   warps 0-4   copiers (0-5 for spans of up to 64 keys): sigma of new
+//               positions, TMA gathers of Q / K / V rows
+//   warps 5-6   maskers (warp 6 alone for spans of up to 64 keys): the
+//               tile's mask words (one 32-bit word per token and
 //               32-key chunk, from sigma), then the hand-over to the tile's
 //               softmax warpgroup
 //   warp 7      lane 0 issues S = Q K^T of every tile in order; the warp
@@ -56,8 +58,15 @@ namespace ring {
 using namespace tcc;
 
 constexpr int kThreads = 512;
-constexpr int kCopiers = 160;   // warps 0-4: sigma of new positions, TMA copies
-constexpr int kMaskers = 64;    // warps 5-6: mask words, sigma hand-off
+// Warps 0-6 split into copiers (sigma of new positions, TMA copies) and
+// maskers (mask words, the hand-over to the softmax warpgroup).  The copies
+// per tile do not depend on the span, the mask words grow with it: spans of
+// up to two 32-key chunks leave one masker warp enough, wider ones take two.
+template <int NCH>
+struct Split {
+  static constexpr int kCopiers = NCH <= 2 ? 192 : 160;
+  static constexpr int kMaskers = 224 - kCopiers;
+};
 constexpr int kMmaWarp = 7;
 constexpr int kFirstSoftmaxWarp = 8;
 constexpr int kLaunchRegs = 128;
@@ -107,7 +116,8 @@ enum : uint32_t {
   kNumBars = 31,
 };
 static_assert(kFullQK + kQStages <= kQKdone && kQKdone + kQStages <= kFullV, "barrier slots");
-static_assert(32 * kMaxChunks <= 2 * kCopiers, "a tile's new positions: two per copier thread");
+static_assert(32 * kMaxChunks <= 2 * Split<kMaxChunks>::kCopiers,
+              "a tile's new positions: two per copier thread");
 
 // Tiles of this CTA: a contiguous range, split evenly over the grid.
 __device__ __forceinline__ void cta_range(const Params& P, int& begin, int& end) {
@@ -211,11 +221,12 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 
 // Copiers (warps 0-4): per tile, wait for the slots it reuses to retire,
 // write sigma of its new positions to the ring, then issue its TMA copies.
-template <int D>
+template <int D, int NCH>
 __device__ void copy_role(const Params& P, const CUtensorMap* tq, const CUtensorMap* tk,
                           const CUtensorMap* tv, uint8_t* smem, uint32_t sbase, uint32_t bars,
                           volatile int* abort_flag, volatile int* votes) {
   constexpr int KB = D / 64;  // 128-byte column blocks per row
+  constexpr int kCopiers = Split<NCH>::kCopiers;
   const int tid = threadIdx.x;
   // This thread's place in a tile's TMA issue order: consecutive copies go to
   // different warps (a warp issues its lanes' copies one after another).
@@ -376,7 +387,8 @@ __device__ void copy_role(const Params& P, const CUtensorMap* tq, const CUtensor
 template <int NCH>
 __device__ void mask_role(const Params& P, uint8_t* smem, uint32_t bars, volatile int* abort_flag,
                           volatile int* votes) {
-  const int mt = threadIdx.x - kCopiers;  // 0 .. kMaskers - 1
+  constexpr int kMaskers = Split<NCH>::kMaskers;
+  const int mt = threadIdx.x - Split<NCH>::kCopiers;  // 0 .. kMaskers - 1
   const int lane = mt & 31, mw = mt >> 5;
   const int32_t* sig2 = reinterpret_cast<const int32_t*>(smem + P.off_sig);
   auto wait = [&](uint32_t bar, uint32_t par) {
@@ -764,8 +776,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
-    if (warp < kCopiers / 32) {
-      copy_role<D>(P, &tm_q, &tm_k, &tm_v, smem, sbase, bars, abort_flag, votes);
+    if (warp < Split<NCH>::kCopiers / 32) {
+      copy_role<D, NCH>(P, &tm_q, &tm_k, &tm_v, smem, sbase, bars, abort_flag, votes);
     } else if (warp < kMmaWarp) {
       mask_role<NCH>(P, smem, bars, abort_flag, votes);
     } else {
