@@ -18,11 +18,13 @@
 // not grow with the window: any window fits.
 //
 // Roles (four warpgroups, 512 threads):
-//   warps 0-6   producers: cp.async of the 256 Q rows of a tile and of the 128
+//   warps 0-6  producers: cp.async of the 256 Q rows of a tile and of the 128
 //               K and V rows of each chunk (with the chunk's key tokens)
-//   warp 7      lane 0 issues the MMAs in whichever order their operands
-//               become ready; the warp owns TMEM
-//   warps 8-11  softmax, O correction and epilogue of rows 0-127
+//   warp 7      lane 0 issues S = Q K^T of each half and chunk as soon as its
+//               operands are ready; the warp owns TMEM
+//   warps 8-11  softmax, O correction, O += P V issue and epilogue of rows
+//               0-127 (one thread of the warpgroup issues the O MMAs, so no
+//               other warp has to notice that P is ready)
 //   warps 12-15 the same for rows 128-255
 // Every wait is bounded (SA_ERRBIT_TIMEOUT); producer copies are drained
 // before exit.
@@ -87,7 +89,8 @@ enum : uint32_t {
   kOfull = 14,   // [h] the half's last O MMA of tile x done
   kOfree = 16,   // [h] the half's epilogue has read O of tile x (4 warps)
   kDrain = 18,
-  kNumBars = 19,
+  kDrainH = 19,  // [h] final completion of the half's O MMAs
+  kNumBars = 21,
 };
 
 struct Tile {
@@ -273,7 +276,6 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   const int nch = P.nchunks;
   const int total = (end - begin) * nch;
   const uint32_t idesc_qk = idesc_bf16(kBM, kKC, 0);
-  const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
   // S of half h in TMEM columns [h*128, h*128 + 128); O of half h at 256 + h*D.
   // Shared-memory descriptors of every stage, built once (kept in registers:
   // chosen by selects, not indexed).
@@ -283,8 +285,6 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
   const uint64_t q11 = sdesc_sw128(sbase + 3 * P.q_bytes, 16, 1024);
   const uint64_t k0 = sdesc_sw128(sbase + P.off_k, 16, 1024);
   const uint64_t k1 = sdesc_sw128(sbase + P.off_k + P.kv_bytes, 16, 1024);
-  const uint64_t v0 = sdesc_sw128(sbase + P.off_v, kKC * 128, 1024);
-  const uint64_t v1 = sdesc_sw128(sbase + P.off_v + P.kv_bytes, kKC * 128, 1024);
   // c: the chunk within its tile; qs: the tile's Q stage.
   auto qk = [&](int h, int call, int c, int qs) {
     fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core reads
@@ -301,54 +301,20 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
     umma_commit(bars + 8 * (kSfull + h));
     if (c == nch - 1) umma_commit(bars + 8 * (kQfree + qs));
   };
-  auto pv = [&](int h, int call, int c) {
-    tc_fence_after();
-    const uint32_t sbuf = tmem_base + uint32_t(h * kKC);
-    const uint32_t o = tmem_base + uint32_t(2 * kKC + h * D);
-    uint64_t bd = (call & 1) ? v1 : v0;
-#pragma unroll
-    for (int kk = 0; kk < kKC / 16; ++kk) {
-      umma_bf16_ts(o, sbuf + 8 * kk, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
-      bd += 128;  // 16 keys of 128 B
-    }
-    umma_commit(bars + 8 * (kPVdone + h));
-    umma_commit(bars + 8 * (kCfree + (call & 1)));
-    if (c == nch - 1) umma_commit(bars + 8 * (kOfull + h));
-  };
-  // Per half: QK(qn) after the half's previous O MMA has read its P (one S
-  // buffer per half), PV(pn) once P is written; PV first when both are ready.
-  // Tile, chunk and Q stage of each half's next QK and PV are kept as
+  // Per half: QK of chunk call once its K rows have landed and the half's
+  // previous O MMA (issued by the half's softmax warpgroup) has read P out of
+  // the S buffer.  Chunk and Q stage of each half's next QK are kept as
   // counters: this single thread's loop stays free of divisions, which would
   // delay every reaction to a barrier.
-  int qn[2] = {0, 0}, pn[2] = {0, 0};
-  int pc[2] = {0, 0}, px[2] = {0, 0};                // PV: chunk, tile
-  int qc[2] = {0, 0};                                // QK: chunk
-  int qst[2] = {0, 0}, qph[2] = {0, 0};              // QK: Q stage and its parity
+  int qn[2] = {0, 0};
+  int qc[2] = {0, 0};                    // QK: chunk
+  int qst[2] = {0, 0}, qph[2] = {0, 0};  // QK: Q stage and its parity
   long long last = clock64();
-  while (pn[0] < total || pn[1] < total) {
+  while (qn[0] < total || qn[1] < total) {
     bool progress = false;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      if (pn[h] < qn[h]) {
-        const int call = pn[h];
-        bool ready = mbar_test_wait(bars + 8 * (kPfull + h), call & 1);
-        // a tile's first O MMA overwrites O: the half's epilogue of the
-        // previous tile must have read it
-        if (ready && pc[h] == 0) ready = mbar_test_wait(bars + 8 * (kOfree + h), (px[h] & 1) ^ 1);
-        if (ready) {
-          pv(h, call, pc[h]);
-          ++pn[h];
-          if (++pc[h] == nch) {
-            pc[h] = 0;
-            ++px[h];
-          }
-          progress = true;
-        }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (qn[h] < total && qn[h] == pn[h]) {
+      if (qn[h] < total) {
         const int call = qn[h];
         bool ready = mbar_test_wait(bars + 8 * (kCfull + (call & 1)), (call >> 1) & 1) &&
                      mbar_test_wait(bars + 8 * (kPVdone + h), (call & 1) ^ 1);
@@ -387,8 +353,8 @@ __device__ void mma_role(const Params& P, uint32_t sbase, uint32_t tmem_base, ui
 
 // ------------------------------------------------------------------ softmax
 template <int D, bool kCausal>
-__device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base, uint32_t bars,
-                             volatile int* abort_flag) {
+__device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uint32_t tmem_base,
+                             uint32_t bars, volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h = (warp - kFirstSoftmaxWarp) >> 2;  // the half of the tile (rows h*128 ..)
@@ -415,6 +381,9 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
   const int ntiles = end - begin;
   const int nch = P.nchunks;
   const uint64_t sl2 = f2_pack(P.scale_log2, P.scale_log2);
+  const bool issuer = quad == 0 && lane == 0;  // issues this half's O MMAs
+  const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
+  bool issued = false;
   bool alive = true;
   for (int x = 0; x < ntiles && alive; ++x) {
     const Tile tl = tile_of(P, begin + x);
@@ -563,6 +532,27 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8 * (kPfull + h));
+      // Once all four warps have written P, one thread issues O += P V (A = P
+      // from the half's S buffer, B = V of the chunk's stage).  The chunk's V
+      // rows landed with its keys (kCfull, waited above).  The tile's first O
+      // MMA overwrites O: every warp of the half read O of the previous tile
+      // before it wrote this P, which the P barrier orders.
+      if (issuer && bounded_wait(bars + 8 * (kPfull + h), uint32_t(call) & 1u, P.timeout_cycles,
+                                 P.err, abort_flag)) {
+        tc_fence_after();
+        const uint32_t sbuf = tmem_base + uint32_t(h * kKC);
+        const uint32_t o = tmem_base + uint32_t(2 * kKC + h * D);
+        uint64_t bd = sdesc_sw128(sbase + P.off_v + uint32_t(b) * P.kv_bytes, kKC * 128, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kKC / 16; ++kk) {
+          umma_bf16_ts(o, sbuf + 8 * kk, bd, idesc_pv, (c > 0 || kk > 0) ? 1u : 0u);
+          bd += 128;  // 16 keys of 128 B
+        }
+        umma_commit(bars + 8 * (kPVdone + h));
+        umma_commit(bars + 8 * (kCfree + b));
+        if (c == nch - 1) umma_commit(bars + 8 * (kOfull + h));
+        issued = true;
+      }
     }
     if (!alive) break;
 
@@ -621,6 +611,12 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t tmem_base,
       }
     }
   }
+  if (issued) {  // an abort can leave this thread's last O MMA in flight
+    umma_commit(bars + 8 * (kDrainH + h));
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bars + 8 * (kDrainH + h), 0) && clock64() - t0 < kDrainCycles) {
+    }
+  }
 }
 
 template <int D>
@@ -648,6 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1) sa_chunk_kernel(const __grid_cons
       mbar_init(bars + 8 * (kOfree + s), 4);
     }
     mbar_init(bars + 8 * kDrain, 1);
+    mbar_init(bars + 8 * (kDrainH + 0), 1);
+    mbar_init(bars + 8 * (kDrainH + 1), 1);
     *abort_flag = 0;
     *vote = 1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -669,9 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1) sa_chunk_kernel(const __grid_cons
   if (warp >= kFirstSoftmaxWarp) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     if (P.causal)
-      softmax_role<D, true>(P, smem, tmem_base, bars, abort_flag);
+      softmax_role<D, true>(P, smem, sbase, tmem_base, bars, abort_flag);
     else
-      softmax_role<D, false>(P, smem, tmem_base, bars, abort_flag);
+      softmax_role<D, false>(P, smem, sbase, tmem_base, bars, abort_flag);
     tc_fence_before();
     __syncthreads();
   } else {
