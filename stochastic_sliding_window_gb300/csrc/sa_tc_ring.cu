@@ -74,7 +74,9 @@ constexpr int kCtrlRegs = 96;
 constexpr int kSoftmaxRegs = 160;
 static_assert(256 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
-constexpr int kMaxChunks = 5;  // spans up to 160 columns (whole row in registers)
+// Spans up to 256 keys: two TMEM stages of S (P over S) and O fit in 512
+// columns for d <= 128; shared memory decides the rest.
+constexpr int kMaxChunks = 8;
 constexpr int kQStages = 2;  // Q buffers; a stage is free once its S MMA is done
 constexpr int kVDepth = 3;   // V (and K) rows of tile x overwrite those of tile x - 3
 constexpr uint32_t kMaxSmem = 232448;
@@ -880,7 +882,10 @@ static cudaError_t launch_variant(int nch, int grid, uint32_t smem, cudaStream_t
     case 2: return launch_one<D, 2>(grid, smem, stream, m, P);
     case 3: return launch_one<D, 3>(grid, smem, stream, m, P);
     case 4: return launch_one<D, 4>(grid, smem, stream, m, P);
-    default: return launch_one<D, 5>(grid, smem, stream, m, P);
+    case 5: return launch_one<D, 5>(grid, smem, stream, m, P);
+    case 6: return launch_one<D, 6>(grid, smem, stream, m, P);
+    case 7: return launch_one<D, 7>(grid, smem, stream, m, P);
+    default: return launch_one<D, 8>(grid, smem, stream, m, P);
   }
 }
 
@@ -888,10 +893,11 @@ static cudaError_t launch_variant(int nch, int grid, uint32_t smem, cudaStream_t
 // register count its setmaxnreg split assumes (checked once per variant), so
 // that the automatic kernel choice never picks a kernel that would refuse to
 // launch.
+static_assert(kMaxChunks == 8, "the variant switches list NCH = 1..8");
 template <int D>
 static bool regs_ok(int nch) {
-  static int cache[6] = {-1, -1, -1, -1, -1, -1};
-  const int i = nch < 1 ? 1 : (nch > 5 ? 5 : nch);
+  static int cache[kMaxChunks + 1] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  const int i = nch < 1 ? 1 : (nch > kMaxChunks ? kMaxChunks : nch);
   if (cache[i] < 0) {
     cudaFuncAttributes fa;
     cudaError_t ce;
@@ -900,7 +906,10 @@ static bool regs_ok(int nch) {
       case 2: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 2>); break;
       case 3: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 3>); break;
       case 4: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 4>); break;
-      default: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 5>); break;
+      case 5: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 5>); break;
+      case 6: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 6>); break;
+      case 7: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 7>); break;
+      default: ce = cudaFuncGetAttributes(&fa, sa_ring_kernel<D, 8>); break;
     }
     cache[i] = (ce == cudaSuccess && fa.numRegs == kLaunchRegs) ? 1 : 0;
   }

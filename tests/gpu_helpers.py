@@ -26,8 +26,9 @@ def span(path: str, g: int, w: int) -> int:
 
 def _ring_fits(sp: int, g: int, d: int) -> bool:
     """The ring kernel's resources: 2 Q stages, K and V rings of span + 2 Bt
-    rows, the doubled sigma ring, two new-token lists, the mask words and 25
-    barriers in 227 KB of shared memory; two TMEM stages in 512 columns."""
+    rows, the doubled sigma ring, two new-token lists, four buffers of mask
+    words and 31 barriers in 227 KB of shared memory; spans of at most 256
+    keys; two TMEM stages in 512 columns."""
     rnd = lambda x, m: -(-x // m) * m
     pad = rnd(sp, 32)
     bt = 128 // g
@@ -36,9 +37,9 @@ def _ring_fits(sp: int, g: int, d: int) -> bool:
     off_vtok = rnd(off_sig + 2 * r * 4, 16)
     off_bits = rnd(off_vtok + 2 * pad * 4, 16)
     off_bar = rnd(off_bits + 4 * bt * (pad // 32) * 4, 64)
-    smem = off_bar + 8 * 25 + 16 + 1024
+    smem = off_bar + 8 * 31 + 32 + 1024
     cols = rnd(max(pad, pad // 2 + d), 32)
-    return pad <= 160 and smem <= 232448 and 2 * cols <= 512
+    return pad <= 256 and smem <= 232448 and 2 * cols <= 512
 
 
 def must_support(kernel: int, path: str, g: int, w: int, w_swa: int = 0, d: int = 128) -> bool:
