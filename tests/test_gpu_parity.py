@@ -84,6 +84,8 @@ EDGE = [
     (200, 8, 1, 128, 16),
     (129, 2, 2, 64, 256),
     (300, 8, 8, 128, 600),   # window wider than the sequence
+    (700, 32, 8, 128, 192),  # ring spans of seven 32-key chunks
+    (400, 32, 4, 128, 224),  # ring spans of eight 32-key chunks (Bt = 16)
 ]
 
 
@@ -101,6 +103,27 @@ def test_gated_separate_swa_window():
     perm, perm_d = perms(3, 0, 1, 700)
     for kernel in KERNELS:
         _check_full("gated", inp, perm, perm_d, 64, True, kernel, window_swa=24)
+
+
+def test_gated_rounding_margin_per_kernel():
+    """The tensor-core kernels' gated merge rounds twice (the SWA term is
+    stored in bf16 and the SA pass adds to it); the CUDA-core kernel rounds
+    once.  Every kernel stays inside the bar, and the second rounding adds at
+    most about one bf16 rounding of the output (2^-8 relative) over the
+    single-rounding kernel.  Run with -s to see the margins."""
+    inp = Inputs(2, 1024, 8, 8, 64, seed=21, std=1.0 / 8.0)
+    perm, perm_d = perms(21, 0, 2, 1024)
+    errs = {}
+    for kernel, name in zip(KERNELS, KERNEL_IDS):
+        errs[name] = _check_full("gated", inp, perm, perm_d, 128, True, kernel)
+    for name, e in errs.items():
+        if e is not None:
+            print(f"gated w=128 {name}: max_abs={e[0]:.3e} rel_l2={e[1]:.3e} "
+                  f"(bars {2e-2:.0e}, {5e-3:.0e})")
+    single = errs["simt"]
+    for name in ("ring", "chunk"):
+        if errs[name] is not None:
+            assert errs[name][1] <= single[1] + 2.0 ** -8, (name, errs[name], single)
 
 
 # ------------------------------------------------------------ pretraining-layer shape
