@@ -242,7 +242,8 @@ sa_status_t sa_gate_projection(const void* x, int32_t tokens, int32_t d_model,
  * k < head_dim/2 the pair (x_k, x_{k + head_dim/2}) of token i is rotated by
  * the angle i * base^(-2k/head_dim).  head_dim even and <= 128, base > 1.
  * Angles are reduced in fp64, rotations done in fp32, results rounded to
- * bf16.  Asynchronous on `stream`.
+ * bf16.  Any 2-byte-aligned x is accepted (16-byte aligned data takes the
+ * widest accesses).  Asynchronous on `stream`.
  */
 sa_status_t sa_rope(void* x, int32_t batch, int32_t seqlen, int32_t heads, int32_t head_dim,
                     double base, cudaStream_t stream);

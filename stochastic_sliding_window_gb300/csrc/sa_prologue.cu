@@ -186,27 +186,102 @@ __global__ void __launch_bounds__(kThreads, 2) sa_gate_proj_kernel(const __grid_
 
 struct RopeParams {
   __nv_bfloat16* x;  // [B, n, H, d], rotated in place
+  long long rows;    // B * n
   int n, H, d;
+  int vec;           // 16-byte accesses: x 16-byte aligned and d/2 a multiple of 8
+  int pairs;         // else 4-byte accesses: x 4-byte aligned and d/2 even (else 2-byte)
+  int tpb;           // tokens per block on the 16-byte path
   double theta[64];  // base^(-2k/d), k < d/2
 };
 
-__global__ void __launch_bounds__(kThreads) sa_rope_kernel(const __grid_constant__ RopeParams P) {
-  __shared__ float s_cos[64], s_sin[64];
-  const long long row = blockIdx.x;  // (b, i)
-  const int i = int(row % P.n);
-  const int half = P.d / 2;
-  if (threadIdx.x < half) {
-    const double a = double(i) * P.theta[threadIdx.x];
-    const double two_pi = 6.283185307179586476925286766559;
-    const float r = float(a - two_pi * rint(a / two_pi));  // in [-pi, pi]
-    float sn, cs;
-    sincosf(r, &sn, &cs);
-    s_cos[threadIdx.x] = cs;
-    s_sin[threadIdx.x] = sn;
+constexpr int kRopePre = 4;     // 16-byte items per thread loaded before the angles
+constexpr int kRopeAngles = 512;  // angle slots per block (tokens per block x d/2)
+
+// The angle i * theta_k of token i, reduced to [-pi, pi] in fp64, then its
+// cosine and sine in fp32.
+__device__ __forceinline__ void rope_angle(const RopeParams& P, long long row, int k, float& c,
+                                           float& s) {
+  const double a = double(row % P.n) * P.theta[k];
+  const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+  sincosf(float(a - two_pi * rint(a * inv_two_pi)), &s, &c);
+}
+
+// 8 rotated pairs: (lo_e, hi_e) -> (lo_e c - hi_e s, hi_e c + lo_e s).
+__device__ __forceinline__ void rope_rotate8(uint4& lo, uint4& hi, const float* cs, const float* sn) {
+  uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
+  uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    __nv_bfloat162 bl = *reinterpret_cast<__nv_bfloat162*>(&pl[e]);
+    __nv_bfloat162 bh = *reinterpret_cast<__nv_bfloat162*>(&ph[e]);
+    const float2 l = __bfloat1622float2(bl), h = __bfloat1622float2(bh);
+    const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
+    bl = __floats2bfloat162_rn(l.x * c0 - h.x * s0, l.y * c1 - h.y * s1);
+    bh = __floats2bfloat162_rn(h.x * c0 + l.x * s0, h.y * c1 + l.y * s1);
+    pl[e] = *reinterpret_cast<uint32_t*>(&bl);
+    ph[e] = *reinterpret_cast<uint32_t*>(&bh);
   }
+}
+
+__global__ void __launch_bounds__(kThreads) sa_rope_kernel(const __grid_constant__ RopeParams P) {
+  __shared__ float s_cos[kRopeAngles], s_sin[kRopeAngles];
+  const int half = P.d / 2;
+  if (P.vec) {
+    // tpb tokens per block; item = (token, head, 8 pairs).  The first items'
+    // rows are loaded before the angles are computed, so the loads overlap
+    // the fp64 angle reduction.
+    const int h8 = half / 8;
+    const int per_tok = P.H * h8;
+    const long long row0 = (long long)blockIdx.x * P.tpb;
+    const int ntok = int(min((long long)P.tpb, P.rows - row0));
+    const int items = ntok * per_tok;
+    uint4 vlo[kRopePre], vhi[kRopePre];
+#pragma unroll
+    for (int u = 0; u < kRopePre; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      if (idx < items) {
+        const int tk = idx / per_tok, rem = idx - tk * per_tok;
+        const int h = rem / h8, k = (rem - h * h8) * 8;
+        const __nv_bfloat16* px = P.x + (size_t(row0 + tk) * P.H + h) * P.d + k;
+        vlo[u] = *reinterpret_cast<const uint4*>(px);
+        vhi[u] = *reinterpret_cast<const uint4*>(px + half);
+      }
+    }
+    for (int a = threadIdx.x; a < ntok * half; a += kThreads) {
+      const int tk = a / half, k = a - tk * half;
+      rope_angle(P, row0 + tk, k, s_cos[a], s_sin[a]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kRopePre; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      if (idx < items) {
+        const int tk = idx / per_tok, rem = idx - tk * per_tok;
+        const int h = rem / h8, k = (rem - h * h8) * 8;
+        __nv_bfloat16* px = P.x + (size_t(row0 + tk) * P.H + h) * P.d + k;
+        rope_rotate8(vlo[u], vhi[u], s_cos + tk * half + k, s_sin + tk * half + k);
+        *reinterpret_cast<uint4*>(px) = vlo[u];
+        *reinterpret_cast<uint4*>(px + half) = vhi[u];
+      }
+    }
+    for (int idx = threadIdx.x + kRopePre * kThreads; idx < items; idx += kThreads) {
+      const int tk = idx / per_tok, rem = idx - tk * per_tok;
+      const int h = rem / h8, k = (rem - h * h8) * 8;
+      __nv_bfloat16* px = P.x + (size_t(row0 + tk) * P.H + h) * P.d + k;
+      uint4 lo = *reinterpret_cast<const uint4*>(px), hi = *reinterpret_cast<const uint4*>(px + half);
+      rope_rotate8(lo, hi, s_cos + tk * half + k, s_sin + tk * half + k);
+      *reinterpret_cast<uint4*>(px) = lo;
+      *reinterpret_cast<uint4*>(px + half) = hi;
+    }
+    return;
+  }
+  // one token per block, 4-byte or 2-byte accesses
+  const long long row = blockIdx.x;  // (b, i)
+  if (threadIdx.x < half) rope_angle(P, row, threadIdx.x, s_cos[threadIdx.x], s_sin[threadIdx.x]);
   __syncthreads();
   __nv_bfloat16* base = P.x + size_t(row) * P.H * P.d;
-  if ((half & 1) == 0) {  // two adjacent pairs per thread, bf16x2 accesses
+  if (P.pairs) {  // two adjacent pairs per thread, bf16x2 accesses
     const int h2 = half / 2;
     for (int idx = threadIdx.x; idx < P.H * h2; idx += blockDim.x) {
       const int h = idx / h2, k = 2 * (idx - (idx / h2) * h2);
@@ -283,11 +358,26 @@ sa_status_t launch_rope(void* x, int batch, int n, int heads, int head_dim, doub
   RopeParams P;
   std::memset(&P, 0, sizeof(P));
   P.x = static_cast<__nv_bfloat16*>(x);
+  P.rows = (long long)batch * n;
   P.n = n;
   P.H = heads;
   P.d = head_dim;
   for (int k = 0; k < head_dim / 2; ++k) P.theta[k] = std::pow(base, -2.0 * k / head_dim);
-  sa_rope_kernel<<<unsigned(size_t(batch) * n), kThreads, 0, stream>>>(P);
+  const int half = head_dim / 2;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(x);
+  P.vec = (half % 8 == 0) && (addr % 16 == 0);
+  P.pairs = (half % 2 == 0) && (addr % 4 == 0);
+  unsigned grid = unsigned(P.rows);
+  if (P.vec) {
+    // enough tokens per block to give every thread an item, within the
+    // block's angle slots
+    const int per_tok = heads * (half / 8);
+    int tpb = per_tok >= kThreads ? 1 : kThreads / per_tok;
+    if (tpb * half > kRopeAngles) tpb = kRopeAngles / half;
+    P.tpb = tpb < 1 ? 1 : tpb;
+    grid = unsigned((P.rows + P.tpb - 1) / P.tpb);
+  }
+  sa_rope_kernel<<<grid, kThreads, 0, stream>>>(P);
   const cudaError_t ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(ce));
   return SA_OK;

@@ -68,7 +68,10 @@ def test_gate_projection_feeds_the_gated_forward():
 
 
 @pytest.mark.parametrize("b,n,h,d,base", [(2, 333, 4, 128, 10000.0), (1, 262144, 2, 128, 10000.0),
-                                          (3, 50, 8, 64, 500000.0), (1, 7, 1, 2, 10.0)])
+                                          (3, 50, 8, 64, 500000.0), (1, 7, 1, 2, 10.0),
+                                          (1, 100, 48, 128, 10000.0),  # 3 items per thread
+                                          (2, 61, 3, 12, 10000.0),     # 4-byte accesses
+                                          (1, 9, 5, 16, 10000.0)])     # partial last block
 def test_rope_matches_oracle(b, n, h, d, base):
     rng = np.random.default_rng(n + d)
     x = round_bf16(rng.standard_normal((b, n, h, d)).astype(np.float32))
@@ -76,6 +79,37 @@ def test_rope_matches_oracle(b, n, h, d, base):
     sa.rope_(xd, base)
     g = xd.float().cpu().numpy().astype(np.float64)
     want = oracle.rope(x, base)
+    assert np.abs(g - want).max() <= 1e-2 * max(1.0, np.abs(want).max())
+    assert _rel(g, want) <= 5e-3
+
+
+def test_rope_unaligned_rows_use_narrow_accesses():
+    """A tensor whose data starts 4 bytes past a 16-byte boundary takes the
+    4-byte path and gives the same result."""
+    rng = np.random.default_rng(5)
+    x = round_bf16(rng.standard_normal((2, 40, 4, 64)).astype(np.float32))
+    buf = torch.empty(x.size + 2, dtype=torch.bfloat16, device="cuda")
+    xd = buf[2:].view(x.shape)
+    xd.copy_(dev_bf16(x))
+    assert xd.data_ptr() % 16 == 4
+    sa.rope_(xd, 10000.0)
+    g = xd.float().cpu().numpy().astype(np.float64)
+    want = oracle.rope(x, 10000.0)
+    assert np.abs(g - want).max() <= 1e-2 * max(1.0, np.abs(want).max())
+    assert _rel(g, want) <= 5e-3
+
+
+def test_rope_odd_element_offset_uses_2byte_accesses():
+    """Data starting 2 bytes past a 4-byte boundary takes the 2-byte path."""
+    rng = np.random.default_rng(6)
+    x = round_bf16(rng.standard_normal((1, 30, 3, 32)).astype(np.float32))
+    buf = torch.empty(x.size + 1, dtype=torch.bfloat16, device="cuda")
+    xd = buf[1:].view(x.shape)
+    xd.copy_(dev_bf16(x))
+    assert xd.data_ptr() % 4 == 2
+    sa.rope_(xd, 10000.0)
+    g = xd.float().cpu().numpy().astype(np.float64)
+    want = oracle.rope(x, 10000.0)
     assert np.abs(g - want).max() <= 1e-2 * max(1.0, np.abs(want).max())
     assert _rel(g, want) <= 5e-3
 
