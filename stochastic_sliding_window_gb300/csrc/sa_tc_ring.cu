@@ -639,59 +639,61 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
     const size_t orow =
         row_valid ? (size_t(tw.b) * P.n + sig_p) * P.Hq + size_t(tw.kvh) * P.g + j : 0;
     if (P.gate != nullptr && row_valid) mul *= 1.f / (1.f + expf(-P.gate[orow]));
-    uint32_t o[D / 32][32];
-#pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) tmem_ld32_async(trow + o_col + ch * 32, o[ch]);
-    tmem_wait_ld();
-#pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) reg_fence(o[ch]);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars + 8 * (kTempty + wg));
+    // O leaves TMEM in 64-column halves (fewer registers held at once); the
+    // stage is handed back once the last half is read.
     const uint64_t mul2 = f2_pack(mul, mul);
-    if (row_valid && !P.accumulate) {
-      // Each thread writes its own row, whole 32-byte sectors per store.
-      __nv_bfloat16* op = P.out + orow * D;
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int k = half * 16 + 2 * e;
-            const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(o[ch][k]),
-                                                      __uint_as_float(o[ch][k + 1])),
-                                              mul2));
-            pk[e] = pack_bf16x2(y.x, y.y);
-          }
-          st_global_v8(op + ch * 32 + half * 16, pk);
-        }
+    __nv_bfloat16* op = P.out + orow * D;
+#pragma unroll 1
+    for (int hf = 0; hf < D / 64; ++hf) {
+      uint32_t o[2][32];
+      tmem_ld32_async(trow + o_col + hf * 64, o[0]);
+      tmem_ld32_async(trow + o_col + hf * 64 + 32, o[1]);
+      tmem_wait_ld();
+      reg_fence(o[0]);
+      reg_fence(o[1]);
+      if (hf == D / 64 - 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (kTempty + wg));
       }
-    } else if (row_valid) {
-      // Second pass of the gated sum: each thread reads its own row, adds in
-      // fp32 and writes it back.
-      __nv_bfloat16* op = P.out + orow * D;
+      if (row_valid && !P.accumulate) {
+        // Each thread writes its own row, whole 32-byte sectors per store.
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint4* dst = reinterpret_cast<uint4*>(op + ch * 32);
-        uint4 prev[4];
-        if (P.accumulate) {
+        for (int ch = 0; ch < 2; ++ch) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int k = half * 16 + 2 * e;
+              const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(o[ch][k]),
+                                                        __uint_as_float(o[ch][k + 1])),
+                                                mul2));
+              pk[e] = pack_bf16x2(y.x, y.y);
+            }
+            st_global_v8(op + hf * 64 + ch * 32 + half * 16, pk);
+          }
+        }
+      } else if (row_valid) {
+        // Second pass of the gated sum: each thread reads its own row, adds in
+        // fp32 and writes it back.
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint4* dst = reinterpret_cast<uint4*>(op + hf * 64 + ch * 32);
+          uint4 prev[4];
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) prev[q4] = dst[q4];
-        }
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float f[8];
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float f[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(o[ch][q4 * 8 + 2 * e]),
-                                                      __uint_as_float(o[ch][q4 * 8 + 2 * e + 1])),
-                                              mul2));
-            f[2 * e] = y.x;
-            f[2 * e + 1] = y.y;
-          }
-          if (P.accumulate) {
+            for (int e = 0; e < 4; ++e) {
+              const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(o[ch][q4 * 8 + 2 * e]),
+                                                        __uint_as_float(o[ch][q4 * 8 + 2 * e + 1])),
+                                                mul2));
+              f[2 * e] = y.x;
+              f[2 * e + 1] = y.y;
+            }
             const __nv_bfloat162* pv2 = reinterpret_cast<const __nv_bfloat162*>(&prev[q4]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -699,9 +701,9 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
               f[2 * e] += pf.x;
               f[2 * e + 1] += pf.y;
             }
+            dst[q4] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                 pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
           }
-          dst[q4] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
         }
       }
     }
