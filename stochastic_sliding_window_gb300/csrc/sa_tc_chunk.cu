@@ -563,50 +563,58 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
     const size_t orow =
         row_valid ? (size_t(tl.b) * P.n + sig_p) * P.Hq + size_t(tl.kvh) * P.g + j : 0;
     if (P.gate != nullptr && row_valid) mul *= 1.f / (1.f + expf(-P.gate[orow]));
-    uint32_t o[D / 32][32];
-#pragma unroll
-    for (int q = 0; q < D / 32; ++q) tmem_ld32_async(o_taddr + q * 32, o[q]);
-    tmem_wait_ld();
-#pragma unroll
-    for (int q = 0; q < D / 32; ++q) reg_fence(o[q]);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars + 8 * (kOfree + h));
+    // O leaves TMEM in 64-column halves (fewer registers held at once); the
+    // accumulator is handed back once the last half is read.
     const uint64_t mul2 = f2_pack(mul, mul);
-    if (row_valid) {
-      __nv_bfloat16* op = P.out + orow * D;
+    __nv_bfloat16* op = P.out + orow * D;
+#pragma unroll 1
+    for (int hf = 0; hf < D / 64; ++hf) {
+      uint32_t o[2][32];
+      tmem_ld32_async(o_taddr + hf * 64, o[0]);
+      tmem_ld32_async(o_taddr + hf * 64 + 32, o[1]);
+      tmem_wait_ld();
+      reg_fence(o[0]);
+      reg_fence(o[1]);
+      if (hf == D / 64 - 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (kOfree + h));
+      }
+      if (row_valid) {
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
+        for (int q = 0; q < 2; ++q) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[8];
-          float f[16];
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[8];
+            float f[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int k = half * 16 + 2 * e;
-            const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(o[q][k]),
-                                                      __uint_as_float(o[q][k + 1])),
-                                              mul2));
-            f[2 * e] = y.x;
-            f[2 * e + 1] = y.y;
-          }
-          if (P.accumulate) {  // second pass of the gated sum: add the row there
-            const uint4* src = reinterpret_cast<const uint4*>(op + q * 32 + half * 16);
+            for (int e = 0; e < 8; ++e) {
+              const int k = half * 16 + 2 * e;
+              const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(o[q][k]),
+                                                        __uint_as_float(o[q][k + 1])),
+                                                mul2));
+              f[2 * e] = y.x;
+              f[2 * e + 1] = y.y;
+            }
+            __nv_bfloat16* dst = op + hf * 64 + q * 32 + half * 16;
+            if (P.accumulate) {  // second pass of the gated sum: add the row there
+              const uint4* src = reinterpret_cast<const uint4*>(dst);
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const uint4 pv4 = src[h2];
-              const __nv_bfloat162* pv2 = reinterpret_cast<const __nv_bfloat162*>(&pv4);
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const uint4 pv4 = src[h2];
+                const __nv_bfloat162* pv2 = reinterpret_cast<const __nv_bfloat162*>(&pv4);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 pf = __bfloat1622float2(pv2[e]);
-                f[8 * h2 + 2 * e] += pf.x;
-                f[8 * h2 + 2 * e + 1] += pf.y;
+                for (int e = 0; e < 4; ++e) {
+                  const float2 pf = __bfloat1622float2(pv2[e]);
+                  f[8 * h2 + 2 * e] += pf.x;
+                  f[8 * h2 + 2 * e + 1] += pf.y;
+                }
               }
             }
-          }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
-          st_global_v8(op + q * 32 + half * 16, pk);
+            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+            st_global_v8(dst, pk);
+          }
         }
       }
     }
