@@ -14,7 +14,7 @@
 // (plus its 128 Q rows); the first tile of a run fetches the whole span.
 // Copier warps fetch rows with TMA four-row gathers (tile::gather4: one
 // 128-byte column block of four arbitrary rows per copy, swizzled by the
-// copy engine), spread over the lanes of five or six warps: the copy engine's
+// copy engine), spread over the lanes of four to six warps: the copy engine's
 // intake grows with the number of warps issuing, and the copies take no
 // load/store-unit slots from the softmax warps.  Q and K of a tile are
 // needed only by S = Q K^T, V only by O = P V, so they land on separate
@@ -26,10 +26,10 @@
 // and s + R) so that a tile's span is always a plain contiguous array.
 //
 // Roles (four warpgroups, 512 threads):
-//   warps 0-4   copiers (0-5 for spans of up to 64 keys): sigma of new
-//               positions, TMA gathers of Q / K / V rows
-//   warps 5-6   maskers (warp 6 alone for spans of up to 64 keys): the
-//               tile's mask words (one 32-bit word per token and
+//   warps 0-3   copiers (0-4 for spans of 96 keys, 0-5 up to 64 keys):
+//               sigma of new positions, TMA gathers of Q / K / V rows
+//   warps 4-6   maskers (5-6 for spans of 96 keys, 6 alone up to 64 keys):
+//               the tile's mask words (one 32-bit word per token and
 //               32-key chunk, from sigma), then the hand-over to the tile's
 //               softmax warpgroup
 //   warp 7      lane 0 issues S = Q K^T of every tile in order; the warp
@@ -60,11 +60,12 @@ using namespace tcc;
 constexpr int kThreads = 512;
 // Warps 0-6 split into copiers (sigma of new positions, TMA copies) and
 // maskers (mask words, the hand-over to the softmax warpgroup).  The copies
-// per tile do not depend on the span, the mask words grow with it: spans of
-// up to two 32-key chunks leave one masker warp enough, wider ones take two.
+// per tile do not depend on the span, the mask words grow with it: one
+// masker warp for spans of up to two 32-key chunks, two for three, three
+// beyond (measured best at each).
 template <int NCH>
 struct Split {
-  static constexpr int kCopiers = NCH <= 2 ? 192 : 160;
+  static constexpr int kCopiers = NCH <= 2 ? 192 : (NCH == 3 ? 160 : 128);
   static constexpr int kMaskers = 224 - kCopiers;
 };
 constexpr int kMmaWarp = 7;
@@ -221,8 +222,9 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
-// Copiers (warps 0-4): per tile, wait for the slots it reuses to retire,
-// write sigma of its new positions to the ring, then issue its TMA copies.
+// Copiers (warps 0-3, 0-4 or 0-5): per tile, wait for the slots it reuses
+// to retire, write sigma of its new positions to the ring, then issue its
+// TMA copies.
 template <int D, int NCH>
 __device__ void copy_role(const Params& P, const CUtensorMap* tq, const CUtensorMap* tk,
                           const CUtensorMap* tv, uint8_t* smem, uint32_t sbase, uint32_t bars,
@@ -380,12 +382,12 @@ __device__ void copy_role(const Params& P, const CUtensorMap* tq, const CUtensor
   }
 }
 
-// Maskers (warps 5-6): per tile, once its sigma is in the ring, the mask
-// words, one per (token, 32-key chunk): bit e set iff key column ch*32 + e
-// lies in the token's window (truncated at the sequence ends) and, when
-// causal, sigma[q] <= sigma[p]; then hand the tile to its softmax warpgroup.
-// Four word buffers, so that a warpgroup still reading the words of tile
-// it - 2 is never overwritten.
+// Maskers (the other warps up to 6): per tile, once its sigma is in the
+// ring, the mask words, one per (token, 32-key chunk): bit e set iff key
+// column ch*32 + e lies in the token's window (truncated at the sequence
+// ends) and, when causal, sigma[q] <= sigma[p]; then hand the tile to its
+// softmax warpgroup.  Four word buffers, so that a warpgroup still reading
+// the words of tile it - 2 is never overwritten.
 template <int NCH>
 __device__ void mask_role(const Params& P, uint8_t* smem, uint32_t bars, volatile int* abort_flag,
                           volatile int* votes) {
