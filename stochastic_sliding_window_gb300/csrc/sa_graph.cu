@@ -82,6 +82,57 @@ __global__ void __launch_bounds__(kTile) rf_step(const unsigned long long* __res
   dst[k] = acc;
 }
 
+// The same layer without the causal test: the window OR of every position
+// comes from a doubling table built in shared memory.  Level L holds the OR
+// of 2^L consecutive staged words; with 2^L <= 2h+1 < 2^(L+1) a window is
+// the OR of two level-L entries (overlapping), so each position costs two
+// reads after ~log2(2h+1) passes over the staged span, instead of 2h+1.
+__global__ void __launch_bounds__(kTile) rf_step_nc(const unsigned long long* __restrict__ src,
+                                                    unsigned long long* __restrict__ dst,
+                                                    const int32_t* __restrict__ perm, int n, int h,
+                                                    int32_t* err) {
+  extern __shared__ unsigned long long s_tab[];  // two [kTile + 2h] tables, then [kTile] tokens
+  const int span = kTile + 2 * h;
+  unsigned long long* cur = s_tab;
+  unsigned long long* nxt = s_tab + span;
+  int32_t* s_tok = reinterpret_cast<int32_t*>(s_tab + 2 * span);
+  const int p0 = blockIdx.x * kTile;
+  for (int i = threadIdx.x; i < span; i += blockDim.x) {
+    const int q = p0 - h + i;
+    int tok = -1;
+    unsigned long long w = 0;
+    if (q >= 0 && q < n) {
+      tok = perm[q];
+      if (unsigned(tok) >= unsigned(n)) {
+        atomicOr(err, SA_ERRBIT_RANGE);
+        tok = -1;
+      } else {
+        w = src[tok];
+      }
+    }
+    cur[i] = w;
+    if (i >= h && i < h + kTile) s_tok[i - h] = tok;
+  }
+  __syncthreads();
+  const int width = 2 * h + 1;
+  int len = 1;
+  while (2 * len <= width) {
+    // entries past span - 2 len are never read again
+    for (int i = threadIdx.x; i + len < span; i += blockDim.x) nxt[i] = cur[i] | cur[i + len];
+    __syncthreads();
+    unsigned long long* t = cur;
+    cur = nxt;
+    nxt = t;
+    len *= 2;
+  }
+  const int p = p0 + threadIdx.x;
+  if (p >= n) return;
+  const int k = s_tok[threadIdx.x];
+  if (k < 0) return;
+  // window [threadIdx.x, threadIdx.x + width) of the staged span
+  dst[k] = cur[threadIdx.x] | cur[threadIdx.x + width - len];
+}
+
 // sizes[t0 + t] += number of tokens whose word has bit t set.
 __global__ void rf_count(const unsigned long long* __restrict__ words, int n, int cnt,
                          int64_t* __restrict__ sizes_row, int t0) {
@@ -125,8 +176,11 @@ sa_status_t launch_receptive_field(const int32_t* perms, int layers, int n, int 
   cudaError_t ce = cudaMemsetAsync(sizes, 0, size_t(layers) * num_targets * sizeof(int64_t), s);
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "clearing sizes: %s", cudaGetErrorString(ce));
   const int step_blocks = (n + kTile - 1) / kTile;
-  const size_t step_smem = size_t(kTile + 2 * h) * (sizeof(unsigned long long) + sizeof(int32_t));
-  ce = cudaFuncSetAttribute(rf_step, cudaFuncAttributeMaxDynamicSharedMemorySize, int(step_smem));
+  const size_t step_smem = causal
+      ? size_t(kTile + 2 * h) * (sizeof(unsigned long long) + sizeof(int32_t))
+      : size_t(kTile + 2 * h) * 2 * sizeof(unsigned long long) + size_t(kTile) * sizeof(int32_t);
+  ce = causal ? cudaFuncSetAttribute(rf_step, cudaFuncAttributeMaxDynamicSharedMemorySize, int(step_smem))
+              : cudaFuncSetAttribute(rf_step_nc, cudaFuncAttributeMaxDynamicSharedMemorySize, int(step_smem));
   if (ce != cudaSuccess) return fail(SA_ERR_CUDA, "rf_step attribute: %s", cudaGetErrorString(ce));
   const int count_blocks = (n + 255) / 256 < 152 * 4 ? (n + 255) / 256 : 152 * 4;
   for (int t0 = 0; t0 < num_targets; t0 += 64) {
@@ -139,8 +193,12 @@ sa_status_t launch_receptive_field(const int32_t* perms, int layers, int n, int 
       unsigned long long* cur = wa;
       unsigned long long* nxt = wb;
       for (int l = L; l >= 1; --l) {
-        rf_step<<<step_blocks, kTile, step_smem, s>>>(cur, nxt, perms + size_t(l - 1) * n, n, h,
-                                                     causal, err);
+        if (causal)
+          rf_step<<<step_blocks, kTile, step_smem, s>>>(cur, nxt, perms + size_t(l - 1) * n, n, h,
+                                                       causal, err);
+        else
+          rf_step_nc<<<step_blocks, kTile, step_smem, s>>>(cur, nxt, perms + size_t(l - 1) * n, n, h,
+                                                          err);
         unsigned long long* t = cur;
         cur = nxt;
         nxt = t;
