@@ -31,6 +31,7 @@ using namespace tcc;
 
 constexpr int kThreads = 128;
 constexpr int kKB = 64;  // d_model columns per block (128 bytes of bf16)
+constexpr int kMaxStages = 4;
 
 struct GateParams {
   const __nv_bfloat16* x;    // [M, D]
@@ -42,6 +43,7 @@ struct GateParams {
   float* a_swa;
   int32_t* err;
   int M, D, Hq, n_pad, num_tiles;
+  int stages;                          // x/w blocks in flight: 2 or kMaxStages (a power of two)
   uint32_t x_bytes, w_bytes, off_bar;  // one stage's x and w blocks; barrier offset
   long long timeout_cycles;
 };
@@ -51,21 +53,23 @@ __global__ void __launch_bounds__(kThreads, 2) sa_gate_proj_kernel(const __grid_
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t stage_bytes = P.x_bytes + P.w_bytes;
-  const uint32_t bars = sbase + P.off_bar;  // [2] MMA of the stage done, [1] drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.off_bar + 24);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.off_bar + 28);
+  const uint32_t bars = sbase + P.off_bar;  // [kMaxStages] MMA of the stage done, then the drain
+  const uint32_t drain_bar = bars + 8 * kMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.off_bar + 8 * kMaxStages + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.off_bar + 8 * kMaxStages + 12);
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int S = P.stages;
+  const long long smask = S - 1;
+  const int sshift = S == 4 ? 2 : 1;
   if (tid == 0) {
-    mbar_init(bars, 1);
-    mbar_init(bars + 8, 1);
-    mbar_init(bars + 16, 1);
+    for (int i = 0; i <= kMaxStages; ++i) mbar_init(bars + 8 * i, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // padded weight rows stay zero in both stages
-  for (int s = 0; s < 2; ++s)
+  // padded weight rows stay zero in every stage
+  for (int st = 0; st < S; ++st)
     for (int i = 2 * P.Hq * 128 + tid * 16; i < P.n_pad * 128; i += kThreads * 16)
-      *reinterpret_cast<uint4*>(smem + s * stage_bytes + P.x_bytes + i) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(smem + st * stage_bytes + P.x_bytes + i) = make_uint4(0, 0, 0, 0);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
@@ -80,13 +84,15 @@ __global__ void __launch_bounds__(kThreads, 2) sa_gate_proj_kernel(const __grid_
   const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
   const int nkb = P.D / kKB;
   const uint32_t id = idesc_bf16(kBM, P.n_pad, 0);
-  uint32_t phase[2] = {0, 0};
+  // Blocks are numbered over all of this CTA's tiles: block g uses stage
+  // g mod S, and its MMA commit completes phase g / S of that stage's barrier.
+  long long g0 = 0;  // number of this CTA's first block in the current tile
   bool alive = true;
-  for (int tile = blockIdx.x; tile < P.num_tiles && alive; tile += gridDim.x) {
+  for (int tile = blockIdx.x; tile < P.num_tiles && alive; tile += gridDim.x, g0 += nkb) {
     const int m0 = tile * kBM;
     // one 64-column block of x (128 rows) and of both weights (2 Hq rows)
-    auto load = [&](int kb, int s) {
-      const uint32_t xs = sbase + s * stage_bytes, ws = xs + P.x_bytes;
+    auto load = [&](int kb) {
+      const uint32_t xs = sbase + uint32_t((g0 + kb) & smask) * stage_bytes, ws = xs + P.x_bytes;
       for (int idx = tid; idx < kBM * 8; idx += kThreads) {
         const int r = idx >> 3, c = idx & 7;
         const int m = min(m0 + r, P.M - 1);
@@ -97,54 +103,54 @@ __global__ void __launch_bounds__(kThreads, 2) sa_gate_proj_kernel(const __grid_
         const __nv_bfloat16* w = r < P.Hq ? P.w_sa + size_t(r) * P.D : P.w_swa + size_t(r - P.Hq) * P.D;
         cp_async16(ws + r * 128 + ((c ^ (r & 7)) << 4), w + kb * kKB + c * 8);
       }
-      asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    load(0, 0);
+    // the first S - 1 blocks (their stages were last read by MMAs that the
+    // previous tile's final wait covers); one commit group per block, empty
+    // past the last block, so the group count stays uniform
+    for (int j = 0; j < S - 1; ++j) {
+      if (j < nkb) load(j);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb & 1;
-      if (kb + 1 < nkb) {
-        // stage 1 - s was last read by the MMAs of block kb - 1
+      const long long gb = g0 + kb;
+      const int nk = kb + S - 1;  // the block loaded now, into the stage block kb - 1 used
+      if (nk < nkb) {
         if (kb >= 1) {
-          const bool ok = bounded_wait(bars + 8 * (1 - s), phase[1 - s], P.timeout_cycles, P.err,
-                                       abort_flag);
-          phase[1 - s] ^= 1;
+          const long long gp = gb - 1;
+          const bool ok = bounded_wait(bars + 8 * uint32_t(gp & smask), uint32_t(gp >> sshift) & 1u,
+                                       P.timeout_cycles, P.err, abort_flag);
           if (__syncthreads_or(ok ? 0 : 1)) {
             alive = false;
             break;
           }
         }
-        load(kb + 1, 1 - s);
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-      } else {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        load(nk);
       }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      // groups committed so far: kb + S; at most S - 1 pending means block kb landed
+      if (S == 4)
+        asm volatile("cp.async.wait_group 3;" ::: "memory");
+      else
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
       fence_proxy_async_smem();
       __syncthreads();
       if (tid == 0) {
         tc_fence_after();
-        const uint32_t xs = sbase + s * stage_bytes;
+        const uint32_t xs = sbase + uint32_t(gb & smask) * stage_bytes;
         const uint64_t a0 = sdesc_sw128(xs, 16, 1024), b0 = sdesc_sw128(xs + P.x_bytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < kKB / 16; ++kk)
           umma_bf16(tmem, a0 + 2 * kk, b0 + 2 * kk, id, (kb > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bars + 8 * s);
+        umma_commit(bars + 8 * uint32_t(gb & smask));
       }
     }
     if (!alive) break;
     // the last block's MMAs (and with them all earlier ones) are done
     {
-      const int s = (nkb - 1) & 1;
-      const bool ok = bounded_wait(bars + 8 * s, phase[s], P.timeout_cycles, P.err, abort_flag);
-      phase[s] ^= 1;
-      if (nkb >= 2) {  // the other stage's last commit was consumed by the loop's wait or is done
-        const int o = 1 - s;
-        const bool ok2 = nkb >= 2 && bounded_wait(bars + 8 * o, phase[o], P.timeout_cycles, P.err,
-                                                   abort_flag);
-        phase[o] ^= 1;
-        if (__syncthreads_or((ok && ok2) ? 0 : 1)) break;
-      } else if (__syncthreads_or(ok ? 0 : 1)) {
-        break;
-      }
+      const long long gl = g0 + nkb - 1;
+      const bool ok = bounded_wait(bars + 8 * uint32_t(gl & smask), uint32_t(gl >> sshift) & 1u,
+                                   P.timeout_cycles, P.err, abort_flag);
+      if (__syncthreads_or(ok ? 0 : 1)) break;
     }
     tc_fence_after();
     const int m = m0 + tid;
@@ -170,9 +176,9 @@ __global__ void __launch_bounds__(kThreads, 2) sa_gate_proj_kernel(const __grid_
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   if (tid == 0) {
-    umma_commit(bars + 16);
+    umma_commit(drain_bar);
     const long long t0 = clock64();
-    while (!mbar_try_wait(bars + 16, 0) && clock64() - t0 < kDrainCycles) {
+    while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < kDrainCycles) {
     }
   }
   tc_fence_before();
@@ -333,11 +339,14 @@ sa_status_t launch_gate_projection(const void* x, int tokens, int d_model, int h
   P.num_tiles = (tokens + kBM - 1) / kBM;
   P.x_bytes = kBM * 128;
   P.w_bytes = uint32_t(P.n_pad) * 128;
-  P.off_bar = 2 * (P.x_bytes + P.w_bytes);
+  // four blocks in flight when two such CTAs fit an SM, else two
+  const uint32_t stage_bytes = P.x_bytes + P.w_bytes;
+  P.stages = uint32_t(kMaxStages) * stage_bytes <= 100u * 1024 ? kMaxStages : 2;
+  P.off_bar = uint32_t(P.stages) * stage_bytes;
   P.timeout_cycles = wait_limit_cycles();
   // at least 80 KB per CTA: at most two CTAs share an SM, so their two
   // 256-column TMEM allocations always fit
-  const uint32_t need = P.off_bar + 32 + 1024;
+  const uint32_t need = P.off_bar + 8 * (kMaxStages + 1) + 16 + 1024;
   const uint32_t smem = need > 80u * 1024 ? need : 80u * 1024;
   cudaError_t ce = cudaFuncSetAttribute(sa_gate_proj_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
