@@ -664,6 +664,89 @@ def run_prologue(args, wl):
     return 0
 
 
+def run_shard(args, wl):
+    """sigma-routed sequence sharding, measured on one GPU: every rank's local
+    problem of the workload's sequence (its span's Q/K/V rows, already
+    gathered, and its local permutation) through sa_forward, one rank after
+    another.  One GPU cannot run the two all-to-all exchanges, so they are not
+    in the number: `value` is the sequence's tokens over the slowest rank's
+    local forward, the rate the ranks would reach if the exchanges overlapped
+    perfectly.  The host plan (sa_shard_plan) is timed separately."""
+    import numpy as np
+    import torch
+    import stochastic_sliding_window_gb300 as sa
+    from stochastic_sliding_window_gb300 import shard
+    rank0, world_procs, local = dist_env()
+    b, n, hq, hkv, d = wl["batch"], wl["seq_len"], wl["num_q_heads"], wl["num_kv_heads"], wl["head_dim"]
+    if b != 1:
+        raise SystemExit("sequence sharding splits one sequence: the workload needs batch 1")
+    w, W = wl["window"], args.shard_world
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    perm = sa.make_perms(wl["seed"], 0, 1, n)[0]
+    t0 = time.perf_counter()
+    ps = shard.plans(perm, w, W)
+    plan_ms = (time.perf_counter() - t0) * 1e3 / W
+    g = torch.Generator(device=dev).manual_seed(0)
+    q = torch.randn((n, hq, d), device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn((n, hkv, d), device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn((n, hkv, d), device=dev, generator=g).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    per_rank, spans = [], []
+    kernels = set()
+    # every rank's local inputs (the rows gather_local would deliver), then a
+    # warm-up of all of them before any is timed
+    local_in = []
+    for pl in ps:
+        tok = torch.from_numpy(pl.tokens.astype(np.int64)).to(dev)
+        ql, kl, vl = (x.index_select(0, tok)[None].contiguous() for x in (q, k, v))
+        lp = torch.from_numpy(pl.local_perm[None, :].copy()).to(dev)
+        local_in.append((ql, kl, vl, lp, torch.empty_like(ql)))
+        spans.append(int(pl.tokens.shape[0]))
+    for _ in range(args.warmup):
+        for ql, kl, vl, lp, yl in local_in:
+            sa.sa_forward(ql, kl, vl, lp, w, causal=wl["causal"], out=yl, err=err)
+            kernels.add(sa.last_kernel())
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    for ql, kl, vl, lp, yl in local_in:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record()
+            sa.sa_forward(ql, kl, vl, lp, w, causal=wl["causal"], out=yl, err=err)
+            ends[i].record()
+        torch.cuda.synchronize(dev)
+        per_rank.append(sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / args.steps)
+    clocks = sampler.stop()
+    if sa.check_error(err) != sa.SA_OK:
+        raise RuntimeError("device error word set")
+    ms = max(per_rank)
+    peaks = load_peaks()
+    # a rank's local bytes: its span's Q/K/V rows and output rows once, and its local sigma
+    bytes_rank = [sp * (2 * (hq + 2 * hkv) * d + 2 * hq * d + 4) for sp in spans]
+    slow = per_rank.index(ms)
+    ach = bytes_rank[slow] / (ms * 1e-3) / 1e9
+    if rank0 == 0:
+        print(json.dumps(dict(
+            metric=f"sharded SA tokens/s over {W} ranks' local forwards, measured one rank at a "
+                   f"time on one GPU (exchanges not included; n={n}, w={w})",
+            value=n / (ms * 1e-3), unit="tokens/s", n_gpus=1, steps=args.steps,
+            warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="strong",
+            vs_baseline=None, dtype="bf16", data="synthetic",
+            config=dict(config_of(wl), world=W),
+            shard=dict(per_rank_ms=per_rank, span_rows=spans, halo_overhead=sum(spans) / n,
+                       plan_ms_per_rank=plan_ms, kernels=sorted(kernels)),
+            roofline=dict(bound="hbm", achieved=ach, peak=peaks["hbm_gbs"], unit="GB/s",
+                          frac=ach / peaks["hbm_gbs"], traffic=None,
+                          bytes_per_launch=bytes_rank[slow]),
+            gpu_launches=W * args.steps, clocks=clocks)), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -677,9 +760,12 @@ def main():
                     help="shape to time (default: the long-prefill GQA headline)")
     ap.add_argument("--window", type=int, default=0, help="override the workload's window")
     ap.add_argument("--seq-len", type=int, default=0, help="override the workload's length")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "receptive", "prologue"], default="fwd",
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "receptive", "prologue", "shard"],
+                    default="fwd",
                     help="time the forward pass (default), the backward pass, or the "
                          "receptive-field analytics of stacked layers")
+    ap.add_argument("--shard-world", type=int, default=8,
+                    help="ranks of the sequence-sharding pass (--pass shard)")
     ap.add_argument("--causal-rf", action="store_true",
                     help="receptive fields of causal SA (default: non-causal)")
     ap.add_argument("--kernel", choices=["auto", "simt", "gather", "ring", "chunk"],
@@ -694,6 +780,8 @@ def main():
         return run_receptive(args)
     if args.pass_ == "prologue":
         return run_prologue(args, wl)
+    if args.pass_ == "shard":
+        return run_shard(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
