@@ -14,7 +14,7 @@
 // (plus its 128 Q rows); the first tile of a run fetches the whole span.
 // Copier warps fetch rows with TMA four-row gathers (tile::gather4: one
 // 128-byte column block of four arbitrary rows per copy, swizzled by the
-// copy engine), spread over the lanes of four to six warps: the copy engine's
+// copy engine), spread over the lanes of five or six warps: the copy engine's
 // intake grows with the number of warps issuing, and the copies take no
 // load/store-unit slots from the softmax warps.  Q and K of a tile are
 // needed only by S = Q K^T, V only by O = P V, so they land on separate
@@ -26,10 +26,10 @@
 // and s + R) so that a tile's span is always a plain contiguous array.
 //
 // Roles (four warpgroups, 512 threads):
-//   warps 0-3   copiers (0-4 for spans of 96 keys, 0-5 up to 64 keys):
-//               sigma of new positions, TMA gathers of Q / K / V rows
-//   warps 4-6   maskers (5-6 for spans of 96 keys, 6 alone up to 64 keys):
-//               the tile's mask words (one 32-bit word per token and
+//   warps 0-4   copiers (0-5 for spans of up to 128 keys): sigma of new
+//               positions, TMA gathers of Q / K / V rows
+//   warps 5-6   maskers (warp 6 alone for spans of up to 128 keys): the
+//               tile's mask words (one 32-bit word per token and
 //               32-key chunk, from sigma), then the hand-over to the tile's
 //               softmax warpgroup
 //   warp 7      lane 0 issues S = Q K^T of every tile in order; the warp
@@ -61,11 +61,11 @@ constexpr int kThreads = 512;
 // Warps 0-6 split into copiers (sigma of new positions, TMA copies) and
 // maskers (mask words, the hand-over to the softmax warpgroup).  The copies
 // per tile do not depend on the span, the mask words grow with it: one
-// masker warp for spans of up to two 32-key chunks, two for three, three
-// beyond (measured best at each).
+// masker warp for spans of up to four 32-key chunks, two beyond (measured
+// best at each).
 template <int NCH>
 struct Split {
-  static constexpr int kCopiers = NCH <= 2 ? 192 : (NCH == 3 ? 160 : 128);
+  static constexpr int kCopiers = NCH <= 4 ? 192 : 160;
   static constexpr int kMaskers = 224 - kCopiers;
 };
 constexpr int kMmaWarp = 7;
@@ -222,7 +222,7 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
-// Copiers (warps 0-3, 0-4 or 0-5): per tile, wait for the slots it reuses
+// Copiers (warps 0-4 or 0-5): per tile, wait for the slots it reuses
 // to retire, write sigma of its new positions to the ring, then issue its
 // TMA copies.
 template <int D, int NCH>
@@ -420,13 +420,18 @@ __device__ void mask_role(const Params& P, uint8_t* smem, uint32_t bars, volatil
       const int hi = w.p0 + tt < P.n ? min(tt + P.left + P.right, P.n - 1 - w.p0 + P.left) : -1;
       uint32_t word = band_bits(lo, hi, ch * 32);
       if (P.causal) {
-        const int ks = sig[ch * 32 + lane];
+        // lane tt compares its token's sigma with the chunk's 32 key tokens,
+        // read four at a time by all lanes together (broadcast loads)
         const int st = sig[P.left + min(tt, P.Bt - 1)];
+        const int4* s4p = reinterpret_cast<const int4*>(sig + ch * 32);
         uint32_t cw = 0u;
-#pragma unroll 8
-        for (int u = 0; u < 32; ++u) {
-          const uint32_t bb = __ballot_sync(0xffffffffu, ks <= __shfl_sync(0xffffffffu, st, u));
-          cw = u == lane ? bb : cw;
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const int4 s4 = s4p[e4];
+          cw |= (s4.x <= st ? 1u : 0u) << (4 * e4);
+          cw |= (s4.y <= st ? 1u : 0u) << (4 * e4 + 1);
+          cw |= (s4.z <= st ? 1u : 0u) << (4 * e4 + 2);
+          cw |= (s4.w <= st ? 1u : 0u) << (4 * e4 + 3);
         }
         word &= cw;
       }
