@@ -417,8 +417,10 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
       // Mask words of the chunk for this warp's tokens: bit e of word
       // (token, q) set iff key column c*128 + 32q + e is attended.
       uint32_t* wb = wall + b * (32 * kSub);
+      // (consecutive lanes take consecutive tokens of one piece, so the
+      // piece's key tokens are broadcast loads)
       for (int w = lane; w < tpw * kSub; w += 32) {
-        const int ti = w / kSub, q = w - ti * kSub;
+        const int q = w / tpw, ti = w - q * tpw;
         const int tt = tw0 + ti;
         const int lo = max(tt, P.left - tl.p0) - c * kKC - 32 * q;
         const int hi = (tl.p0 + tt < P.n ? min(tt + P.left + P.right, P.n - 1 - tl.p0 + P.left)
