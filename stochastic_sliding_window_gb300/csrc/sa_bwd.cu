@@ -299,13 +299,25 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
       return bits;
     };
     const int nch = sp / 32;
+    // This row's words of its pieces ch = part + 2k (k < 4: spans of up to
+    // 256 keys), built once for the three passes; picked by a select chain
+    // (an indexed register array would live in local memory).
+    uint32_t wb0 = 0u, wb1 = 0u, wb2 = 0u, wb3 = 0u;
+    if (part < nch) wb0 = bits_of(part);
+    if (part + 2 < nch) wb1 = bits_of(part + 2);
+    if (part + 4 < nch) wb2 = bits_of(part + 4);
+    if (part + 6 < nch) wb3 = bits_of(part + 6);
+    auto word = [&](int ch) {
+      const int k = (ch - part) >> 1;
+      return k == 0 ? wb0 : (k == 1 ? wb1 : (k == 2 ? wb2 : wb3));
+    };
     // pass 1: the attended maximum of the raw scores (this half's pieces)
     float mx = -INFINITY;
 #pragma unroll 1
     for (int ch = part; ch < nch; ch += 2) {
       uint32_t s_[32];
       tmem_ld32(trow + ch * 32, s_);
-      const uint32_t bits = bits_of(ch);
+      const uint32_t bits = word(ch);
 #pragma unroll
       for (int e = 0; e < 32; ++e)
         if ((bits >> e) & 1u) mx = fmaxf(mx, __uint_as_float(s_[e]));
@@ -321,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
       uint32_t s_[32], dp[32];
       tmem_ld32(trow + ch * 32, s_);
       tmem_ld32(trow + sp + ch * 32, dp);
-      const uint32_t bits = bits_of(ch);
+      const uint32_t bits = word(ch);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const float ex = (bits >> e) & 1u ? fast_exp2(fmaf(__uint_as_float(s_[e]), P.scale_log2, -ms))
@@ -353,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
       uint32_t s_[32], dp[32];
       tmem_ld32(trow + ch * 32, s_);
       tmem_ld32(trow + sp + ch * 32, dp);
-      const uint32_t bits = bits_of(ch);
+      const uint32_t bits = word(ch);
       uint32_t pk[16];
 #pragma unroll
       for (int e2 = 0; e2 < 16; ++e2) {
@@ -526,25 +538,34 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
         tmem_ld32(trow + c_st + ch * 32, s_);
         tmem_ld32(trow + c_dpt + ch * 32, dp);
         uint32_t pk[16], dk2[16];
+        // the rows' lse2' and D four at a time (the same for every lane:
+        // broadcast loads)
 #pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          float pv[2], dv[2];
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const int rb = ch * 32 + 4 * e4;
+          const float4 l4 = *reinterpret_cast<const float4*>(cl + rb);
+          const float4 d4 = *reinterpret_cast<const float4*>(cd + rb);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dv[4];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int rr = ch * 32 + 2 * e2 + u;
+          for (int u = 0; u < 4; ++u) {
+            const int rr = rb + u;
             const int tq = rr >> P.log2g;
             const int qpos = c0 + tq;
             const int qtk = qt[tq];
             bool ok = sig_k >= 0 && qtk >= 0 && kpos >= qpos - P.left && kpos <= qpos + P.right;
             if (kCausal) ok = ok && sig_k <= qtk;
-            const float p = ok ? fast_exp2(fmaf(__uint_as_float(s_[2 * e2 + u]), P.scale_log2,
-                                                -cl[rr]))
+            const float p = ok ? fast_exp2(fmaf(__uint_as_float(s_[4 * e4 + u]), P.scale_log2,
+                                                -lv[u]))
                                : 0.f;
             pv[u] = p;
-            dv[u] = p * (__uint_as_float(dp[2 * e2 + u]) - cd[rr]);
+            dv[u] = p * (__uint_as_float(dp[4 * e4 + u]) - dv4[u]);
           }
-          pk[e2] = pack_bf16x2(pv[0], pv[1]);
-          dk2[e2] = pack_bf16x2(dv[0], dv[1]);
+          pk[2 * e4] = pack_bf16x2(pv[0], pv[1]);
+          pk[2 * e4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk2[2 * e4] = pack_bf16x2(dv[0], dv[1]);
+          dk2[2 * e4 + 1] = pack_bf16x2(dv[2], dv[3]);
         }
         tmem_st16(trow + c_st + ch * 32, pk);
         tmem_st16(trow + c_dpt + ch * 32, dk2);
