@@ -107,11 +107,11 @@ enum : uint32_t {
   kQKdone = 3,   // [kQStages] S MMA of tile it done: its Q stage and K rows are free
   kFullV = 6,    // [kVDepth] new V rows of tile it landed (TMA bytes)
   kPVdone = 9,   // [kVDepth] O MMA of tile it done: its V rows are free
-  kSready = 12,  // [2] sigma of tile it written (per softmax warpgroup)
-  kSfree = 14,   // [2] the warpgroup has read the sigma it needs for tile it
+  kSready = 12,  // [2] sigma and mask words of tile it ready (per softmax warpgroup)
+  kSfree = 14,   // [2] the warpgroup has read the sigma and words of tile it
   kSfull = 16,   // [2] S of tile it in TMEM stage it & 1
   kPfull = 18,   // [2] P of tile it written to TMEM (the warpgroup's 4 warps)
-  kOfull = 20,   // [2] O of tile it in TMEM
+  kOfull = 20,   // [2] O of tile it in TMEM (committed by the warpgroup's issuer)
   kTempty = 22,  // [2] TMEM stage read out by the epilogue
   kDrain = 24,   // final completion of the S MMAs
   kDrainWg = 25, // [2] final completion of the warpgroup's O MMAs
