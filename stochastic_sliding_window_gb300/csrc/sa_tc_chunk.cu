@@ -451,32 +451,23 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
       }
       tc_fence_after();
       const uint32_t sb = tmem_base + lanes + uint32_t(h * kKC);
-      // pass 1: the chunk's attended maximum
+      // pass 1: the chunk's maximum over all its 128 key columns, attended
+      // or not, returned by the TMEM loads themselves (no mask test).  Every
+      // column holds a real key of this launch (positions past either end
+      // load a clamped token's rows), so the reference below is finite and
+      // never below the row's attended maximum; a reference so far above it
+      // that the attended p underflow shows as a row sum below 2^-60, and
+      // that row is recomputed exactly (exact_row).
       float mx = -INFINITY;
 #pragma unroll 1
-      for (int q = 0; q < kSub; ++q) {
-        uint32_t v[32];
-        tmem_ld32(sb + q * 32, v);
-        const uint32_t bits = wrow[q];
-        float m0 = mx, m1 = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float x0 = (bits >> e) & 1u ? __uint_as_float(v[e]) : -INFINITY;
-          const float x1 = (bits >> (e + 1)) & 1u ? __uint_as_float(v[e + 1]) : -INFINITY;
-          const float x2 = (bits >> (e + 2)) & 1u ? __uint_as_float(v[e + 2]) : -INFINITY;
-          const float x3 = (bits >> (e + 3)) & 1u ? __uint_as_float(v[e + 3]) : -INFINITY;
-          m0 = fmax3(m0, x0, x1);
-          m1 = fmax3(m1, x2, x3);
-        }
-        mx = fmaxf(m0, m1);
-      }
+      for (int q = 0; q < kSub; ++q) mx = fmaxf(mx, tmem_max32(sb + q * 32));
       // online reference: rescale only when the maximum grows past 2^8
       float alpha = 1.f;
       bool rescale = false;
       if (mx != -INFINITY) {
         const float msc = mx * P.scale_log2;
         if (ms_ref == -INFINITY) {
-          ms_ref = msc;  // first attended keys of the row: O and l are still 0
+          ms_ref = msc;  // the row's first chunk: O and l are still 0
         } else if (msc > ms_ref + kRescaleLog2) {
           alpha = fast_exp2(ms_ref - msc);
           ms_ref = msc;
@@ -561,6 +552,10 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
     // epilogue: O / l (x sigmoid(gate)), scattered to row sigma[p0 + t]
     if (!wwait(bars + 8 * (kOfull + h), uint32_t(x & 1))) break;
     tc_fence_after();
+    // l is at least the row's largest attended p, 2^-(reference - attended
+    // maximum) (every valid row attends its own key): l < 2^-60 means that
+    // gap is above 60, and the row is computed exactly instead
+    const bool exact = row_valid && l < 0x1p-60f;
     float mul = l > 0.f ? 1.f / l : 0.f;
     const size_t orow =
         row_valid ? (size_t(tl.b) * P.n + sig_p) * P.Hq + size_t(tl.kvh) * P.g + j : 0;
@@ -582,7 +577,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + 8 * (kOfree + h));
       }
-      if (row_valid) {
+      if (row_valid && !exact) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
 #pragma unroll
@@ -620,6 +615,10 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
         }
       }
     }
+    if (exact)
+      exact_row<D>(ExactRow{P.q, P.k, P.v, P.perm ? P.perm + size_t(tl.b) * P.n : nullptr,
+                            P.gate, P.out, orow, size_t(tl.b) * P.n, P.n, P.Hkv, tl.kvh, tl.p0 + t,
+                            sig_p, P.left, P.right, P.causal, P.accumulate, P.scale_log2});
   }
   if (issued) {  // an abort can leave this thread's last O MMA in flight
     umma_commit(bars + 8 * (kDrainH + h));

@@ -202,6 +202,35 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// Maximum of 32 consecutive fp32 columns of this thread's TMEM lane, taken by
+// the loads themselves (tcgen05.ld.red, an sm_103 form: the load returns the
+// max of the elements it read beside the elements).  The elements are not
+// used.  Two 16-column loads, one wait (a 32-column ld.red made ptxas spill).
+#pragma nv_diag_suppress 550  // a and b are written and deliberately unused
+__device__ __forceinline__ float tmem_max32(uint32_t taddr) {
+  uint32_t a[16], b[16];
+  float m0, m1;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15}, %16, [%17];"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]),
+        "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]),
+        "=r"(a[14]), "=r"(a[15]), "=f"(m0)
+      : "r"(taddr)
+      : "memory");
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15}, %16, [%17];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]),
+        "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]),
+        "=r"(b[14]), "=r"(b[15]), "=f"(m1)
+      : "r"(taddr + 16)
+      : "memory");
+  return fmaxf(m0, m1);
+}
+#pragma nv_diag_default 550
 // Orders every later use of r after the preceding tmem_wait_ld().
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 #pragma unroll
@@ -336,6 +365,76 @@ __device__ __forceinline__ void exp_store_chunk(const uint32_t (&v)[32], float m
     uint4* dst = reinterpret_cast<uint4*>(pbase + kb * (kBM * 128) + r * 128 +
                                           ((c16 ^ (r & 7)) << 4));
     *dst = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+// One SA output row computed exactly by one thread on its own, from global
+// memory: the row of position p (query token sig_p) at output row `orow`.
+// fp32 scores against the keys of the band [p - left, p + right] within
+// [0, n) that the row attends (sigma(q) <= sigma(p) when causal), their
+// maximum, the softmax and the weighted sum of V rows, then the gate and the
+// accumulation as the tensor-core epilogues apply them.  The tensor-core
+// kernels take their softmax reference from every key column they hold,
+// attended or not; this is the path of a row whose attended maximum lies so
+// far below that reference that its p underflow (a row sum below 2^-60),
+// which ordinary inputs never produce.  Kept out of line.
+struct ExactRow {
+  const __nv_bfloat16* q;   // [B, n, Hq, d]
+  const __nv_bfloat16* k;   // [B, n, Hkv, d]
+  const __nv_bfloat16* v;
+  const int32_t* perm_b;    // sigma of this batch row, or nullptr (identity)
+  const float* gate;        // logits [B, n, Hq] or nullptr
+  __nv_bfloat16* out;
+  size_t orow, kv0;         // output (= query) row; b * n
+  int n, Hkv, kvh, p, sig_p, left, right, causal, accumulate;
+  float scale_log2;
+};
+
+template <int D>
+__device__ __noinline__ void exact_row(const ExactRow r) {
+  const __nv_bfloat16* qr = r.q + r.orow * D;
+  const int q_lo = max(r.p - r.left, 0), q_hi = min(r.p + r.right, r.n - 1);
+  auto key_token = [&](int pos) { return r.perm_b ? r.perm_b[pos] : pos; };
+  auto attended = [&](int tok) {
+    return unsigned(tok) < unsigned(r.n) && !(r.causal && tok > r.sig_p);
+  };
+  auto score = [&](int tok) {
+    const __nv_bfloat16* kr = r.k + ((r.kv0 + tok) * r.Hkv + r.kvh) * D;
+    float s = 0.f;
+    for (int e = 0; e < D; ++e) s = fmaf(__bfloat162float(qr[e]), __bfloat162float(kr[e]), s);
+    return s * r.scale_log2;
+  };
+  float m = -INFINITY;
+  for (int pos = q_lo; pos <= q_hi; ++pos) {
+    const int tok = key_token(pos);
+    if (attended(tok)) m = fmaxf(m, score(tok));
+  }
+  float mul = 1.f;
+  if (r.gate != nullptr) mul = 1.f / (1.f + expf(-r.gate[r.orow]));
+  __nv_bfloat16* op = r.out + r.orow * D;
+  // 32 output columns at a time (registers, no local array); the weights
+  // are recomputed for each block
+  for (int e0 = 0; e0 < D; e0 += 32) {
+    float y[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) y[e] = 0.f;
+    float l = 0.f;
+    for (int pos = q_lo; pos <= q_hi; ++pos) {
+      const int tok = key_token(pos);
+      if (!attended(tok)) continue;
+      const float w = exp2f(score(tok) - m);
+      l += w;
+      const __nv_bfloat16* vr = r.v + ((r.kv0 + tok) * r.Hkv + r.kvh) * D + e0;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) y[e] = fmaf(w, __bfloat162float(vr[e]), y[e]);
+    }
+    const float f = l > 0.f ? mul / l : 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      float o = y[e] * f;
+      if (r.accumulate) o += __bfloat162float(op[e0 + e]);
+      op[e0 + e] = __float2bfloat16(o);
+    }
   }
 }
 

@@ -560,27 +560,42 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
     tc_fence_after();
     // Two passes over the row's 32-column chunks, loops kept rolled so the
     // code stays small (the roles share each SM's instruction cache):
-    // the attended maximum, then p = 2^(s*scale*log2e - max) for attended
-    // columns (0 elsewhere) written back to TMEM as bf16 over the row's own S
-    // columns (P column pair c/2 holds keys c and c+1; chunk ch's P lands on
-    // S columns already consumed).
+    // a reference maximum, then p = 2^(s*scale*log2e - reference) for
+    // attended columns (0 elsewhere) written back to TMEM as bf16 over the
+    // row's own S columns (P column pair c/2 holds keys c and c+1; chunk ch's
+    // P lands on S columns already consumed).
+    // From three chunks on, the reference is the maximum over ALL the span's
+    // columns, attended or not, which the TMEM loads return themselves (no
+    // mask test, no compare per element).  Every span column is a real key
+    // of this launch (a position past either end loads a clamped token's
+    // row), so for finite inputs the reference is finite and at least the
+    // attended maximum: no p exceeds 1.  Softmax does not depend on the
+    // reference; a reference so far above the attended maximum that the
+    // attended p underflow shows as a row sum below 2^-60, and that row is
+    // recomputed exactly (exact_row).  Spans of one or two chunks keep the
+    // attended maximum, which costs no more there.
     float mx = -INFINITY;
+    if constexpr (NCH <= 2) {
 #pragma unroll 1
-    for (int ch = 0; ch < NCH; ++ch) {
-      uint32_t v[32];
-      tmem_ld32(trow + ch * 32, v);
-      const uint32_t bits = word_of(wd, ch);
-      float m0 = mx, m1 = -INFINITY;
+      for (int ch = 0; ch < NCH; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(trow + ch * 32, v);
+        const uint32_t bits = word_of(wd, ch);
+        float m0 = mx, m1 = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float x0 = (bits >> e) & 1u ? __uint_as_float(v[e]) : -INFINITY;
-        const float x1 = (bits >> (e + 1)) & 1u ? __uint_as_float(v[e + 1]) : -INFINITY;
-        const float x2 = (bits >> (e + 2)) & 1u ? __uint_as_float(v[e + 2]) : -INFINITY;
-        const float x3 = (bits >> (e + 3)) & 1u ? __uint_as_float(v[e + 3]) : -INFINITY;
-        m0 = fmax3(m0, x0, x1);
-        m1 = fmax3(m1, x2, x3);
+        for (int e = 0; e < 32; e += 4) {
+          const float x0 = (bits >> e) & 1u ? __uint_as_float(v[e]) : -INFINITY;
+          const float x1 = (bits >> (e + 1)) & 1u ? __uint_as_float(v[e + 1]) : -INFINITY;
+          const float x2 = (bits >> (e + 2)) & 1u ? __uint_as_float(v[e + 2]) : -INFINITY;
+          const float x3 = (bits >> (e + 3)) & 1u ? __uint_as_float(v[e + 3]) : -INFINITY;
+          m0 = fmax3(m0, x0, x1);
+          m1 = fmax3(m1, x2, x3);
+        }
+        mx = fmaxf(m0, m1);
       }
-      mx = fmaxf(m0, m1);
+    } else {
+#pragma unroll 1
+      for (int ch = 0; ch < NCH; ++ch) mx = fmaxf(mx, tmem_max32(trow + ch * 32));
     }
     const float ms = (mx == -INFINITY) ? 0.f : mx * P.scale_log2;
     const uint64_t sl2 = f2_pack(P.scale_log2, P.scale_log2);
@@ -606,6 +621,10 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
     }
     const float2 a01 = f2_unpack(acc2[0]), a23 = f2_unpack(acc2[1]);
     const float l = (a01.x + a01.y) + (a23.x + a23.y);
+    // l is at least the row's largest attended p, 2^-(reference - attended
+    // maximum) (every valid row attends its own key): l < 2^-60 means that
+    // gap is above 60
+    const bool exact = row_valid && l < 0x1p-60f;
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -650,6 +669,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
     // stage is handed back once the last half is read.
     const uint64_t mul2 = f2_pack(mul, mul);
     __nv_bfloat16* op = P.out + orow * D;
+    const bool stores = row_valid && !exact;  // an exact row is written by exact_row
 #pragma unroll 1
     for (int hf = 0; hf < D / 64; ++hf) {
       uint32_t o[2][32];
@@ -663,7 +683,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + 8 * (kTempty + wg));
       }
-      if (row_valid && !P.accumulate) {
+      if (stores && !P.accumulate) {
         // Each thread writes its own row, whole 32-byte sectors per store.
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
@@ -681,7 +701,7 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
             st_global_v8(op + hf * 64 + ch * 32 + half * 16, pk);
           }
         }
-      } else if (row_valid) {
+      } else if (stores) {
         // Second pass of the gated sum: each thread reads its own row, adds in
         // fp32 and writes it back.
 #pragma unroll
@@ -714,6 +734,10 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
         }
       }
     }
+    if (exact)
+      exact_row<D>(ExactRow{P.q, P.k, P.v, P.identity ? nullptr : P.perm + size_t(tw.b) * P.n,
+                            P.gate, P.out, orow, size_t(tw.b) * P.n, P.n, P.Hkv, tw.kvh, tw.p0 + t,
+                            sig_p, P.left, P.right, P.causal, P.accumulate, P.scale_log2});
   }
   if (issued) {  // an abort can leave this thread's last O MMA in flight
     umma_commit(bars + 8 * (kDrainWg + wg));

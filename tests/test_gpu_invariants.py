@@ -94,11 +94,13 @@ def test_tensor_core_and_simt_kernels_agree():
     inp = Inputs(1, n, 32, 8, 128, seed=17, gates=True)
     perm, perm_d = perms(17, 0, 1, n)
     for w in (32, 64, 128):
-        # ring and gather run the same MMAs and the same softmax code
+        # ring and gather run the same MMAs; their softmax references differ
+        # (span maximum against attended maximum), which changes only how p
+        # rounds to bf16
         a = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_TCGEN05_RING)
         b = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
                           kernel=sa.KERNEL_TCGEN05_GATHER)
-        assert torch.equal(a, b)
+        assert (a.float() - b.float()).abs().max().item() <= 2e-2
     for w in (32, 128):
         # the chunk kernel streams the same windows in chunks (online softmax)
         a = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_TCGEN05_RING)

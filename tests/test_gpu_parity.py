@@ -167,12 +167,15 @@ def test_long_prefill_gqa_causal_sa(long_prefill, w):
                        kernel=sa.KERNEL_TCGEN05_CHUNK, err=err)
     assert sa.check_error(err) == sa.SA_OK
     compare(gather_rows(yf, rows), want, f"c3 chunk w={w}")
-    # the gather kernel computes the same MMAs and softmax: identical bits
+    # the gather kernel computes the same MMAs; its softmax reference is the
+    # attended maximum where the ring's is the span maximum, so the two agree
+    # to rounding
     yg = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True,
                        kernel=sa.KERNEL_TCGEN05_GATHER, err=err)
     assert sa.check_error(err) == sa.SA_OK
+    compare(gather_rows(yg, rows), want, f"c3 gather w={w}")
     if w <= 128:
-        assert torch.equal(yg, y)
+        assert (yg.float() - y.float()).abs().max().item() <= 2e-2
     # the CUDA-core kernel agrees on the same rows
     y2 = sa.sa_forward(inp.q, inp.k, inp.v, perm_d, w, causal=True, kernel=sa.KERNEL_SIMT, err=err)
     assert sa.check_error(err) == sa.SA_OK
@@ -244,3 +247,59 @@ def test_chunk_kernel_rescales_when_scores_grow_across_chunks(causal):
     ys = sa.sa_forward(dev(q), dev(k), dev(v), perm_d, w, causal=causal, kernel=sa.KERNEL_SIMT,
                        err=err)
     assert (y.float() - ys.float()).abs().max().item() <= 2e-2
+
+
+def _spiked_case(b, n, hq, hkv, d, seed):
+    """Queries with a common large component and, on every 37th token, a key
+    whose score is ~90 above the others (~130 in base 2): wherever such a key
+    lies in a tile's span without being attended (masked by sigma, or outside
+    the row's own band), the span's maximum lies far above the row's attended
+    maximum."""
+    from sa_synth import round_bf16
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((b, n, hq, d)).astype(np.float32) * 0.3
+    q[..., 0] = 8.0
+    k = rng.standard_normal((b, n, hkv, d)).astype(np.float32) * 0.3
+    k[..., 0] = 0.0
+    k[:, 5::37, :, 0] = 128.0
+    # small V: rows attending a spike return nearly its V row (no averaging),
+    # and the gated sum rounds twice to bf16, so values stay below 2
+    v = rng.standard_normal((b, n, hkv, d)).astype(np.float32) * 0.25
+    ga = rng.standard_normal((b, n, hq)).astype(np.float32)
+    gw = rng.standard_normal((b, n, hq)).astype(np.float32)
+    return round_bf16(q), round_bf16(k), round_bf16(v), ga, gw
+
+
+@pytest.mark.parametrize("kernel,w", [(sa.KERNEL_TCGEN05_RING, 128), (sa.KERNEL_TCGEN05_CHUNK, 128),
+                                      (sa.KERNEL_TCGEN05_CHUNK, 384)], ids=["ring128", "chunk128",
+                                                                            "chunk384"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_exact_rows_when_unattended_keys_dominate(kernel, w, causal):
+    """The ring and chunk kernels take their softmax reference from every key
+    column they hold, attended or not.  Rows whose attended scores lie more
+    than 2^60 below it are recomputed exactly by their thread; with spiked
+    keys many rows take that path (sigma-masked spikes, spikes of a
+    neighbour's band), and every row must match the fp64 oracle, on the SA
+    path and on the gated path (whose SA pass accumulates onto the SWA
+    pass)."""
+    b, n, hq, hkv, d = 2, 700, 8, 2, 128
+    q, k, v, ga, gw = _spiked_case(b, n, hq, hkv, d, seed=11)
+    perm, perm_d = perms(3, 0, b, n)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+    q64, k64, v64 = q.astype(np.float64), k.astype(np.float64), v.astype(np.float64)
+    err = _err()
+    y = sa.sa_forward(dev(q), dev(k), dev(v), perm_d, w, causal=causal, kernel=kernel, err=err)
+    assert sa.check_error(err) == sa.SA_OK
+    assert kernel_ran(kernel)
+    want = oracle.sa_rows(q64, k64, v64, perm, w, causal).reshape(b, n, hq, d)
+    compare(y, want, f"spiked sa kernel={kernel} w={w} causal={causal}")
+    if causal:
+        gad = torch.from_numpy(ga).cuda()
+        gwd = torch.from_numpy(gw).cuda()
+        yg = sa.sa_swa_gated_forward(dev(q), dev(k), dev(v), perm_d, gad, gwd, w, causal=True,
+                                     kernel=kernel, err=err)
+        assert sa.check_error(err) == sa.SA_OK
+        assert kernel_ran(kernel)
+        wantg = oracle.gated_rows(q64, k64, v64, perm, ga.astype(np.float64),
+                                  gw.astype(np.float64), w, None, True).reshape(b, n, hq, d)
+        compare(yg, wantg, f"spiked gated kernel={kernel} w={w}")
