@@ -70,7 +70,8 @@ enum {
   SA_KERNEL_SIMT = 1,    /* CUDA-core kernel: any window, the correctness baseline */
   SA_KERNEL_TCGEN05 = 2, /* the better-fitting tcgen05 kernel; SA_ERR_UNSUPPORTED if none fits */
   SA_KERNEL_TCGEN05_GATHER = 3, /* tcgen05 kernel that gathers every window with TMA */
-  SA_KERNEL_TCGEN05_RING = 4,   /* tcgen05 kernel with a sliding K/V ring (spans <= 160 keys) */
+  SA_KERNEL_TCGEN05_RING = 4,   /* tcgen05 kernel with a sliding K/V ring (spans <= 256 keys
+                                   whose rings fit shared memory) */
   SA_KERNEL_TCGEN05_CHUNK = 5   /* tcgen05 kernel streaming the span in 128-key chunks with an
                                    online softmax (any window) */
 };
