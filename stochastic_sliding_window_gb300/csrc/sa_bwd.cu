@@ -15,10 +15,12 @@
 // kernels: a tile is Bt = 128/g consecutive permuted positions of one
 // (sequence, kv head) pair stacked with the g query heads (128 MMA rows).
 //
-// Two kernels, both one 128-thread CTA per SM walking tiles, each thread
-// owning one TMEM lane (one MMA row):
+// Two kernels, both one 256-thread CTA per SM walking tiles; the two warps
+// of a TMEM lane quarter share its 32 rows (one MMA row per lane) and split
+// each row's 32-column pieces:
 //   sa_bwd_dq_kernel   query tiles: gathers the tile's Q and dY rows and the
-//                      K and V rows of its key span into shared memory;
+//                      K and V rows of its key span into shared memory (the
+//                      next tile's rows while this one is computed);
 //                      S = Q K^T and dP = dY V^T into TMEM; per row the
 //                      log-sum-exp and D from its whole window, then
 //                      dS (bf16) over S; dQ = dS K; dQ rows scattered to
@@ -213,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
   const uint32_t bars = sbase + P.off_bar;
   volatile int* abort_flag;
   const uint32_t tmem_base = cta_setup(P, smem, bars, abort_flag);
-  int32_t* sig = reinterpret_cast<int32_t*>(smem + P.off_sig);  // span column -> token (-1: none)
+  // span column -> token (-1: none), two buffers: this tile's and the next one's
+  int32_t* sigbuf = reinterpret_cast<int32_t*>(smem + P.off_sig);
   float* red = reinterpret_cast<float*>(smem + P.off_col);       // [3][2][128] row partials
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, part = warp >> 2;
@@ -224,36 +227,70 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
                  sv = sbase + P.off_v;
   const int sp = P.span_pad;
   uint32_t mma_phase = 0;
-  for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x) {
-    const int seq = tile / P.tiles_per_seq;
-    const int p0 = (tile - seq * P.tiles_per_seq) * P.Bt;
-    const int b = seq / P.Hkv, kvh = seq - (seq / P.Hkv) * P.Hkv;
-    const size_t tokb = size_t(b) * P.n;
+  struct TileAt {
+    int p0, kvh;
+    size_t tokb, qh;
+  };
+  auto tile_at = [&](int tile_) {
+    const int seq = tile_ / P.tiles_per_seq;
+    const int b = seq / P.Hkv;
+    TileAt c;
+    c.p0 = (tile_ - seq * P.tiles_per_seq) * P.Bt;
+    c.kvh = seq - b * P.Hkv;
+    c.tokb = size_t(b) * P.n;
+    c.qh = size_t(c.kvh) * P.g;
+    return c;
+  };
+  // the tile's span tokens into sg (the caller synchronises before use)
+  auto fill_sig = [&](const TileAt& c, int32_t* sg) {
     for (int i = tid; i < sp; i += kThreads) {
-      const int pos = p0 - P.left + i;
+      const int pos = c.p0 - P.left + i;
       int tok = -1;
       if (pos >= 0 && pos < P.n) {
-        tok = P.perm ? __ldg(P.perm + tokb + pos) : pos;
+        tok = P.perm ? __ldg(P.perm + c.tokb + pos) : pos;
         if (unsigned(tok) >= unsigned(P.n)) {
           atomicOr(P.err, SA_ERRBIT_RANGE);
           tok = -1;
         }
       }
-      sig[i] = tok;
+      sg[i] = tok;
     }
-    __syncthreads();
-    // Q and dY rows of the tile (r = t*g + j), K and V rows of the span;
-    // rows past the sequence end read token 0 and are never written.
-    const size_t qh = size_t(kvh) * P.g;
+  };
+  // Q and dY rows of the tile (r = t*g + j), K or V rows of the span; rows
+  // past the sequence end read token 0 and are never written.
+  auto gather_qdy = [&](const TileAt& c, const int32_t* sg) {
     auto qrow = [&](int rr) {
-      const int tk = max(sig[P.left + (rr >> P.log2g)], 0);
-      return ((tokb + tk) * P.Hq + qh + (rr & (P.g - 1))) * D;
+      const int tk = max(sg[P.left + (rr >> P.log2g)], 0);
+      return ((c.tokb + tk) * P.Hq + c.qh + (rr & (P.g - 1))) * D;
     };
-    auto krow = [&](int s_) { return ((tokb + max(sig[s_], 0)) * P.Hkv + kvh) * D; };
     gather_rows<D>(sq, kBM * 128, kBM, P.q, qrow);
     gather_rows<D>(sdy, kBM * 128, kBM, P.dy, qrow);
-    gather_rows<D>(sk, sp * 128, sp, P.k, krow);
-    gather_rows<D>(sv, sp * 128, sp, P.v, krow);
+  };
+  auto gather_kv = [&](const TileAt& c, const int32_t* sg, uint32_t dst,
+                       const __nv_bfloat16* src) {
+    auto krow = [&](int s_) { return ((c.tokb + max(sg[s_], 0)) * P.Hkv + c.kvh) * D; };
+    gather_rows<D>(dst, sp * 128, sp, src, krow);
+  };
+  // The operands of the first tile; every later tile's are gathered while
+  // the tile before it is computed: its Q, dY and V rows once that tile's
+  // S and dP MMAs are done, its K rows once that tile's dQ MMA is.
+  int cur = 0;
+  if (int(blockIdx.x) < P.num_tiles) {
+    const TileAt c0 = tile_at(blockIdx.x);
+    fill_sig(c0, sigbuf);
+    __syncthreads();
+    gather_qdy(c0, sigbuf);
+    gather_kv(c0, sigbuf, sk, P.k);
+    gather_kv(c0, sigbuf, sv, P.v);
+  }
+  for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, cur ^= 1) {
+    const TileAt c = tile_at(tile);
+    const int p0 = c.p0;
+    const size_t tokb = c.tokb, qh = c.qh;
+    const int32_t* sig = sigbuf + cur * sp;
+    int32_t* sig_nx = sigbuf + (cur ^ 1) * sp;
+    const int next = tile + int(gridDim.x);
+    const bool has_next = next < P.num_tiles;
     asm volatile("cp.async.wait_all;" ::: "memory");
     fence_proxy_async_smem();
     __syncthreads();
@@ -271,9 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
       }
       umma_commit(bars + 8 * kBarMma);
     }
+    if (has_next) fill_sig(tile_at(next), sig_nx);  // overlaps the MMAs
     if (!cta_wait(bars + 8 * kBarMma, mma_phase, P, abort_flag)) break;
     mma_phase ^= 1;
     tc_fence_after();
+    // Q, dY and V are free: the next tile's rows land during the passes
+    // (cta_wait above also ordered sig_nx's writes before these reads)
+    TileAt cn{};
+    if (has_next) {
+      cn = tile_at(next);
+      gather_qdy(cn, sig_nx);
+      gather_kv(cn, sig_nx, sv, P.v);
+    }
 
     // Per row: window band in span columns, its token, gate.
     const int sig_p = sig[P.left + t];
@@ -401,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
     if (!cta_wait(bars + 8 * kBarMma, mma_phase, P, abort_flag)) break;
     mma_phase ^= 1;
     tc_fence_after();
+    if (has_next) gather_kv(cn, sig_nx, sk, P.k);  // K is free once dQ = dS K is done
     // tcgen05.ld is warp-collective: every lane loads, valid rows store.
 #pragma unroll 1
     for (int ch = part; ch < D / 32; ch += 2) {
@@ -409,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dq_kernel(const __grid_con
       if (row_valid) write_row<D>(P, P.dq, orow, o, ch * 32, P.scale);
     }
     tc_fence_before();
-    __syncthreads();  // TMEM, the span tokens and the operands are reused
+    __syncthreads();  // TMEM and this tile's span tokens are reused
   }
   cta_teardown(P, bars, tmem_base);
 }
