@@ -584,6 +584,39 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
         uint32_t s_[32], dp[32];
         tmem_ld32(trow + c_st + ch * 32, s_);
         tmem_ld32(trow + c_dpt + ch * 32, dp);
+        // The piece's 32 chunk rows that this key attends, as bits: rows of
+        // the tokens whose window covers the key (a contiguous run), of
+        // valid tokens and, when causal, of tokens with sigma(key) <= sigma(q)
+        // (the piece's tokens are the same for every lane: broadcast loads).
+        uint32_t bits = 0u;
+        if (sig_k >= 0) {
+          const int r0 = ch * 32;
+          const int tq_lo = kpos - P.right - c0, tq_hi = kpos + P.left - c0;
+          bits = band_bits(tq_lo * P.g, (tq_hi + 1) * P.g - 1, r0);
+          if (bits != 0u) {
+            const int t0 = r0 >> P.log2g;
+            const int ntok = P.log2g >= 5 ? 1 : (32 >> P.log2g);
+            const uint32_t gm = P.log2g >= 5 ? 0xffffffffu : ((1u << P.g) - 1u);
+            uint32_t tb = 0u;
+            auto tok_ok = [&](int qtk) { return qtk >= 0 && (!kCausal || sig_k <= qtk); };
+            if (ntok >= 4) {  // g <= 8: four tokens per load (t0 is a multiple of 4)
+              const int4* q4 = reinterpret_cast<const int4*>(qt + t0);
+#pragma unroll 1
+              for (int i4 = 0; i4 < (ntok >> 2); ++i4) {
+                const int4 v4 = q4[i4];
+                const int sh = (4 * i4) << P.log2g;
+                if (tok_ok(v4.x)) tb |= gm << sh;
+                if (tok_ok(v4.y)) tb |= gm << (sh + P.g);
+                if (tok_ok(v4.z)) tb |= gm << (sh + 2 * P.g);
+                if (tok_ok(v4.w)) tb |= gm << (sh + 3 * P.g);
+              }
+            } else {
+              for (int i = 0; i < ntok; ++i)
+                if (tok_ok(qt[t0 + i])) tb |= gm << (i << P.log2g);
+            }
+            bits &= tb;
+          }
+        }
         uint32_t pk[16], dk2[16];
         // the rows' lse2' and D four at a time (the same for every lane:
         // broadcast loads)
@@ -597,12 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_bwd_dkv_kernel(const __grid_co
           float pv[4], dv[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int rr = rb + u;
-            const int tq = rr >> P.log2g;
-            const int qpos = c0 + tq;
-            const int qtk = qt[tq];
-            bool ok = sig_k >= 0 && qtk >= 0 && kpos >= qpos - P.left && kpos <= qpos + P.right;
-            if (kCausal) ok = ok && sig_k <= qtk;
+            const bool ok = (bits >> (4 * e4 + u)) & 1u;
             const float p = ok ? fast_exp2(fmaf(__uint_as_float(s_[4 * e4 + u]), P.scale_log2,
                                                 -lv[u]))
                                : 0.f;
