@@ -281,9 +281,9 @@ __device__ __forceinline__ uint32_t band_bits(int lo, int hi, int c0) {
 }
 
 // Row sums of p are accumulated in one fixed order by every tcgen05 kernel
-// (so that kernels subtracting the same reference agree bit for bit): pair e2 of a 32-column chunk adds
-// p[2 e2] to acc[2 (e2 & 1)] and p[2 e2 + 1] to acc[2 (e2 & 1) + 1]; the row
-// sum is (acc[0] + acc[1]) + (acc[2] + acc[3]).
+// (so that kernels subtracting the same reference agree bit for bit): pair
+// e2 of a 32-column chunk adds p[2 e2] to acc[2 (e2 & 1)] and p[2 e2 + 1] to
+// acc[2 (e2 & 1) + 1]; the row sum is (acc[0] + acc[1]) + (acc[2] + acc[3]).
 
 // Per-row state of one tile, shared by the softmax variants.
 struct RowCtx {
