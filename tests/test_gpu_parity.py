@@ -251,7 +251,8 @@ def test_chunk_kernel_rescales_when_scores_grow_across_chunks(causal):
 
 def _spiked_case(b, n, hq, hkv, d, seed):
     """Queries with a common large component and, on every 37th token, a key
-    whose score is ~90 above the others (~130 in base 2): wherever such a key
+    whose score is 1024/sqrt(d) above the others (~90 at d = 128, ~130 in base
+    2; ~128 at d = 64): wherever such a key
     lies in a tile's span without being attended (masked by sigma, or outside
     the row's own band), the span's maximum lies far above the row's attended
     maximum."""
@@ -270,11 +271,19 @@ def _spiked_case(b, n, hq, hkv, d, seed):
     return round_bf16(q), round_bf16(k), round_bf16(v), ga, gw
 
 
-@pytest.mark.parametrize("kernel,w", [(sa.KERNEL_TCGEN05_RING, 128), (sa.KERNEL_TCGEN05_CHUNK, 128),
-                                      (sa.KERNEL_TCGEN05_CHUNK, 384)], ids=["ring128", "chunk128",
-                                                                            "chunk384"])
+SPIKED = [  # kernel, w, hq, hkv, d
+    (sa.KERNEL_TCGEN05_RING, 128, 8, 2, 128),
+    (sa.KERNEL_TCGEN05_CHUNK, 128, 8, 2, 128),
+    (sa.KERNEL_TCGEN05_CHUNK, 384, 8, 2, 128),
+    (sa.KERNEL_TCGEN05_RING, 128, 4, 4, 64),   # MHA d=64: a 256-key span, eight chunks
+    (sa.KERNEL_TCGEN05_CHUNK, 256, 4, 4, 64),
+]
+
+
+@pytest.mark.parametrize("kernel,w,hq,hkv,d", SPIKED,
+                         ids=["ring128", "chunk128", "chunk384", "ring128_d64", "chunk256_d64"])
 @pytest.mark.parametrize("causal", [True, False])
-def test_exact_rows_when_unattended_keys_dominate(kernel, w, causal):
+def test_exact_rows_when_unattended_keys_dominate(kernel, w, hq, hkv, d, causal):
     """The ring and chunk kernels take their softmax reference from every key
     column they hold, attended or not.  Rows whose attended scores lie more
     than 2^60 below it are recomputed exactly by their thread; with spiked
@@ -282,7 +291,7 @@ def test_exact_rows_when_unattended_keys_dominate(kernel, w, causal):
     neighbour's band), and every row must match the fp64 oracle, on the SA
     path and on the gated path (whose SA pass accumulates onto the SWA
     pass)."""
-    b, n, hq, hkv, d = 2, 700, 8, 2, 128
+    b, n = 2, 700
     q, k, v, ga, gw = _spiked_case(b, n, hq, hkv, d, seed=11)
     perm, perm_d = perms(3, 0, b, n)
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
