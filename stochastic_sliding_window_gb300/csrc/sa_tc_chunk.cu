@@ -10,12 +10,13 @@
 // [p0 - left, p0 + 2*Bt - 1 + right].  The span is cut into chunks of 128
 // keys, each loaded once for both halves.  Per chunk and half, S = Q K^T lands
 // in the half's TMEM buffer; the half's softmax warpgroup masks it (window
-// band and, when causal, sigma[q] <= sigma[p]), keeps a running maximum and
-// sum per row and writes bf16 P over S; O += P V accumulates in the half's
-// TMEM accumulator.  A row's reference maximum is raised -- and O and the
-// sum rescaled by 2^(old - new) -- only when a chunk's maximum exceeds it by
-// more than 2^8, so most chunks need no correction of O.  Shared memory does
-// not grow with the window: any window fits.
+// band and, when causal, sigma[q] <= sigma[p]), keeps a running reference
+// maximum (from the chunks' maxima over every key column, returned by the
+// TMEM loads) and sum per row and writes bf16 P over S; O += P V accumulates
+// in the half's TMEM accumulator.  A row's reference maximum is raised -- and
+// O and the sum rescaled by 2^(old - new) -- only when a chunk's maximum
+// exceeds it by more than 2^8, so most chunks need no correction of O.  Shared
+// memory does not grow with the window: any window fits.
 //
 // Roles (four warpgroups, 512 threads):
 //   warps 0-6  producers: cp.async of the 256 Q rows of a tile and of the 128

@@ -37,14 +37,15 @@
 //   warps 8-11  softmax, O MMA and epilogue of even tiles (TMEM stage 0)
 //   warps 12-15 softmax, O MMA and epilogue of odd tiles  (TMEM stage 1)
 // Per tile: S = Q K^T (one or two MMAs when the span wraps the ring) into
-// TMEM; each row's window is read from TMEM in 32-column chunks in two
-// passes (the attended maximum, then exponentials) and P is written back to
-// TMEM as bf16 over its own S columns; one thread of the warpgroup then
-// issues O = P V with P taken from TMEM and V used MN-major straight from
-// the ring (so no other warp has to notice that P is ready); the epilogue
-// scales by 1/rowsum, optionally applies the gate and the previous out row,
-// and scatters row sigma[p0+t].  Mask words and copies are thus off the
-// softmax warps' path, which is the longest per tile.
+// TMEM; each row's window is read from TMEM in 32-column chunks in two passes
+// (a reference maximum -- from three chunks on the maximum over every span
+// column, returned by the TMEM loads -- then exponentials) and P is written
+// back to TMEM as bf16 over its own S columns; one thread of the warpgroup
+// then issues O = P V with P taken from TMEM and V used MN-major straight
+// from the ring (so no other warp has to notice that P is ready); the
+// epilogue scales by 1/rowsum, optionally applies the gate and the previous
+// out row, and scatters row sigma[p0+t].  Mask words and copies are thus off
+// the softmax warps' path, which is the longest per tile.
 // Every wait is bounded (SA_ERRBIT_TIMEOUT); the copiers wait for their last
 // copies to land, and each O issuer for its last MMA, before exit.
 #include "sa_internal.h"
