@@ -139,3 +139,30 @@ def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
     assert cb["unit"] == "tokens/s" and cb["sample"]
     assert line["e2e"] == dict(value=line["value"], unit="tokens/s", h2d_bytes_per_step=0,
                                d2h_bytes_per_step=0)
+
+
+def test_profiled_traffic_follows_the_kernel_source_hash(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu record only while the
+    kernel sources hash to the value recorded with it; otherwise it is null."""
+    rec = {"traffic_bytes_per_launch": 643352832,
+           "kernel_source_sha256": bench.kernel_source_sha256()}
+    p = tmp_path / "rec.json"
+    p.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "PROFILE", str(p))
+    assert bench.profiled_traffic() == 643352832
+    rec["kernel_source_sha256"] = "0" * 64
+    p.write_text(json.dumps(rec))
+    assert bench.profiled_traffic() is None
+    monkeypatch.setattr(bench, "PROFILE", str(tmp_path / "missing.json"))
+    assert bench.profiled_traffic() is None
+
+
+def test_committed_traffic_record_is_plausible():
+    """The committed record names the headline kernel and a DRAM byte count
+    within 10% of the algorithmic bytes (no operand re-read)."""
+    with open(bench.PROFILE) as f:
+        rec = json.load(f)
+    assert rec["kernel"].startswith("sa::ring::sa_ring_kernel<128")
+    alg = 671219712
+    assert 0.9 * alg <= rec["traffic_bytes_per_launch"] <= 1.1 * alg
+    assert rec["traffic_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
