@@ -632,12 +632,19 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
     if (lane == 0) mbar_arrive(bars + 8 * (kPfull + wg));
     // Once P of all 128 rows is in TMEM and the tile's V rows have landed,
     // one thread of the warpgroup issues O = P V (A = P from this stage, B =
-    // V straight from the ring, MN-major).  Its waits are bounded like every
-    // other wait.
+    // V straight from the ring, MN-major).  The span's older V rows came with
+    // earlier tiles, whose copies complete on their own barriers in any
+    // order: waiting for the previous tile's O MMA (which waited for its own
+    // rows and, in turn, for the O MMA before it) covers them all.  The other
+    // warpgroup issues that MMA, and this thread issued the one two tiles
+    // back, so the phase waited for is never two behind or ahead.  Every
+    // wait is bounded like every other wait.
     if (issuer &&
         bounded_wait(bars + 8 * (kPfull + wg), ph, P.timeout_cycles, P.err, abort_flag) &&
         bounded_wait(bars + 8 * (kFullV + it % kVDepth), (it / kVDepth) & 1, P.timeout_cycles,
-                     P.err, abort_flag)) {
+                     P.err, abort_flag) &&
+        (it == 0 || bounded_wait(bars + 8 * (kPVdone + (it - 1) % kVDepth),
+                                 ((it - 1) / kVDepth) & 1, P.timeout_cycles, P.err, abort_flag))) {
       tc_fence_after();
       const uint32_t stage = tmem_base + uint32_t(wg * P.cols_stage);
       const uint32_t idesc_pv = idesc_bf16(kBM, D, 1);
