@@ -81,7 +81,8 @@ struct Params {
 // half families by the half (softmax warpgroup) h.
 enum : uint32_t {
   kQfull = 0,    // [stage] Q rows and tokens of tile x landed (cp.async)
-  kQfree = 2,    // [stage] both halves' last S MMA of tile x done: the stage is free
+  kQfree = 2,    // [stage] both halves' last S MMA of tile x done and every softmax warp
+                 // has read the tile's tokens: the stage is free
   kCfull = 4,    // [2] K, V rows and key tokens of chunk c_all landed
   kCfree = 6,    // [2] both halves' O MMA of chunk c_all done: its stage is free
   kSfull = 8,    // [h] S of the half's current chunk in its TMEM buffer
@@ -401,6 +402,10 @@ __device__ void softmax_role(const Params& P, uint8_t* smem, uint32_t sbase, uin
     __syncwarp();  // the previous tile's reads of wsig are done
     if (lane < tpw) wsig[lane] = wtok;
     __syncwarp();
+    // The Q stage's tokens are read: with one chunk per tile the tile's only
+    // S MMAs can be done before this warp gets here, so the stage is refilled
+    // only once every softmax warp has also arrived.
+    if (lane == 0) mbar_arrive(bars + 8 * (kQfree + qs));
     bool row_valid = tl.p0 + t < P.n;
     if (row_valid && unsigned(sig_p) >= unsigned(P.n)) {
       atomicOr(P.err, SA_ERRBIT_RANGE);
@@ -644,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) sa_chunk_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bars + 8 * (kQfull + s), kProducers);
-      mbar_init(bars + 8 * (kQfree + s), 2);  // one commit per half
+      mbar_init(bars + 8 * (kQfree + s), 2 + 8);  // one commit per half, one per softmax warp
       mbar_init(bars + 8 * (kCfull + s), kProducers);
       mbar_init(bars + 8 * (kCfree + s), 2);  // one commit per half
       mbar_init(bars + 8 * (kSfull + s), 1);
