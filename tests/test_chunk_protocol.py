@@ -16,41 +16,13 @@ the tile's tokens, so the Q stage must also wait for those reads.
 
 from __future__ import annotations
 
-import random
 from dataclasses import dataclass
 
 import pytest
 
-from test_ring_protocol import Barrier, Buffer, ProtocolError
-
-
-class Accumulator(Buffer):
-    """A TMEM accumulator: a tile's first O MMA replaces it, the tile's later
-    ones add to it (MMAs into one accumulator run in issue order)."""
-
-    def __init__(self, name):
-        super().__init__(name)
-        self.inflight = 0
-
-    def begin_mma(self, who, tag, replace):
-        if replace:
-            if self.readers:
-                raise ProtocolError(f"{who} replaces {self.name} while {sorted(self.readers)} "
-                                    f"read {self.content}")
-            if self.inflight:
-                raise ProtocolError(f"{who} replaces {self.name} under earlier O MMAs")
-        elif self.content != tag:
-            raise ProtocolError(f"{who} adds to {self.name} holding {self.content}, not {tag}")
-        self.content = tag
-        self.inflight += 1
-
-    def end_mma(self):
-        self.inflight -= 1
-
-    def begin_read(self, who, want):
-        if self.inflight:
-            raise ProtocolError(f"{who} reads {self.name} under O MMAs in flight")
-        super().begin_read(who, want)
+from protocol_model import (Accumulator, Barrier, Buffer, ProtocolError, arrive, copy, mma,
+                            simulate, wait)
+from protocol_model import call as do
 
 
 @dataclass
@@ -94,16 +66,17 @@ class ChunkModel:
             qs = x % g.qstages
             if x >= g.qstages:
                 z = x // g.qstages - 1
-                yield ("wait", self.q_free[qs], z & 1, z)
-            yield ("load", [(self.qrows[qs], x), (self.qtok[qs], x)], f"loadQ{x}", self.q_full[qs])
+                yield wait(self.q_free[qs], z & 1, z)
+            yield copy([(self.qrows[qs], x), (self.qtok[qs], x)], f"loadQ{x}", self.q_full[qs],
+                       "arrive")
             for c in range(g.nch):
                 call = x * g.nch + c
                 s = call & 1
                 if call >= 2 and self.mut.producers_wait_chunk_free:
                     z = (call >> 1) - 1
-                    yield ("wait", self.c_free[s], z & 1, z)
-                yield ("load", [(self.kv[s], call), (self.csig[s], call)], f"loadC{call}",
-                       self.c_full[s])
+                    yield wait(self.c_free[s], z & 1, z)
+                yield copy([(self.kv[s], call), (self.csig[s], call)], f"loadC{call}",
+                           self.c_full[s], "arrive")
 
     def mma(self):
         """One thread polls both halves; modelled as one actor per half, which
@@ -115,14 +88,14 @@ class ChunkModel:
             for call in range(total):
                 x, c = divmod(call, g.nch)
                 qs = x % g.qstages
-                yield ("wait", self.c_full[call & 1], (call >> 1) & 1, call >> 1)
+                yield wait(self.c_full[call & 1], (call >> 1) & 1, call >> 1)
                 if self.mut.qk_waits_previous_pv:
-                    yield ("wait", self.pv_done[h], (call & 1) ^ 1, call - 1)
+                    yield wait(self.pv_done[h], (call & 1) ^ 1, call - 1)
                 if c == 0:
                     z = x // g.qstages
-                    yield ("wait", self.q_full[qs], z & 1, z)
+                    yield wait(self.q_full[qs], z & 1, z)
                 commits = [self.s_full[h]] + ([self.q_free[qs]] if c == g.nch - 1 else [])
-                yield ("mma", [(self.qrows[qs], x), (self.kv[call & 1], call)],
+                yield mma([(self.qrows[qs], x), (self.kv[call & 1], call)],
                        [(self.s_buf[h], ("S", call))], f"QK{h}.{call}", commits)
         return half(0), half(1)
 
@@ -132,115 +105,41 @@ class ChunkModel:
         for x in range(g.ntiles):
             qs = x % g.qstages
             z = x // g.qstages
-            yield ("wait", self.q_full[qs], z & 1, z)
-            yield ("call", lambda qs=qs, x=x: (self.qtok[qs].begin_read(who, x),
+            yield wait(self.q_full[qs], z & 1, z)
+            yield do(lambda qs=qs, x=x: (self.qtok[qs].begin_read(who, x),
                                                self.qtok[qs].end_read(who)))
             if self.mut.softmax_releases_q_stage:
-                yield ("arrive", self.q_free[qs], 4)
+                yield arrive(self.q_free[qs], 4)
             for c in range(g.nch):
                 call = x * g.nch + c
                 b = call & 1
-                yield ("wait", self.c_full[b], (call >> 1) & 1, call >> 1)
-                yield ("call", lambda b=b, call=call: (self.csig[b].begin_read(who, call),
+                yield wait(self.c_full[b], (call >> 1) & 1, call >> 1)
+                yield do(lambda b=b, call=call: (self.csig[b].begin_read(who, call),
                                                        self.csig[b].end_read(who)))
-                yield ("wait", self.s_full[h], call & 1, call)
+                yield wait(self.s_full[h], call & 1, call)
                 if c > 0:  # the O correction reads O once the previous O MMA is done
-                    yield ("wait", self.pv_done[h], (call - 1) & 1, call - 1)
+                    yield wait(self.pv_done[h], (call - 1) & 1, call - 1)
 
                 def passes(call=call):
                     self.s_buf[h].begin_read(who, ("S", call))
                     self.s_buf[h].end_read(who)
                     self.s_buf[h].begin_write(who)
                     self.s_buf[h].end_write(("P", call))
-                yield ("call", passes)
-                yield ("arrive", self.p_full[h], 4)
-                yield ("wait", self.p_full[h], call & 1, call)
+                yield do(passes)
+                yield arrive(self.p_full[h], 4)
+                yield wait(self.p_full[h], call & 1, call)
                 commits = [self.pv_done[h], self.c_free[b]] + \
                           ([self.o_full[h]] if c == g.nch - 1 else [])
-                yield ("mma", [(self.s_buf[h], ("P", call)), (self.kv[b], call)],
+                yield mma([(self.s_buf[h], ("P", call)), (self.kv[b], call)],
                        [(self.o_buf[h], ("O", x), c == 0)], f"PV{h}.{call}", commits)
-            yield ("wait", self.o_full[h], x & 1, x)
-            yield ("call", lambda x=x: (self.o_buf[h].begin_read(who + "epi", ("O", x)),
+            yield wait(self.o_full[h], x & 1, x)
+            yield do(lambda x=x: (self.o_buf[h].begin_read(who + "epi", ("O", x)),
                                         self.o_buf[h].end_read(who + "epi")))
 
-    # ------------------------------------------------------------ scheduler
-    def run(self, seed: int, max_steps: int = 200000):
-        rng = random.Random(seed)
+    def run(self, seed: int):
         m0, m1 = self.mma()
-        roles = {"producers": self.producers(), "qk0": m0, "qk1": m1,
-                 "softmax0": self.softmax(0), "softmax1": self.softmax(1)}
-        speed = {n: rng.choice([0.02, 0.2, 1.0, 5.0]) for n in list(roles) + ["copy", "pipe"]}
-        nxt = {n: next(gen) for n, gen in roles.items()}
-        copies, pipe = [], []
-        steps = 0
-
-        def runnable(n):
-            a = nxt[n]
-            return a[0] != "wait" or a[1].passes(a[2])
-
-        while nxt or copies or pipe:
-            steps += 1
-            if steps > max_steps:
-                raise ProtocolError("no progress bound reached")
-            for n, a in nxt.items():
-                if a[0] == "wait" and a[1].k - 1 > a[3]:
-                    raise ProtocolError(f"{n}: {a[1].name} is past the phase {a[3]} it waits for")
-            choices = [("role", n) for n in nxt if runnable(n)]
-            choices += [("copy", i) for i in range(len(copies))]
-            if pipe:
-                choices.append(("pipe", 0))
-            if not choices:
-                raise ProtocolError("deadlock: " + ", ".join(
-                    f"{n} waits {a[1].name}" for n, a in nxt.items()))
-            weights = [speed[n] if k == "role" else speed[k] for k, n in choices]
-            kind, key = rng.choices(choices, weights=weights)[0]
-            if kind == "copy":
-                bufs, who, bar = copies.pop(key)
-                for buf, tag in bufs:
-                    buf.end_write(tag)
-                bar.arrive()
-                continue
-            if kind == "pipe":
-                reads, writes, who, commits = pipe.pop(0)
-                for buf, _ in reads:
-                    buf.end_read(who)
-                for w in writes:
-                    if isinstance(w[0], Accumulator):
-                        w[0].end_mma()
-                    else:
-                        w[0].end_write(w[1])
-                for bar in commits:
-                    bar.arrive()
-                continue
-            a = nxt[key]
-            if a[0] == "wait":
-                if a[1].k - 1 != a[3]:
-                    raise ProtocolError(f"{key}: {a[1].name} released at phase {a[1].k - 1}, "
-                                        f"the wait means phase {a[3]}")
-            elif a[0] == "arrive":
-                for _ in range(a[2]):
-                    a[1].arrive()
-            elif a[0] == "call":
-                a[1]()
-            elif a[0] == "load":
-                for buf, _ in a[1]:
-                    buf.begin_write(a[2])
-                copies.append((a[1], a[2], a[3]))
-            elif a[0] == "mma":
-                reads, writes, who, commits = a[1], a[2], a[3], a[4]
-                for buf, tag in reads:
-                    buf.begin_read(who, tag)
-                for w in writes:
-                    if isinstance(w[0], Accumulator):
-                        w[0].begin_mma(who, w[1], w[2])
-                    else:
-                        w[0].begin_write(who)
-                pipe.append((reads, writes, who, commits))
-            try:
-                nxt[key] = next(roles[key])
-            except StopIteration:
-                del nxt[key]
-        return steps
+        return simulate({"producers": self.producers(), "qk0": m0, "qk1": m1,
+                         "softmax0": self.softmax(0), "softmax1": self.softmax(1)}, seed)
 
 
 GEOMETRIES = {

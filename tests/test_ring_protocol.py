@@ -28,78 +28,15 @@ must each be caught.
 
 from __future__ import annotations
 
-import random
 from dataclasses import dataclass, field
 
 import pytest
 
+from protocol_model import (Buffer, Barrier, ProtocolError, arrive, call, copy, mma, simulate,
+                            wait)
+
 K_QSTAGES = 2  # Q stages
 K_VDEPTH = 3   # V (and K) rows of tile x overwrite those of tile x - 3
-
-
-class ProtocolError(AssertionError):
-    pass
-
-
-class Barrier:
-    """mbarrier: `count` arrivals plus all expected transaction units
-    complete a phase; `k` phases have completed."""
-
-    def __init__(self, name: str, count: int):
-        self.name, self.count = name, count
-        self.pending, self.tx, self.k = count, 0, 0
-
-    def _maybe_complete(self):
-        if self.pending == 0 and self.tx == 0:
-            self.k += 1
-            self.pending = self.count
-
-    def arrive(self, expect_tx: int = 0):
-        if self.pending <= 0:
-            raise ProtocolError(f"{self.name}: arrival beyond the count")
-        self.tx += expect_tx
-        self.pending -= 1
-        self._maybe_complete()
-
-    def complete_tx(self, units: int = 1):
-        self.tx -= units
-        if self.tx < 0:
-            raise ProtocolError(f"{self.name}: transaction bytes before they were expected")
-        self._maybe_complete()
-
-    def passes(self, parity: int) -> bool:
-        return (self.k & 1) != parity
-
-
-class Buffer:
-    def __init__(self, name: str):
-        self.name = name
-        self.content = None
-        self.readers: dict[str, object] = {}
-        self.writer = None
-
-    def begin_write(self, who: str):
-        if self.readers:
-            raise ProtocolError(f"{who} writes {self.name} while {sorted(self.readers)} read "
-                                f"{self.content}")
-        if self.writer is not None:
-            raise ProtocolError(f"{who} writes {self.name} during {self.writer}'s write")
-        self.writer = who
-        self.content = None
-
-    def end_write(self, tag):
-        self.writer = None
-        self.content = tag
-
-    def begin_read(self, who: str, want):
-        if self.writer is not None:
-            raise ProtocolError(f"{who} reads {self.name} during {self.writer}'s write")
-        if self.content != want:
-            raise ProtocolError(f"{who} reads {self.name}: holds {self.content}, wants {want}")
-        self.readers[who] = want
-
-    def end_read(self, who: str):
-        del self.readers[who]
 
 
 @dataclass
@@ -173,32 +110,6 @@ class Mutation:
 
 
 @dataclass
-class Action:
-    kind: str
-    args: tuple = ()
-
-
-def wait(bar, parity, meant):  # `meant`: the phase index the wait is for (-1: none yet)
-    return Action("wait", (bar, parity, meant))
-
-
-def arrive(bar, n=1, tx=0):
-    return Action("arrive", (bar, n, tx))
-
-
-def call(fn):
-    return Action("call", (fn,))
-
-
-def tma(buffers_tags, who, bar):
-    return Action("tma", (buffers_tags, who, bar))
-
-
-def mma(reads, writes, who, commits):
-    return Action("mma", (reads, writes, who, commits))
-
-
-@dataclass
 class Model:
     geo: Geometry
     mut: Mutation = field(default_factory=Mutation)
@@ -261,11 +172,11 @@ class Model:
                     self.sg[slot].begin_read(f"copierQ{it}", tag)
                     self.sg[slot].end_read(f"copierQ{it}")
             yield call(read_rows)
-            yield tma([(self.q[s], it)], f"tmaQ{it}", self.full_qk[s])
-            yield tma([(self.kr[x], (t.run, p)) for x, p in zip(t.ld_slots, t.ld_pos)],
-                      f"tmaK{it}", self.full_qk[s])
-            yield tma([(self.vr[x], (t.run, p)) for x, p in zip(t.ld_slots, t.ld_pos)],
-                      f"tmaV{it}", self.full_v[it % K_VDEPTH])
+            yield copy([(self.q[s], it)], f"tmaQ{it}", self.full_qk[s], "tx")
+            yield copy([(self.kr[x], (t.run, p)) for x, p in zip(t.ld_slots, t.ld_pos)],
+                       f"tmaK{it}", self.full_qk[s], "tx")
+            yield copy([(self.vr[x], (t.run, p)) for x, p in zip(t.ld_slots, t.ld_pos)],
+                       f"tmaV{it}", self.full_v[it % K_VDEPTH], "tx")
         n = len(self.tiles)
         for x in range(max(0, n - K_QSTAGES), n):  # the last copies land before exit
             yield wait(self.full_qk[x % K_QSTAGES], (x // K_QSTAGES) & 1, x // K_QSTAGES)
@@ -360,95 +271,10 @@ class Model:
             yield call(read_o)
             yield arrive(self.t_empty[wg], n=4)
 
-    # ------------------------------------------------------------ scheduler
-    def run(self, seed: int, max_steps: int = 200000):
-        rng = random.Random(seed)
-        roles = {"copier": self.copier(), "masker": self.masker(), "mma": self.mma_warp(),
-                 "wg0": self.softmax(0), "wg1": self.softmax(1)}
-        nxt = {name: next(gen) for name, gen in roles.items()}
-        tma_inflight = []   # (buffers_tags, who, bar): land in any order
-        pipe = []           # MMAs in issue order: (reads, writes, who, commits)
-        steps = 0
-
-        def advance(name):
-            try:
-                nxt[name] = next(roles[name])
-            except StopIteration:
-                del nxt[name]
-
-        def runnable(name):
-            a = nxt[name]
-            if a.kind != "wait":
-                return True
-            bar, parity, meant = a.args
-            return bar.passes(parity)
-
-        # each actor runs at its own random speed, so that runs where one role
-        # lags far behind the others (the adversarial cases) come up often
-        speed = {name: rng.choice([0.02, 0.2, 1.0, 5.0]) for name in list(roles) + ["tma", "pipe"]}
-
-        while nxt or tma_inflight or pipe:
-            steps += 1
-            if steps > max_steps:
-                raise ProtocolError("no progress bound reached")
-            # a wait overrun by a later phase can never mean what it waits for
-            for name, a in nxt.items():
-                if a.kind == "wait":
-                    bar, parity, meant = a.args
-                    if bar.k - 1 > meant:
-                        raise ProtocolError(f"{name}: {bar.name} is {bar.k - 1 - meant} phases "
-                                            f"past the phase {meant} it waits for")
-            choices = [("role", n) for n in nxt if runnable(n)]
-            choices += [("tma", i) for i in range(len(tma_inflight))]
-            if pipe:
-                choices.append(("pipe", 0))
-            if not choices:
-                raise ProtocolError("deadlock: " + ", ".join(
-                    f"{n} waits {a.args[0].name} parity {a.args[1]}" for n, a in nxt.items()))
-            weights = [speed[n] if k == "role" else speed[k] for k, n in choices]
-            kind, key = rng.choices(choices, weights=weights)[0]
-            if kind == "tma":
-                bufs, who, bar = tma_inflight.pop(key)
-                for buf, tag in bufs:
-                    buf.end_write(tag)
-                bar.complete_tx(1)
-                continue
-            if kind == "pipe":
-                reads, writes, who, commits = pipe.pop(0)
-                for buf, _ in reads:
-                    buf.end_read(who)
-                for buf, tag in writes:
-                    buf.end_write(tag)
-                for bar in commits:
-                    bar.arrive()
-                continue
-            a = nxt[key]
-            if a.kind == "wait":
-                bar, parity, meant = a.args
-                if bar.k - 1 != meant:
-                    raise ProtocolError(f"{key}: {bar.name} released at phase {bar.k - 1}, "
-                                        f"the wait means phase {meant}")
-            elif a.kind == "arrive":
-                bar, n, tx = a.args
-                bar.arrive(expect_tx=tx)
-                for _ in range(n - 1):
-                    bar.arrive()
-            elif a.kind == "call":
-                a.args[0]()
-            elif a.kind == "tma":
-                bufs, who, bar = a.args
-                for buf, _ in bufs:
-                    buf.begin_write(who)
-                tma_inflight.append(a.args)
-            elif a.kind == "mma":
-                reads, writes, who, commits = a.args
-                for buf, tag in reads:
-                    buf.begin_read(who, tag)
-                for buf, _ in writes:
-                    buf.begin_write(who)
-                pipe.append(a.args)
-            advance(key)
-        return steps
+    def run(self, seed: int):
+        return simulate({"copier": self.copier(), "masker": self.masker(),
+                         "mma": self.mma_warp(), "wg0": self.softmax(0),
+                         "wg1": self.softmax(1)}, seed)
 
 
 GEOMETRIES = {
