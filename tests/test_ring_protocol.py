@@ -12,7 +12,9 @@ under many random interleavings.  The model has
     its barrier once the MMAs issued before it are done;
   - the buffers the roles hand to one another: the Q stages, the K, V and
     sigma ring slots, the mask-word buffers and each TMEM stage (its S/P
-    columns and the columns O shares with S).
+    columns and the columns O shares with S), per TMEM lane quarter;
+  - each softmax warp as its own actor (the warps of a warpgroup meet only
+    at the kernel's barriers), warp 0's first lane issuing the O MMAs.
 The roles issue the kernel's waits and arrivals in the kernel's order
 (copy_role, mask_role, mma_role, softmax_role).  Each run checks that
   - no role is left waiting forever;
@@ -133,9 +135,13 @@ class Model:
         self.kr = [Buffer(f"K[{x}]") for x in range(g.ring)]
         self.vr = [Buffer(f"V[{x}]") for x in range(g.ring)]
         self.sg = [Buffer(f"sigma[{x}]") for x in range(g.ring)]
-        self.words = [Buffer(f"words{b}") for b in range(self.mut.word_buffers)]
-        self.tp = [Buffer(f"TMEM{w}.S/P") for w in range(2)]   # S and P columns
-        self.to = [Buffer(f"TMEM{w}.O") for w in range(2)]     # O columns (S spills into them)
+        # per TMEM lane quarter (warp q of a warpgroup reads and writes only its
+        # quarter): the words of its rows, its S/P columns and its O columns
+        # (S spills into the O columns)
+        self.words = [[Buffer(f"words{b}.{q}") for q in range(4)]
+                      for b in range(self.mut.word_buffers)]
+        self.tp = [[Buffer(f"TMEM{w}.{q}.S/P") for q in range(4)] for w in range(2)]
+        self.to = [[Buffer(f"TMEM{w}.{q}.O") for q in range(4)] for w in range(2)]
 
     def word_buf(self, it):
         if self.mut.word_buffers == 4:
@@ -194,11 +200,13 @@ class Model:
             def start(t=t, who=who, wb=wb):
                 for slot, tag in g.span_slots(t):
                     self.sg[slot].begin_read(who, tag)
-                wb.begin_write(who)
+                for quarter in wb:
+                    quarter.begin_write(who)
             yield call(start)
 
             def finish(t=t, it=it, who=who, wb=wb):
-                wb.end_write(it)
+                for quarter in wb:
+                    quarter.end_write(it)
                 for slot, _ in g.span_slots(t):
                     self.sg[slot].end_read(who)
             yield call(finish)
@@ -215,18 +223,20 @@ class Model:
             if m.mma_waits_readout:
                 yield wait(self.t_empty[st], ((it >> 1) & 1) ^ 1, (it >> 1) - 1)
             reads = [(self.q[s], it)] + [(self.kr[x], tag) for x, tag in g.span_slots(t)]
-            writes = [(self.tp[st], ("S", it)), (self.to[st], ("S", it))]
+            writes = [(b, ("S", it)) for b in self.tp[st] + self.to[st]]
             yield mma(reads, writes, f"QK{it}", [self.s_full[st], self.qk_done[s]])
 
-    def softmax(self, wg: int):
+    def softmax_warp(self, wg: int, q: int):
+        """Warp q of softmax warpgroup wg; warp 0's first lane issues the
+        warpgroup's O MMAs (its other lanes wait for it)."""
         g = self.geo
         for it, t in enumerate(self.tiles):
             if (it & 1) != wg:
                 continue
             ph, meant = (it >> 1) & 1, it >> 1
-            who = f"softmax{it}"
+            who = f"softmax{it}.{q}"
             yield wait(self.s_ready[wg], ph, meant)
-            wb = self.word_buf(it)
+            wb = self.word_buf(it)[q]
 
             def read_words(t=t, who=who, wb=wb, it=it):
                 wb.begin_read(who, it)
@@ -239,42 +249,39 @@ class Model:
                 for slot, _ in g.row_slots(t):
                     self.sg[slot].end_read(who)
             yield call(words_done)
-            yield arrive(self.s_free[wg], n=4)
+            yield arrive(self.s_free[wg])
             yield wait(self.s_full[wg], ph, meant)
+            tp, to = self.tp[wg][q], self.to[wg][q]
 
-            def passes(who=who, it=it):
-                self.tp[wg].begin_read(who, ("S", it))
-                self.to[wg].begin_read(who, ("S", it))
-                self.to[wg].end_read(who)
-                self.tp[wg].end_read(who)
-                self.tp[wg].begin_write(who)
-                self.tp[wg].end_write(("P", it))
+            def passes(who=who, it=it, tp=tp, to=to):
+                tp.read(who, ("S", it))
+                to.read(who, ("S", it))
+                tp.write(who, ("P", it))
             yield call(passes)
-            yield arrive(self.p_full[wg], n=4)
-            # the warpgroup's issuer
-            yield wait(self.p_full[wg], ph, meant)
-            yield wait(self.full_v[it % K_VDEPTH], (it // K_VDEPTH) & 1, it // K_VDEPTH)
-            if self.mut.pv_waits_previous and it > 0:
-                # the span's older V rows came with earlier tiles, whose own
-                # waits this chain of O MMAs inherits
-                z = it - 1
-                yield wait(self.pv_done[z % K_VDEPTH], (z // K_VDEPTH) & 1, z // K_VDEPTH)
-            reads = [(self.tp[wg], ("P", it))] + [(self.vr[x], tag) for x, tag in g.span_slots(t)]
-            yield mma(reads, [(self.to[wg], ("O", it))], f"PV{it}",
-                      [self.o_full[wg], self.pv_done[it % K_VDEPTH]])
+            yield arrive(self.p_full[wg])
+            if q == 0:  # the warpgroup's issuer
+                yield wait(self.p_full[wg], ph, meant)
+                yield wait(self.full_v[it % K_VDEPTH], (it // K_VDEPTH) & 1, it // K_VDEPTH)
+                if self.mut.pv_waits_previous and it > 0:
+                    # the span's older V rows came with earlier tiles, whose own
+                    # waits this chain of O MMAs inherits
+                    z = it - 1
+                    yield wait(self.pv_done[z % K_VDEPTH], (z // K_VDEPTH) & 1, z // K_VDEPTH)
+                reads = [(b, ("P", it)) for b in self.tp[wg]] + \
+                        [(self.vr[x], tag) for x, tag in g.span_slots(t)]
+                yield mma(reads, [(b, ("O", it)) for b in self.to[wg]], f"PV{it}",
+                          [self.o_full[wg], self.pv_done[it % K_VDEPTH]])
             # epilogue
             yield wait(self.o_full[wg], ph, meant)
-
-            def read_o(who=who, it=it):
-                self.to[wg].begin_read(who + "epi", ("O", it))
-                self.to[wg].end_read(who + "epi")
-            yield call(read_o)
-            yield arrive(self.t_empty[wg], n=4)
+            yield call(lambda who=who, it=it, to=to: to.read(who + "epi", ("O", it)))
+            yield arrive(self.t_empty[wg])
 
     def run(self, seed: int):
-        return simulate({"copier": self.copier(), "masker": self.masker(),
-                         "mma": self.mma_warp(), "wg0": self.softmax(0),
-                         "wg1": self.softmax(1)}, seed)
+        roles = {"copier": self.copier(), "masker": self.masker(), "mma": self.mma_warp()}
+        for wg in range(2):
+            for q in range(4):
+                roles[f"wg{wg}.warp{q}"] = self.softmax_warp(wg, q)
+        return simulate(roles, seed)
 
 
 GEOMETRIES = {
