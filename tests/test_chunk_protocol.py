@@ -6,10 +6,11 @@ buffer handed between roles), restated for csrc/sa_tc_chunk.cu: producers
 loading each tile's Q rows and tokens into a Q stage and each 128-key chunk's
 K, V rows and key tokens into one of two chunk stages; one thread issuing S
 = Q K^T per half and chunk as soon as the chunk has landed and the half's
-previous O MMA has read P out of the S buffer; per half, a softmax
-warpgroup that reads the tile's query tokens, builds each chunk's masks from
-its key tokens, writes P, issues O += P V and reads O out after the tile's
-last chunk.  Geometries with one chunk per tile and one Q stage are
+previous O MMA has read P out of the S buffer; per half, four softmax
+warps (each its own actor, on its own TMEM lane quarter) that read the
+tile's query tokens, build each chunk's masks from its key tokens, correct
+O when a reference rises, write P and read O out after the tile's last
+chunk, warp 0's first lane issuing O += P V.  Geometries with one chunk per tile and one Q stage are
 included: there the tile's only S MMA can finish before the softmax has read
 the tile's tokens, so the Q stage must also wait for those reads.
 """
@@ -56,8 +57,9 @@ class ChunkModel:
         self.qtok = [Buffer(f"qtok{s}") for s in range(geo.qstages)]
         self.kv = [Buffer(f"KV{s}") for s in range(2)]
         self.csig = [Buffer(f"csig{s}") for s in range(2)]
-        self.s_buf = [Buffer(f"S/P{h}") for h in range(2)]
-        self.o_buf = [Accumulator(f"O{h}") for h in range(2)]
+        # per TMEM lane quarter (warp q of a half's warpgroup owns quarter q)
+        self.s_buf = [[Buffer(f"S/P{h}.{q}") for q in range(4)] for h in range(2)]
+        self.o_buf = [[Accumulator(f"O{h}.{q}") for q in range(4)] for h in range(2)]
 
     # ------------------------------------------------------------ roles
     def producers(self):
@@ -96,50 +98,56 @@ class ChunkModel:
                     yield wait(self.q_full[qs], z & 1, z)
                 commits = [self.s_full[h]] + ([self.q_free[qs]] if c == g.nch - 1 else [])
                 yield mma([(self.qrows[qs], x), (self.kv[call & 1], call)],
-                       [(self.s_buf[h], ("S", call))], f"QK{h}.{call}", commits)
+                          [(b, ("S", call)) for b in self.s_buf[h]], f"QK{h}.{call}", commits)
         return half(0), half(1)
 
-    def softmax(self, h):
+    def softmax_warp(self, h, q):
+        """Warp q of half h's softmax warpgroup; warp 0's first lane issues the
+        half's O MMAs.  A warp corrects O (after the previous O MMA) only on
+        chunks where one of its rows raised its reference: here on a fixed
+        pattern that differs between warps."""
         g = self.geo
-        who = f"softmax{h}"
+        who = f"softmax{h}.{q}"
+        sb, ob = self.s_buf[h][q], self.o_buf[h][q]
         for x in range(g.ntiles):
             qs = x % g.qstages
             z = x // g.qstages
             yield wait(self.q_full[qs], z & 1, z)
-            yield do(lambda qs=qs, x=x: (self.qtok[qs].begin_read(who, x),
-                                               self.qtok[qs].end_read(who)))
+            yield do(lambda qs=qs, x=x: self.qtok[qs].read(who, x))
             if self.mut.softmax_releases_q_stage:
-                yield arrive(self.q_free[qs], 4)
+                yield arrive(self.q_free[qs])
             for c in range(g.nch):
                 call = x * g.nch + c
                 b = call & 1
                 yield wait(self.c_full[b], (call >> 1) & 1, call >> 1)
-                yield do(lambda b=b, call=call: (self.csig[b].begin_read(who, call),
-                                                       self.csig[b].end_read(who)))
+                yield do(lambda b=b, call=call: self.csig[b].read(who, call))
                 yield wait(self.s_full[h], call & 1, call)
-                if c > 0:  # the O correction reads O once the previous O MMA is done
+                if c > 0 and (call + q) % 3 == 0:  # O correction
                     yield wait(self.pv_done[h], (call - 1) & 1, call - 1)
+                    yield do(lambda x=x: ob.read(who, ("O", x)))
 
                 def passes(call=call):
-                    self.s_buf[h].begin_read(who, ("S", call))
-                    self.s_buf[h].end_read(who)
-                    self.s_buf[h].begin_write(who)
-                    self.s_buf[h].end_write(("P", call))
+                    sb.read(who, ("S", call))
+                    sb.write(who, ("P", call))
                 yield do(passes)
-                yield arrive(self.p_full[h], 4)
-                yield wait(self.p_full[h], call & 1, call)
-                commits = [self.pv_done[h], self.c_free[b]] + \
-                          ([self.o_full[h]] if c == g.nch - 1 else [])
-                yield mma([(self.s_buf[h], ("P", call)), (self.kv[b], call)],
-                       [(self.o_buf[h], ("O", x), c == 0)], f"PV{h}.{call}", commits)
+                yield arrive(self.p_full[h])
+                if q == 0:  # the half's issuer
+                    yield wait(self.p_full[h], call & 1, call)
+                    commits = [self.pv_done[h], self.c_free[b]] + \
+                              ([self.o_full[h]] if c == g.nch - 1 else [])
+                    yield mma([(bb, ("P", call)) for bb in self.s_buf[h]] + [(self.kv[b], call)],
+                              [(ab, ("O", x), c == 0) for ab in self.o_buf[h]],
+                              f"PV{h}.{call}", commits)
             yield wait(self.o_full[h], x & 1, x)
-            yield do(lambda x=x: (self.o_buf[h].begin_read(who + "epi", ("O", x)),
-                                        self.o_buf[h].end_read(who + "epi")))
+            yield do(lambda x=x: ob.read(who + "epi", ("O", x)))
 
     def run(self, seed: int):
         m0, m1 = self.mma()
-        return simulate({"producers": self.producers(), "qk0": m0, "qk1": m1,
-                         "softmax0": self.softmax(0), "softmax1": self.softmax(1)}, seed)
+        roles = {"producers": self.producers(), "qk0": m0, "qk1": m1}
+        for h in range(2):
+            for q in range(4):
+                roles[f"softmax{h}.{q}"] = self.softmax_warp(h, q)
+        return simulate(roles, seed)
 
 
 GEOMETRIES = {
