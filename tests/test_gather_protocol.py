@@ -5,8 +5,8 @@ producer warp gathering a tile's sigma, Q, K and V rows into shared-memory
 stage it % S (the copies complete transaction bytes on the stage's full
 barrier); one thread issuing S = Q K^T into TMEM stage it % T and, one tile
 behind, O = P V into the same columns; softmax warpgroups taking tiles it %
-num_wg, reading S, writing P over the stage's dead Q and K bytes, and
-reading O out.  Every stage count the host picks (S in {1, 2}, T in 1..4,
+num_wg, each warp its own actor on its TMEM lane quarter, reading S,
+writing P over the stage's dead Q and K bytes, and reading O out.  Every stage count the host picks (S in {1, 2}, T in 1..4,
 two warpgroups only with S and T even) must be free of deadlock, phase
 aliasing and buffer races; planted mistakes must be caught, among them one
 of the kind behind the GPU fault of an early version (two warpgroups sharing
@@ -46,9 +46,11 @@ class GatherModel:
         self.ofull = [Barrier(f"ofull{t}", 1) for t in range(T)]
         self.tempty = [Barrier(f"tempty{t}", 4) for t in range(T)]
         self.sig = [Buffer(f"sigma{s}") for s in range(S)]
-        self.qk = [Buffer(f"QK/P{s}") for s in range(S)]   # Q and K rows, then P over them
+        # Q and K rows, then P over them (per quarter of the 128 rows)
+        self.qk = [[Buffer(f"QK/P{s}.{q}") for q in range(4)] for s in range(S)]
         self.v = [Buffer(f"V{s}") for s in range(S)]
-        self.tm = [Buffer(f"TMEM{t}") for t in range(T)]   # S, then O in the same columns
+        # S, then O in the same columns, per TMEM lane quarter
+        self.tm = [[Buffer(f"TMEM{t}.{q}") for q in range(4)] for t in range(T)]
 
     def producer(self):
         c = self.cfg
@@ -60,7 +62,7 @@ class GatherModel:
             yield do(lambda s=s, it=it: self.sig[s].write("producer", it))
             yield arrive(self.full[s], tx=2)
             yield do(lambda s=s, it=it: self.sig[s].read("producer", it))  # the gathers' rows
-            yield copy([(self.qk[s], ("QK", it))], f"gatherQK{it}", self.full[s], "tx")
+            yield copy([(b, ("QK", it)) for b in self.qk[s]], f"gatherQK{it}", self.full[s], "tx")
             yield copy([(self.v[s], it)], f"gatherV{it}", self.full[s], "tx")
 
     def mma_thread(self):
@@ -72,14 +74,14 @@ class GatherModel:
             yield wait(self.full[s], (it // S) & 1, it // S)
             if c.qk_waits_tempty:
                 yield wait(self.tempty[ts], ((it // T) & 1) ^ 1, it // T - 1)
-            yield mma([(self.qk[s], ("QK", it))], [(self.tm[ts], ("S", it))], f"QK{it}",
-                      [self.sfull[ts]])
+            yield mma([(b, ("QK", it)) for b in self.qk[s]], [(b, ("S", it)) for b in self.tm[ts]],
+                      f"QK{it}", [self.sfull[ts]])
 
         def pv(it):
             s, ts = it % S, it % T
             yield wait(self.pfull[s], (it // S) & 1, it // S)
-            yield mma([(self.qk[s], ("P", it)), (self.v[s], it)], [(self.tm[ts], ("O", it))],
-                      f"PV{it}", [self.ofull[ts], self.empty[s]])
+            yield mma([(b, ("P", it)) for b in self.qk[s]] + [(self.v[s], it)],
+                      [(b, ("O", it)) for b in self.tm[ts]], f"PV{it}", [self.ofull[ts], self.empty[s]])
 
         overlap = S >= 2 and T >= 2
         for it in range(c.ntiles):
@@ -91,10 +93,11 @@ class GatherModel:
         if c.ntiles > 0:
             yield from pv(c.ntiles - 1)
 
-    def softmax(self, wg):
+    def softmax_warp(self, wg, q):
+        """Warp q of softmax warpgroup wg: TMEM lane quarter q, rows 32q..."""
         c = self.cfg
         S, T = c.s_stages, c.t_stages
-        who = f"softmax{wg}"
+        who = f"softmax{wg}.{q}"
         for it in range(c.ntiles):
             if it % c.num_wg != wg:
                 continue
@@ -108,18 +111,19 @@ class GatherModel:
 
             def passes(s=s, ts=ts, it=it):
                 self.sig[s].read(who, it)
-                self.tm[ts].read(who, ("S", it))
-                self.qk[s].write(who, ("P", it))  # over the dead Q and K bytes
+                self.tm[ts][q].read(who, ("S", it))
+                self.qk[s][q].write(who, ("P", it))  # over the dead Q and K bytes
             yield do(passes)
-            yield arrive(self.pfull[s], n=4)
+            yield arrive(self.pfull[s])
             yield wait(self.ofull[ts], (it // T) & 1, it // T)
-            yield do(lambda ts=ts, it=it: self.tm[ts].read(who + "epi", ("O", it)))
-            yield arrive(self.tempty[ts], n=4)
+            yield do(lambda ts=ts, it=it: self.tm[ts][q].read(who + "epi", ("O", it)))
+            yield arrive(self.tempty[ts])
 
     def run(self, seed: int):
         roles = {"producer": self.producer(), "mma": self.mma_thread()}
         for wg in range(self.cfg.num_wg):
-            roles[f"softmax{wg}"] = self.softmax(wg)
+            for q in range(4):
+                roles[f"softmax{wg}.{q}"] = self.softmax_warp(wg, q)
         return simulate(roles, seed)
 
 
