@@ -146,8 +146,13 @@ def call(fn):
 def copy(writes, who: str, bar: Barrier, completes: str):
     """An asynchronous copy into `writes` [(buffer, tag)]; on landing it
     completes one transaction unit on `bar` ("tx") or arrives on it
-    ("arrive")."""
+    ("arrive"); with no barrier, only wait_copies sees it land."""
     return ("copy", writes, who, bar, completes)
+
+
+def wait_copies():
+    """cp.async.wait_all: passes once every copy issued so far has landed."""
+    return ("wait_copies",)
 
 
 def mma(reads, writes, who: str, commits):
@@ -171,6 +176,8 @@ def simulate(roles: dict, seed: int, max_steps: int = 400000) -> int:
 
     def runnable(name):
         a = nxt[name]
+        if a[0] == "wait_copies":
+            return not copies
         return a[0] != "wait" or a[1].passes(a[2])
 
     while nxt or copies or pipe:
@@ -187,14 +194,17 @@ def simulate(roles: dict, seed: int, max_steps: int = 400000) -> int:
             choices.append(("pipe", 0))
         if not choices:
             raise ProtocolError("deadlock: " + ", ".join(
-                f"{n} waits {a[1].name} parity {a[2]}" for n, a in nxt.items()))
+                f"{n} waits {a[1].name} parity {a[2]}" if a[0] == "wait" else f"{n}: {a[0]}"
+                for n, a in nxt.items()))
         weights = [speed[n] if k == "role" else speed[k] for k, n in choices]
         kind, key = rng.choices(choices, weights=weights)[0]
         if kind == "copy":
             writes, who, bar, completes = copies.pop(key)
             for buf, tag in writes:
                 buf.end_write(tag)
-            if completes == "tx":
+            if bar is None:  # a cp.async waited for with wait_copies
+                pass
+            elif completes == "tx":
                 bar.complete_tx(1)
             else:
                 bar.arrive()
