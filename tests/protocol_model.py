@@ -155,6 +155,18 @@ def wait_copies():
     return ("wait_copies",)
 
 
+def commit_group():
+    """cp.async.commit_group: closes the group the copies since the last
+    commit belong to (a group may be empty)."""
+    return ("commit_group",)
+
+
+def wait_group(n: int):
+    """cp.async.wait_group n: passes once at most the n newest committed
+    groups still have copies in flight."""
+    return ("wait_group", n)
+
+
 def mma(reads, writes, who: str, commits):
     """An MMA reading [(buffer, tag)] and writing [(buffer, tag)] or
     [(accumulator, tag, replace)], followed by commits to `commits`."""
@@ -172,12 +184,15 @@ def simulate(roles: dict, seed: int, max_steps: int = 400000) -> int:
         except StopIteration:
             pass
     copies, pipe = [], []
+    groups = 0  # cp.async groups committed so far (copies carry their group)
     steps = 0
 
     def runnable(name):
         a = nxt[name]
         if a[0] == "wait_copies":
             return not copies
+        if a[0] == "wait_group":
+            return all(cp[4] >= groups - a[1] for cp in copies)
         return a[0] != "wait" or a[1].passes(a[2])
 
     while nxt or copies or pipe:
@@ -199,7 +214,7 @@ def simulate(roles: dict, seed: int, max_steps: int = 400000) -> int:
         weights = [speed[n] if k == "role" else speed[k] for k, n in choices]
         kind, key = rng.choices(choices, weights=weights)[0]
         if kind == "copy":
-            writes, who, bar, completes = copies.pop(key)
+            writes, who, bar, completes, _ = copies.pop(key)
             for buf, tag in writes:
                 buf.end_write(tag)
             if bar is None:  # a cp.async waited for with wait_copies
@@ -237,7 +252,9 @@ def simulate(roles: dict, seed: int, max_steps: int = 400000) -> int:
             _, writes, who, bar, completes = a
             for buf, _ in writes:
                 buf.begin_write(who)
-            copies.append((writes, who, bar, completes))
+            copies.append((writes, who, bar, completes, groups))
+        elif a[0] == "commit_group":
+            groups += 1
         elif a[0] == "mma":
             _, reads, writes, who, commits = a
             for buf, tag in reads:
