@@ -1,4 +1,4 @@
-"""Model check of the backward query-tile kernel's operand pipeline (no GPU).
+"""Model check of the backward kernels' operand pipelines (no GPU).
 
 The model of tests/protocol_model.py restated for sa_bwd_dq_kernel in
 csrc/sa_bwd.cu.  The kernel's threads meet at CTA barriers, so they are one
@@ -8,9 +8,14 @@ tokens go to one of two buffers; Q, dY, K and V rows are gathered; S = Q K^T
 and dP = dY V^T run into TMEM; the next tile's tokens are written and its Q,
 dY and V rows gathered once those MMAs are done; three passes over TMEM
 write dS over S; dQ = dS K runs into the dP columns; the next tile's K rows
-are gathered once it is done; dQ is read out.  Planted mistakes (a gather
-issued before the MMA that reads its buffer is done, one token buffer, the
-wait for the copies left out) must be caught.
+are gathered once it is done; dQ is read out.  The key-tile kernel
+(sa_bwd_dkv_kernel) keeps a tile's K and V rows and walks its query chunks
+through two stages: chunk c + 1's tokens, Q and dY rows, lse2' and D are
+prepared into the other stage while chunk c is computed (S^T and dP^T into
+TMEM, the elementwise pass over them, dV and dK accumulated in TMEM).
+Planted mistakes (a gather issued before the MMA that reads its buffer is
+done, one token buffer, the wait for the copies left out, a chunk's second
+MMAs not waited for) must be caught.
 """
 
 from __future__ import annotations
@@ -19,8 +24,8 @@ from dataclasses import dataclass
 
 import pytest
 
-from protocol_model import (Barrier, Buffer, ProtocolError, copy, mma, simulate, wait,
-                            wait_copies)
+from protocol_model import (Accumulator, Barrier, Buffer, ProtocolError, commit_group, copy,
+                            mma, simulate, wait, wait_copies)
 from protocol_model import call as do
 
 
@@ -115,3 +120,94 @@ def test_planted_dq_pipeline_mistakes_are_caught(name):
         except ProtocolError:
             return
     pytest.fail(f"the model did not catch: {name}")
+
+
+@dataclass
+class DkvConfig:
+    ntiles: int
+    nchunks: int
+    waits_second_mmas: bool = True   # a chunk's dV / dK MMAs done before the next chunk
+
+
+class DkvModel:
+    def __init__(self, cfg: DkvConfig):
+        self.cfg = cfg
+        self.mma_bar = Barrier("mma", 1)
+        self.ktok = Buffer("ktok")
+        self.k, self.v = Buffer("K"), Buffer("V")
+        self.qtok = [Buffer(f"qtok{s}") for s in range(2)]
+        self.q = [Buffer(f"Q{s}") for s in range(2)]
+        self.dy = [Buffer(f"dY{s}") for s in range(2)]
+        self.col = [Buffer(f"lse/D{s}") for s in range(2)]
+        self.ts, self.tp = Buffer("TMEM.S^T"), Buffer("TMEM.dP^T")  # then P' and dS^T over them
+        self.dv, self.dk = Accumulator("TMEM.dV"), Accumulator("TMEM.dK")
+
+    def cta(self):
+        c = self.cfg
+        phase = 0
+        for x in range(c.ntiles):
+            yield do(lambda x=x: self.ktok.write("cta", x))
+            yield do(lambda x=x: self.ktok.read("gather", x))
+            yield copy([(self.k, x)], f"K{x}", None, "")
+            yield copy([(self.v, x)], f"V{x}", None, "")
+
+            def prepare(ch, x=x):
+                st = ch & 1
+                tag = (x, ch)
+                yield do(lambda: self.qtok[st].write("prepare", tag))
+                yield do(lambda: self.qtok[st].read("gather", tag))
+                yield copy([(self.q[st], tag)], f"Q{tag}", None, "")
+                yield copy([(self.dy[st], tag)], f"dY{tag}", None, "")
+                yield commit_group()
+                yield do(lambda: self.col[st].write("prepare", tag))
+            yield from prepare(0)
+            for ch in range(c.nchunks):
+                st, tag = ch & 1, (x, ch)
+                yield wait_copies()
+                if ch + 1 < c.nchunks:
+                    yield from prepare(ch + 1)
+                yield mma([(self.k, x), (self.q[st], tag), (self.v, x), (self.dy[st], tag)],
+                          [(self.ts, ("S", tag)), (self.tp, ("dP", tag))], f"SdP{tag}",
+                          [self.mma_bar])
+                yield wait(self.mma_bar, phase & 1, phase)
+                phase += 1
+
+                def elementwise(st=st, tag=tag):
+                    self.qtok[st].read("elementwise", tag)
+                    self.col[st].read("elementwise", tag)
+                    self.ts.read("elementwise", ("S", tag))
+                    self.tp.read("elementwise", ("dP", tag))
+                    self.ts.write("elementwise", ("P", tag))
+                    self.tp.write("elementwise", ("dS", tag))
+                yield do(elementwise)
+                yield mma([(self.ts, ("P", tag)), (self.dy[st], tag), (self.tp, ("dS", tag)),
+                           (self.q[st], tag)],
+                          [(self.dv, ("dV", x), ch == 0), (self.dk, ("dK", x), ch == 0)],
+                          f"dVdK{tag}", [self.mma_bar])
+                if c.waits_second_mmas:
+                    yield wait(self.mma_bar, phase & 1, phase)
+                phase += 1
+            if not c.waits_second_mmas:  # the last chunk's MMAs, at least
+                yield wait(self.mma_bar, (phase - 1) & 1, phase - 1)
+            yield do(lambda x=x: (self.dv.read("write-out", ("dV", x)),
+                                  self.dk.read("write-out", ("dK", x))))
+
+    def run(self, seed: int):
+        return simulate({"cta": self.cta()}, seed)
+
+
+def test_dkv_pipeline_has_no_race_or_deadlock():
+    for ntiles, nch in ((1, 1), (2, 3), (3, 9)):
+        for seed in range(200):
+            DkvModel(DkvConfig(ntiles=ntiles, nchunks=nch)).run(seed)
+
+
+def test_dkv_planted_mistake_is_caught():
+    """A chunk's dV / dK MMAs not waited for before the next chunk's S^T and
+    dP^T overwrite the TMEM columns they read."""
+    for seed in range(600):
+        try:
+            DkvModel(DkvConfig(ntiles=2, nchunks=4, waits_second_mmas=False)).run(seed)
+        except ProtocolError:
+            return
+    pytest.fail("the model did not catch the missing wait")
